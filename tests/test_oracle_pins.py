@@ -1,0 +1,304 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+* an independent float64 brute-force decoder with explicit loops (tests/brute_force.py);
+* torch's own pre-LN transformer layer (nn.TransformerEncoderLayer, norm_first=True,
+  ReLU, causal mask) in float64, and torch's layer_norm / logsumexp;
+* invariants the pages state: the incremental KV cache gives the same logits as a
+  full recompute; the LoRA-merged forward equals base + explicit low-rank branch;
+* closed forms and special cases: zero layer weights, constant LayerNorm input,
+  uniform attention, zero LoRA B factor, exact ties, log-prob identities;
+* mutation checks: plausible mistakes planted in the oracle (on the CPU) must
+  fail the brute-force pin.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import opt_oracle as oo
+from oracle.opt_oracle import OracleModel, layer_norm, log_softmax_pick, greedy, merge_lora
+from synth.workloads import WORKLOADS, OptConfig, make_model, make_prompts
+from tests.brute_force import BruteForce
+
+# A tiny model with large weights so that every term of the layer moves the logits.
+BF_CFG = OptConfig("bf-tiny", 9, 1, 8, 2, 32, 16, 16, "f32", 2, 5, 6, init_std=0.5,
+                   bias_std=0.3, ln_gamma_std=0.3, ln_beta_std=0.3)
+BF_CFG2 = BF_CFG.with_(name="bf-tiny-2l", index=10, n_layers=2, init_std=0.4)
+
+
+def _bf_case(cfg):
+    inputs = make_model(cfg)
+    prompts = make_prompts(cfg)
+    return inputs, prompts
+
+
+@pytest.mark.parametrize("cfg", [BF_CFG, BF_CFG2], ids=lambda c: c.name)
+def test_oracle_matches_fp64_brute_force(cfg):
+    inputs, prompts = _bf_case(cfg)
+    bf = BruteForce(inputs)
+    ids, lps, logged = OracleModel(inputs).generate(prompts, cfg.gen_len,
+                                                   log_steps=range(cfg.gen_len))
+    for b in range(cfg.batch):
+        bids, blps, brows = bf.generate(prompts[b], cfg.gen_len)
+        assert list(ids[b]) == bids
+        np.testing.assert_allclose(lps[b], blps, atol=1e-5, rtol=0)
+        for k in range(cfg.gen_len):
+            np.testing.assert_allclose(logged[k][b], brows[k], atol=1e-5, rtol=1e-5)
+
+
+def test_brute_force_pin_catches_planted_mistakes(monkeypatch):
+    """Each plausible slip below, planted in the oracle, must break the brute-force pin."""
+    inputs, prompts = _bf_case(BF_CFG)
+    bf = BruteForce(inputs)
+    _, ref_lps, ref_rows = bf.generate(prompts[0], BF_CFG.gen_len)
+    ref = np.array(ref_rows)
+
+    def deviation(model):
+        _, _, logged = model.generate(prompts[:1], BF_CFG.gen_len, log_steps=range(BF_CFG.gen_len))
+        return max(np.abs(logged[k][0] - ref[k]).max() for k in range(BF_CFG.gen_len))
+
+    assert deviation(OracleModel(inputs)) < 1e-5
+
+    class NoPosOffset(OracleModel):
+        def embed(self, ids, positions):
+            return self.tok_emb[ids] + self.pos_emb[positions]
+
+    assert deviation(NoPosOffset(inputs)) > 1e-3
+
+    def unbiased_ln(x, g, b, eps):
+        mean = x.mean(axis=-1, keepdims=True)
+        var = x.var(axis=-1, keepdims=True, ddof=1)
+        return (x - mean) / np.sqrt(var + eps) * g + b
+
+    with monkeypatch.context() as m:
+        m.setattr(oo, "layer_norm", unbiased_ln)
+        assert deviation(OracleModel(inputs)) > 1e-3
+
+    def lora_without_scale(w, a, b, alpha, r):
+        return oo.to_f32(w) + oo.to_f32(b) @ oo.to_f32(a)
+
+    with monkeypatch.context() as m:
+        m.setattr(oo, "merge_lora", lora_without_scale)
+        assert deviation(OracleModel(inputs)) > 1e-3
+
+    class TransposedLoRA(OracleModel):
+        def __init__(self, inp):
+            super().__init__(inp, "none")
+            s = np.float32(inp.cfg.lora_alpha / inp.cfg.lora_r)
+            for lw, fac in zip(self.layers, inp.lora):
+                for name in ("wq", "wk", "wv", "wo"):  # square ones: a transposed delta fits
+                    a, b = fac[name]
+                    lw[name] = lw[name] + s * (oo.to_f32(b) @ oo.to_f32(a)).T
+
+    assert deviation(TransposedLoRA(inputs)) > 1e-3
+
+    class NoBiasOnFc1(OracleModel):
+        def _proj(self, lw, name, x):
+            y = super()._proj(lw, name, x)
+            return y - lw["b1"] if name == "w1" else y
+
+    assert deviation(NoBiasOnFc1(inputs)) > 1e-3
+
+    class NoFinalLN(OracleModel):
+        def logits(self, x):
+            return x @ self.tok_emb.T
+
+    assert deviation(NoFinalLN(inputs)) > 1e-3
+
+
+def test_kv_cache_equals_full_recompute():
+    """Incremental decode (one token per pass over the cache) == one causal pass."""
+    for name in ("opt-tiny-fp32", "opt-tiny-fp32-bias"):
+        cfg = WORKLOADS[name]
+        inputs = make_model(cfg)
+        prompts = make_prompts(cfg)
+        model = OracleModel(inputs)
+        ids, _, logged = model.generate(prompts, cfg.gen_len, log_steps=range(cfg.gen_len))
+        seq = np.concatenate([prompts, ids[:, :-1]], axis=1)
+        full = model.full_logits(seq)
+        for k in range(cfg.gen_len):
+            row = full[:, cfg.prompt_len - 1 + k]
+            scale = np.abs(row).max()
+            np.testing.assert_allclose(logged[k], row, atol=1e-5 * scale, rtol=0)
+
+
+@pytest.mark.slow
+def test_kv_cache_equals_full_recompute_opt125m_one_sequence():
+    cfg = WORKLOADS["opt-125m"].with_(prompt_len=24, gen_len=8, batch=1)
+    inputs = make_model(cfg)
+    prompts = make_prompts(cfg)
+    model = OracleModel(inputs)
+    ids, _, logged = model.generate(prompts, cfg.gen_len, log_steps=range(cfg.gen_len))
+    full = model.full_logits(np.concatenate([prompts, ids[:, :-1]], axis=1))
+    for k in range(cfg.gen_len):
+        row = full[:, cfg.prompt_len - 1 + k]
+        np.testing.assert_allclose(logged[k], row, atol=1e-5 * np.abs(row).max(), rtol=0)
+
+
+def test_lora_merged_equals_unmerged_branch():
+    for name in ("opt-tiny-fp32", "opt-tiny-fp32-bias"):
+        cfg = WORKLOADS[name]
+        inputs = make_model(cfg)
+        prompts = make_prompts(cfg)
+        ids, lps_m, lg_m = OracleModel(inputs, "merged").generate(
+            prompts, cfg.gen_len, log_steps=range(cfg.gen_len))
+        _, lps_u, lg_u = OracleModel(inputs, "unmerged").generate(
+            prompts, cfg.gen_len, force_ids=ids, log_steps=range(cfg.gen_len))
+        np.testing.assert_allclose(lps_m, lps_u, atol=1e-5, rtol=0)
+        for k in lg_m:
+            np.testing.assert_allclose(lg_m[k], lg_u[k], atol=1e-5, rtol=0)
+        # and the LoRA delta is not negligible: the base model differs
+        _, _, lg_b = OracleModel(inputs, "none").generate(
+            prompts, cfg.gen_len, force_ids=ids, log_steps=range(cfg.gen_len))
+        assert max(np.abs(lg_m[k] - lg_b[k]).max() for k in lg_m) > 1e-4
+
+
+def test_lora_zero_b_leaves_weight_bits():
+    cfg = WORKLOADS["opt-125m"]
+    rng = np.random.default_rng(0)
+    w = rng.standard_normal((64, 48)).astype(np.float32)
+    a = rng.standard_normal((8, 48)).astype(np.float32)
+    b = np.zeros((64, 8), np.float32)
+    out = merge_lora(w, a, b, cfg.lora_alpha, cfg.lora_r)
+    assert out.tobytes() == w.tobytes()
+
+
+def test_lora_delta_rank_and_scale():
+    """B A has rank <= r and the update is exactly (alpha/r) times it (2 for 16/8)."""
+    rng = np.random.default_rng(1)
+    a = rng.standard_normal((8, 40)).astype(np.float32)
+    b = rng.standard_normal((30, 8)).astype(np.float32)
+    d = oo.lora_delta(a, b, 16.0, 8)
+    sv = np.linalg.svd(d.astype(np.float64), compute_uv=False)
+    assert sv[7] > 1e-2 * sv[0] and sv[8] < 1e-5 * sv[0]  # rank r up to fp32 rounding
+    np.testing.assert_allclose(d, 2.0 * (b.astype(np.float64) @ a.astype(np.float64)),
+                               rtol=1e-5, atol=1e-5)
+
+
+def _torch_layer(cfg, lw):
+    d = cfg.d_model
+    layer = torch.nn.TransformerEncoderLayer(d, cfg.n_heads, cfg.ffn, dropout=0.0,
+                                             activation="relu", layer_norm_eps=cfg.ln_eps,
+                                             batch_first=True, norm_first=True,
+                                             dtype=torch.float64)
+    t = lambda a: torch.tensor(np.asarray(a, np.float64))
+    with torch.no_grad():
+        layer.self_attn.in_proj_weight.copy_(torch.cat([t(lw["wq"]), t(lw["wk"]), t(lw["wv"])]))
+        layer.self_attn.in_proj_bias.copy_(torch.cat([t(lw["bq"]), t(lw["bk"]), t(lw["bv"])]))
+        layer.self_attn.out_proj.weight.copy_(t(lw["wo"]))
+        layer.self_attn.out_proj.bias.copy_(t(lw["bo"]))
+        layer.linear1.weight.copy_(t(lw["w1"]))
+        layer.linear1.bias.copy_(t(lw["b1"]))
+        layer.linear2.weight.copy_(t(lw["w2"]))
+        layer.linear2.bias.copy_(t(lw["b2"]))
+        layer.norm1.weight.copy_(t(lw["ln1_g"]))
+        layer.norm1.bias.copy_(t(lw["ln1_b"]))
+        layer.norm2.weight.copy_(t(lw["ln2_g"]))
+        layer.norm2.bias.copy_(t(lw["ln2_b"]))
+    return layer.eval()
+
+
+def test_layer_matches_torch_pre_ln_transformer_layer():
+    """One oracle layer == torch's pre-LN encoder layer with a causal mask (float64)."""
+    cfg = WORKLOADS["opt-tiny-fp32-bias"].with_(init_std=0.1)
+    inputs = make_model(cfg)
+    model = OracleModel(inputs)
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((2, 11, cfg.d_model)).astype(np.float32)
+    cache = model.new_cache(2, 11)
+    ours = model.layer(1, x.copy(), cache[1], 0)
+    layer = _torch_layer(cfg, model.layers[1])
+    mask = torch.nn.Transformer.generate_square_subsequent_mask(11, dtype=torch.float64)
+    with torch.no_grad():
+        ref = layer(torch.tensor(x, dtype=torch.float64), src_mask=mask, is_causal=True).numpy()
+    np.testing.assert_allclose(ours, ref, atol=2e-5, rtol=1e-5)
+    # the same layer fed one token at a time over the cache gives the same rows
+    cache2 = model.new_cache(2, 11)
+    rows = [model.layer(1, x[:, t:t + 1].copy(), cache2[1], t) for t in range(11)]
+    np.testing.assert_allclose(np.concatenate(rows, axis=1), ref, atol=2e-5, rtol=1e-5)
+
+
+def test_layer_norm_matches_torch_and_constant_rows():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 96)).astype(np.float32) * 3 + 1
+    g = rng.standard_normal(96).astype(np.float32)
+    b = rng.standard_normal(96).astype(np.float32)
+    ref = torch.nn.functional.layer_norm(torch.tensor(x, dtype=torch.float64), (96,),
+                                         torch.tensor(g, dtype=torch.float64),
+                                         torch.tensor(b, dtype=torch.float64), 1e-5).numpy()
+    np.testing.assert_allclose(layer_norm(x, g, b, 1e-5), ref, atol=2e-5, rtol=1e-5)
+    const = np.full((3, 96), 7.25, np.float32)
+    assert np.array_equal(layer_norm(const, g, b, 1e-5), np.broadcast_to(b, (3, 96)))
+
+
+def test_zero_layers_give_closed_form_logits():
+    """All layer weights and biases zero: logits = LN_f(E[id] + P[t+2]) E^T at every step."""
+    cfg = WORKLOADS["opt-tiny-fp32"]
+    inputs = make_model(cfg, with_lora=False)
+    for lw in inputs.layers:
+        for k in lw:
+            if k.startswith(("w", "b")):
+                lw[k] = np.zeros_like(lw[k])
+    prompts = make_prompts(cfg)
+    ids, lps, logged = OracleModel(inputs).generate(prompts, 4, log_steps=range(4))
+    E = torch.tensor(inputs.globals["tok_emb"], dtype=torch.float64)
+    P = torch.tensor(inputs.globals["pos_emb"], dtype=torch.float64)
+    for k in range(4):
+        tok = prompts[:, -1] if k == 0 else ids[:, k - 1]
+        pos = cfg.prompt_len - 1 + k
+        x = E[torch.tensor(tok, dtype=torch.long)] + P[pos + 2]
+        y = torch.nn.functional.layer_norm(x, (cfg.d_model,), eps=cfg.ln_eps)
+        ref = (y @ E.T).numpy()
+        np.testing.assert_allclose(logged[k], ref, atol=1e-5, rtol=0)
+        assert np.array_equal(ids[:, k], ref.argmax(-1))
+
+
+def test_uniform_attention_averages_values():
+    """W_q = 0, b_q = 0: every score is equal, so the context is the mean of v_0..v_t."""
+    cfg = WORKLOADS["opt-tiny-fp32-bias"]
+    inputs = make_model(cfg, with_lora=False)
+    lw0 = inputs.layers[0]
+    lw0["wq"] = np.zeros_like(lw0["wq"])
+    lw0["bq"] = np.zeros_like(lw0["bq"])
+    d = cfg.d_model
+    lw0["wo"] = np.eye(d, dtype=np.float32)
+    for k in ("bo", "w1", "b1", "w2", "b2"):
+        lw0[k] = np.zeros_like(lw0[k])
+    model = OracleModel(inputs)
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((1, 9, d)).astype(np.float32)
+    out = model.layer(0, x.copy(), model.new_cache(1, 9)[0], 0)
+    X = torch.tensor(x[0], dtype=torch.float64)
+    h = torch.nn.functional.layer_norm(X, (d,), torch.tensor(lw0["ln1_g"], dtype=torch.float64),
+                                       torch.tensor(lw0["ln1_b"], dtype=torch.float64), cfg.ln_eps)
+    v = h @ torch.tensor(lw0["wv"], dtype=torch.float64).T + torch.tensor(lw0["bv"], dtype=torch.float64)
+    mean_v = torch.cumsum(v, 0) / torch.arange(1, 10, dtype=torch.float64)[:, None]
+    np.testing.assert_allclose(out[0], (X + mean_v).numpy(), atol=1e-5, rtol=1e-5)
+
+
+def test_greedy_lowest_index_on_exact_ties():
+    lg = np.array([[0.5, 2.0, -1.0, 2.0, 2.0], [3.0, 3.0, 3.0, 3.0, 3.0]], np.float32)
+    assert list(greedy(lg)) == [1, 0]
+
+
+def test_logprob_identities():
+    cfg = WORKLOADS["opt-tiny-fp32-bias"]
+    inputs = make_model(cfg)
+    prompts = make_prompts(cfg)
+    ids, lps, logged = OracleModel(inputs).generate(prompts, cfg.gen_len,
+                                                   log_steps=range(cfg.gen_len))
+    assert (lps <= 0).all()
+    for k, lg in logged.items():
+        t = torch.tensor(lg, dtype=torch.float64)
+        lse = torch.logsumexp(t, -1)
+        np.testing.assert_allclose(lps[:, k], (t.max(-1).values - lse).numpy(), atol=1e-5)
+        # greedy: log-prob of the chosen token = -log sum exp(l - l_max)
+        np.testing.assert_allclose(
+            lps[:, k], -np.log(np.exp((t - t.max(-1, keepdim=True).values).numpy()).sum(-1)),
+            atol=1e-5)
+    # a forced token that is not the argmax has a strictly smaller log-prob
+    lg = np.array([[0.0, 1.0, 2.0]], np.float32)
+    assert log_softmax_pick(lg, np.array([0]))[0] < log_softmax_pick(lg, np.array([2]))[0]
+    assert math.isclose(float(log_softmax_pick(lg, np.array([2]))[0]),
+                        2.0 - math.log(1 + math.e + math.e ** 2), abs_tol=1e-6)
