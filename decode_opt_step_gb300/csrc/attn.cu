@@ -1,0 +1,316 @@
+// Attention over the KV cache.
+//
+// Decode: one query per (sequence, head) against keys 0..n-1.  The cache rows of
+// one (b, h) are contiguous ([max_seq][hd]), so a group of hd*sizeof(T)/16 lanes
+// reads one key (or value) row with 16-byte loads; the CTA's groups walk the keys
+// in an interleaved order, several keys in flight per group, with an online
+// (running max) softmax per group, and the groups are merged at the end.  Long
+// contexts with few (b, h) pairs are split over the sequence; the slices are
+// merged by a second small kernel (no inter-CTA waiting).
+//
+// Prefill: causal attention inside each prompt, 64 queries per CTA, key blocks
+// of 64 staged in shared memory, online softmax across key blocks (CUDA cores).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace he {
+
+namespace {
+
+template <typename T> struct Vec16;
+template <> struct Vec16<bf16> {
+  static constexpr int N = 8;
+  __device__ static void load(const bf16 *p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float *p, float (&v)[4]) {
+    const float4 u = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = u.x;
+    v[1] = u.y;
+    v[2] = u.z;
+    v[3] = u.w;
+  }
+};
+
+template <typename T, int HD, int UNROLL>
+__global__ void __launch_bounds__(128)
+    k_attn_decode(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
+                  T *__restrict__ ctx, int H, int max_seq, int n_keys, int per_split,
+                  float *__restrict__ part) {
+  constexpr int VEC = Vec16<T>::N;
+  constexpr int LPK = HD / VEC;       // lanes per key row
+  constexpr int GROUPS = 128 / LPK;   // key groups per CTA
+  static_assert(LPK <= 32 && (32 % LPK) == 0, "a key row must fit in a warp");
+  __shared__ float s_m[GROUPS], s_l[GROUPS];
+  __shared__ float s_o[GROUPS][HD];
+
+  const int bh = blockIdx.x, sidx = blockIdx.y, nsplit = gridDim.y;
+  const int b = bh / H, h = bh - b * H;
+  const int j0 = sidx * per_split, j1 = min(n_keys, j0 + per_split);
+  const int g = threadIdx.x / LPK, li = threadIdx.x % LPK;
+  const long long row0 = ((long long)b * H + h) * max_seq;
+  const T *kb = kc + row0 * HD + li * VEC;
+  const T *vb = vc + row0 * HD + li * VEC;
+
+  float qv[VEC];
+  Vec16<T>::load(q + ((long long)b * H + h) * HD + li * VEC, qv);
+  float m = -INFINITY, l = 0.f, o[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) o[i] = 0.f;
+
+  for (int base = j0; base < j1; base += GROUPS * UNROLL) {
+    float kv[UNROLL][VEC], vv[UNROLL][VEC], s[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int j = base + u * GROUPS + g;
+      if (j < j1) {
+        Vec16<T>::load(kb + (long long)j * HD, kv[u]);
+        Vec16<T>::load(vb + (long long)j * HD, vv[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) kv[u][i] = vv[u][i] = 0.f;
+      }
+    }
+    float mb = m;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) d = fmaf(qv[i], kv[u][i], d);
+#pragma unroll
+      for (int o2 = LPK / 2; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
+      const int j = base + u * GROUPS + g;
+      s[u] = j < j1 ? d : -INFINITY;
+      mb = fmaxf(mb, s[u]);
+    }
+    if (mb == -INFINITY) continue;  // no key of this group in this round
+    const float corr = expf(m - mb);
+    l *= corr;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] *= corr;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const float p = expf(s[u] - mb);
+      l += p;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) o[i] = fmaf(p, vv[u][i], o[i]);
+    }
+    m = mb;
+  }
+  if (li == 0) {
+    s_m[g] = m;
+    s_l[g] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) s_o[g][li * VEC + i] = o[i];
+  __syncthreads();
+  if (threadIdx.x < HD) {
+    const int dd = threadIdx.x;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < GROUPS; ++k) M = fmaxf(M, s_m[k]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int k = 0; k < GROUPS; ++k) {
+      const float w = s_m[k] == -INFINITY ? 0.f : expf(s_m[k] - M);
+      L = fmaf(s_l[k], w, L);
+      O = fmaf(s_o[k][dd], w, O);
+    }
+    if (nsplit == 1) {
+      ctx[((long long)b * H + h) * HD + dd] = from_f<T>(O / L);
+    } else {
+      float *pp = part + ((long long)bh * nsplit + sidx) * (HD + 2);
+      pp[dd] = O;
+      if (dd == 0) {
+        pp[HD] = M;
+        pp[HD + 1] = L;
+      }
+    }
+  }
+}
+
+template <typename T, int HD>
+__global__ void k_attn_combine(const float *__restrict__ part, T *__restrict__ ctx, int H,
+                               int nsplit) {
+  const int bh = blockIdx.x, dd = threadIdx.x;
+  const float *pp = part + (long long)bh * nsplit * (HD + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[s * (HD + 2) + HD]);
+  float L = 0.f, O = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float ms = pp[s * (HD + 2) + HD];
+    const float w = ms == -INFINITY ? 0.f : expf(ms - M);
+    L = fmaf(pp[s * (HD + 2) + HD + 1], w, L);
+    O = fmaf(pp[s * (HD + 2) + dd], w, O);
+  }
+  ctx[(long long)bh * HD + dd] = from_f<T>(O / L);
+}
+
+// ---------------------------------------------------------------------------
+// Prefill (causal) attention.  Thread (query qi, part p) of 256: scores of keys
+// p*16..p*16+15 of the current key block, output dims p*HD/4..(p+1)*HD/4.
+// ---------------------------------------------------------------------------
+template <typename T, int HD>
+__global__ void __launch_bounds__(256)
+    k_attn_prefill(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
+                   T *__restrict__ ctx, int H, int Lp, int max_seq) {
+  constexpr int QB = 64, KB = 64, LD = HD + 1, DP = HD / 4;
+  extern __shared__ float sm[];
+  float *qs = sm;               // [QB][LD]
+  float *ks = qs + QB * LD;     // [KB][LD]
+  float *vs = ks + KB * LD;     // [KB][LD]
+  float *ps = vs + KB * LD;     // [QB][KB + 1]
+  const int qb = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / H, h = bh - b * H;
+  const int d = H * HD;
+  const int qi = threadIdx.x >> 2, p = threadIdx.x & 3;
+  const int t_q = qb * QB + qi;  // query position
+  const long long row0 = ((long long)b * H + h) * max_seq;
+
+  for (int e = threadIdx.x; e < QB * HD; e += 256) {
+    const int r = e / HD, c = e - r * HD, t = qb * QB + r;
+    qs[r * LD + c] = t < Lp ? to_f<T>(q[((long long)b * Lp + t) * d + h * HD + c]) : 0.f;
+  }
+  float m = -INFINITY, l = 0.f, o[DP];
+#pragma unroll
+  for (int i = 0; i < DP; ++i) o[i] = 0.f;
+
+  for (int kb = 0; kb <= qb; ++kb) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < KB * HD; e += 256) {
+      const int r = e / HD, c = e - r * HD, t = kb * KB + r;
+      const bool in = t < Lp;
+      ks[r * LD + c] = in ? to_f<T>(kc[(row0 + t) * HD + c]) : 0.f;
+      vs[r * LD + c] = in ? to_f<T>(vc[(row0 + t) * HD + c]) : 0.f;
+    }
+    __syncthreads();
+    float s[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) s[jj] = 0.f;
+    for (int c = 0; c < HD; ++c) {
+      const float qv = qs[qi * LD + c];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) s[jj] = fmaf(qv, ks[(p * 16 + jj) * LD + c], s[jj]);
+    }
+    float mb = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int t_k = kb * KB + p * 16 + jj;
+      if (t_k > t_q) s[jj] = -INFINITY;
+      mb = fmaxf(mb, s[jj]);
+    }
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const float mn = fmaxf(m, mb);  // finite: key 0 <= every query position
+    const float corr = expf(m - mn);
+    float rs = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const float pj = expf(s[jj] - mn);
+      rs += pj;
+      ps[qi * (KB + 1) + p * 16 + jj] = pj;
+    }
+    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+    l = l * corr + rs;
+    m = mn;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < DP; ++i) o[i] *= corr;
+    for (int j = 0; j < KB; ++j) {
+      const float pj = ps[qi * (KB + 1) + j];
+#pragma unroll
+      for (int i = 0; i < DP; ++i) o[i] = fmaf(pj, vs[j * LD + p * DP + i], o[i]);
+    }
+  }
+  if (t_q < Lp) {
+    T *out = ctx + ((long long)b * Lp + t_q) * d + h * HD + p * DP;
+#pragma unroll
+    for (int i = 0; i < DP; ++i) out[i] = from_f<T>(o[i] / l);
+  }
+}
+
+template <typename T, int HD>
+cudaError_t decode_t(const void *q, const void *kc, const void *vc, void *ctx, int B, int H,
+                     int max_seq, int n_keys, int split, float *part, cudaStream_t st) {
+  const int per = (n_keys + split - 1) / split;
+  const int ns = (n_keys + per - 1) / per;
+  if (ns > 1 && !part) return cudaErrorInvalidValue;
+  dim3 grid(B * H, ns);
+  k_attn_decode<T, HD, 4><<<grid, 128, 0, st>>>((const T *)q, (const T *)kc, (const T *)vc,
+                                                (T *)ctx, H, max_seq, n_keys, per, part);
+  if (ns > 1) k_attn_combine<T, HD><<<B * H, HD, 0, st>>>(part, (T *)ctx, H, ns);
+  return cudaGetLastError();
+}
+
+template <typename T, int HD>
+cudaError_t prefill_t(const void *q, const void *kc, const void *vc, void *ctx, int B, int Lp,
+                      int H, int max_seq, cudaStream_t st) {
+  constexpr int LD = HD + 1;
+  const size_t sm = (size_t)(64 * LD * 3 + 64 * 65) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<T, HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((Lp + 63) / 64, B * H);
+  k_attn_prefill<T, HD><<<grid, 256, sm, st>>>((const T *)q, (const T *)kc, (const T *)vc,
+                                               (T *)ctx, H, Lp, max_seq);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_decode_pick_split(int B, int H, int n_keys, int num_sms) {
+  // Enough CTAs for several per SM; no slice shorter than 64 keys.
+  const int pairs = B * H;
+  int s = 1;
+  while (pairs * s < 4 * num_sms && n_keys / (2 * s) >= 64 && s < 32) s *= 2;
+  const int per = (n_keys + s - 1) / s;
+  return (n_keys + per - 1) / per;
+}
+
+cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
+                               void *ctx, int B, int H, int hd, int max_seq, int n_keys,
+                               int split, float *part, cudaStream_t st) {
+  if (n_keys <= 0 || split < 1) return cudaErrorInvalidValue;
+  if (dtype == 1) {
+    if (hd == 128) return decode_t<bf16, 128>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 64) return decode_t<bf16, 64>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 32) return decode_t<bf16, 32>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+  } else {
+    if (hd == 128) return decode_t<float, 128>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 64) return decode_t<float, 64>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 32) return decode_t<float, 32>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const void *vc,
+                                void *ctx, int B, int Lp, int H, int hd, int max_seq,
+                                cudaStream_t st) {
+  if (dtype == 1) {
+    if (hd == 128) return prefill_t<bf16, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 64) return prefill_t<bf16, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 32) return prefill_t<bf16, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+  } else {
+    if (hd == 128) return prefill_t<float, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 64) return prefill_t<float, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 32) return prefill_t<float, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace he

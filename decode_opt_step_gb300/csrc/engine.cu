@@ -1,0 +1,824 @@
+// libhe: engine state, workspace, and the launch sequence of one generation.
+//
+// Host C++ only (kernels live in gemm_tc.cu, gemm_simt.cu, attn.cu, rows.cu).
+// The engine records the caller's weight pointers (one model instance), owns a
+// workspace taken through the caller's allocator (KV cache + activations), and
+// enqueues every step of generation on the caller's stream.  No host
+// synchronisation happens inside he_generate: the token chosen at step k is
+// embedded on the device by the head kernel for step k + 1.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/he.h"
+#include "../../include/he_ops.h"
+#include "kernels.h"
+
+using namespace he;
+
+namespace {
+
+thread_local std::string g_err;
+
+he_status fail(he_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+void *default_alloc(size_t bytes, void *, void *) {
+  void *p = nullptr;
+  return cudaMalloc(&p, bytes) == cudaSuccess ? p : nullptr;
+}
+void default_free(void *p, size_t, void *, void *) { cudaFree(p); }
+
+struct Buf {
+  void *p = nullptr;
+  size_t bytes = 0;
+};
+
+constexpr int kMaxGemmSplit = 16;
+constexpr int kMaxAttnSplit = 32;
+constexpr int kClasses = 8;
+
+}  // namespace
+
+struct he_engine {
+  he_config cfg{};
+  int device = 0, num_sms = 0;
+  size_t elem = 4;
+  const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_g = nullptr, *lnf_b = nullptr;
+  std::vector<he_layer_weights> layers;
+  he_allocator alloc{};
+
+  bool taken = false, fused = false, profiling = false;
+  // workspace (released / retaken together)
+  Buf kc, vc, x, h, q, ctx, mid, partial, logits, attn_part, ids_in, ids_out, lp_out, logmap;
+  // held for the engine's lifetime
+  Buf err;
+  // LoRA restore copy (held while fused)
+  Buf restore;
+
+  he_stats stats{};
+  cudaEvent_t ph[6] = {};  // fuse begin/end ... (lazily created)
+  struct Pair { cudaEvent_t a, b; };
+  std::vector<Pair> prof_pool[kClasses];
+  size_t prof_used[kClasses] = {};
+  bool stats_pending = false, fuse_pending = false, unfuse_pending = false;
+
+  size_t kv_layer_elems() const {
+    return (size_t)cfg.max_batch * cfg.n_heads * cfg.max_seq * (cfg.d_model / cfg.n_heads);
+  }
+};
+
+namespace {
+
+he_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(HE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool get(he_engine *h, Buf &b, size_t bytes, cudaStream_t st) {
+  b.bytes = bytes;
+  b.p = bytes ? h->alloc.alloc(bytes, st, h->alloc.ctx) : nullptr;
+  if (bytes && !b.p) {
+    b.bytes = 0;
+    return false;
+  }
+  return true;
+}
+
+void put(he_engine *h, Buf &b, cudaStream_t st) {
+  if (b.p) h->alloc.free(b.p, b.bytes, st, h->alloc.ctx);
+  b.p = nullptr;
+  b.bytes = 0;
+}
+
+void free_workspace(he_engine *h, cudaStream_t st) {
+  Buf *all[] = {&h->kc, &h->vc, &h->x, &h->h, &h->q, &h->ctx, &h->mid, &h->partial,
+                &h->logits, &h->attn_part, &h->ids_in, &h->ids_out, &h->lp_out, &h->logmap};
+  for (Buf *b : all) put(h, *b, st);
+  h->taken = false;
+  h->stats.workspace_bytes = 0;
+  h->stats.kv_bytes = 0;
+}
+
+he_status take_workspace(he_engine *h, cudaStream_t st) {
+  const he_config &c = h->cfg;
+  const size_t e = h->elem, hd = c.d_model / c.n_heads;
+  const size_t max_tok = (size_t)c.max_batch * c.max_seq;
+  const size_t kv = (size_t)c.n_layers * h->kv_layer_elems() * e;
+  const size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
+  size_t part = max_tok * c.d_model;
+  if ((size_t)kMaxGemmSplit * c.max_batch * wide > part) part = (size_t)kMaxGemmSplit * c.max_batch * wide;
+  struct {
+    Buf *b;
+    size_t bytes;
+  } want[] = {
+      {&h->kc, kv},
+      {&h->vc, kv},
+      {&h->x, max_tok * c.d_model * 4},
+      {&h->h, max_tok * c.d_model * e},
+      {&h->q, max_tok * c.d_model * e},
+      {&h->ctx, max_tok * c.d_model * e},
+      {&h->mid, max_tok * c.ffn * e},
+      {&h->partial, part * 4},
+      {&h->logits, (size_t)c.max_batch * c.vocab * 4},
+      {&h->attn_part, (size_t)c.max_batch * c.n_heads * kMaxAttnSplit * (hd + 2) * 4},
+      {&h->ids_in, max_tok * 4},
+      {&h->ids_out, max_tok * 4},
+      {&h->lp_out, max_tok * 4},
+      {&h->logmap, max_tok * 4},
+  };
+  size_t total = 0;
+  for (auto &w : want) {
+    if (!get(h, *w.b, w.bytes, st)) {
+      free_workspace(h, st);
+      return fail(HE_ERR_OOM, "workspace allocation of %zu bytes failed", w.bytes);
+    }
+    total += w.bytes;
+  }
+  h->taken = true;
+  h->stats.workspace_bytes = total;
+  h->stats.kv_bytes = 2 * kv;
+  return HE_OK;
+}
+
+// ---- profiling helpers -----------------------------------------------------
+struct Timed {
+  he_engine *h;
+  int cls;
+  cudaStream_t st;
+  he_engine::Pair *p = nullptr;
+  Timed(he_engine *h_, int c, cudaStream_t s) : h(h_), cls(c), st(s) {
+    if (!h->profiling) return;
+    auto &pool = h->prof_pool[cls];
+    if (h->prof_used[cls] == pool.size()) {
+      he_engine::Pair np{};
+      cudaEventCreate(&np.a);
+      cudaEventCreate(&np.b);
+      pool.push_back(np);
+    }
+    p = &pool[h->prof_used[cls]++];
+    cudaEventRecord(p->a, st);
+  }
+  ~Timed() {
+    if (p) cudaEventRecord(p->b, st);
+  }
+};
+
+void ensure_phase_events(he_engine *h) {
+  if (!h->ph[0])
+    for (auto &e : h->ph) cudaEventCreate(&e);
+}
+
+// ---- the generation sequence -------------------------------------------------
+struct Ctx {
+  he_engine *h;
+  cudaStream_t st;
+  cudaError_t e = cudaSuccess;
+  void check(cudaError_t r, int launches) {
+    if (e == cudaSuccess && r != cudaSuccess) e = r;
+    h->stats.launches += launches;
+  }
+};
+
+inline const char *at(const void *p, size_t off) { return static_cast<const char *>(p) + off; }
+inline char *at(void *p, size_t off) { return static_cast<char *>(p) + off; }
+
+// GEMM (+ split-K reduction for element-wise epilogues).
+void gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
+          int group_rows, int M, int K, Epi epi, bool allow_split) {
+  he_engine *h = c.h;
+  GemmArgs a{};
+  a.dtype = h->cfg.dtype;
+  a.x = x;
+  a.ldx = ldx;
+  for (int g = 0; g < n_groups; ++g) a.w[g] = w[g];
+  a.n_groups = n_groups;
+  a.group_rows = group_rows;
+  a.M = M;
+  a.N = n_groups * group_rows;
+  a.K = K;
+  int split = allow_split ? gemm_pick_split(a, h->num_sms) : 1;
+  if (split > kMaxGemmSplit) split = kMaxGemmSplit;
+  split = effective_split(K, split);
+  a.split = split;
+  const bool via_partial = split > 1 && epi.kind != EPI_PARTIAL;
+  if (via_partial) {
+    Epi pe = epi;
+    pe.kind = EPI_PARTIAL;
+    pe.partial = static_cast<float *>(h->partial.p);
+    pe.ldp = a.N;
+    pe.split_stride = (long long)M * a.N;
+    a.epi = pe;
+  } else {
+    a.epi = epi;
+    if (epi.kind == EPI_PARTIAL) a.epi.split_stride = (long long)M * epi.ldp;
+  }
+  {
+    Timed t(h, cls, c.st);
+    c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+    if (via_partial)
+      c.check(launch_reduce_epi(h->cfg.dtype, static_cast<float *>(h->partial.p), split,
+                                (long long)M * a.N, a.N, M, a.N, epi, c.st),
+              1);
+  }
+}
+
+// Returns the split used for an EPI_PARTIAL GEMM (the row kernel must know it).
+int gemm_partial(Ctx &c, int cls, const void *x, int ldx, const void *w, int N, int M, int K,
+                 bool allow_split) {
+  he_engine *h = c.h;
+  GemmArgs a{};
+  a.dtype = h->cfg.dtype;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  int split = allow_split ? gemm_pick_split(a, h->num_sms) : 1;
+  if (split > kMaxGemmSplit) split = kMaxGemmSplit;
+  split = effective_split(K, split);
+  Epi e{};
+  e.kind = EPI_PARTIAL;
+  e.partial = static_cast<float *>(h->partial.p);
+  e.ldp = N;
+  a.x = x;
+  a.ldx = ldx;
+  a.w[0] = w;
+  a.n_groups = 1;
+  a.group_rows = N;
+  a.split = split;
+  a.epi = e;
+  a.epi.split_stride = (long long)M * N;
+  Timed t(h, cls, c.st);
+  c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+  return split;
+}
+
+Epi qkv_epi(he_engine *h, int layer, int tok_per_seq, int pos0) {
+  const he_config &c = h->cfg;
+  const he_layer_weights &lw = h->layers[layer];
+  Epi e{};
+  e.kind = EPI_QKV;
+  e.bias[0] = lw.b[HE_PROJ_Q];
+  e.bias[1] = lw.b[HE_PROJ_K];
+  e.bias[2] = lw.b[HE_PROJ_V];
+  e.out = h->q.p;
+  e.ldo = c.d_model;
+  const size_t lay = (size_t)layer * h->kv_layer_elems() * h->elem;
+  e.kc = at(h->kc.p, lay);
+  e.vc = at(h->vc.p, lay);
+  e.d_model = c.d_model;
+  e.n_heads = c.n_heads;
+  e.head_dim = c.d_model / c.n_heads;
+  e.max_seq = c.max_seq;
+  e.tok_per_seq = tok_per_seq;
+  e.pos0 = pos0;
+  e.q_scale = 1.0f / sqrtf((float)e.head_dim);
+  return e;
+}
+
+// One decoder layer over M tokens (prefill: M = B*Lp, tok_per_seq = Lp, pos0 = 0;
+// decode: M = B, tok_per_seq = 1, pos0 = t).  Input h = LN1(x); output h = LN1 of
+// the next layer (or the final LN after the last layer).
+void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool prefill) {
+  he_engine *h = c.h;
+  const he_config &cf = h->cfg;
+  const he_layer_weights &lw = h->layers[l];
+  const int d = cf.d_model, hd = d / cf.n_heads;
+  const int cls_g = prefill ? HE_KCLASS_PREFILL_GEMM : HE_KCLASS_GEMM;
+  const bool dec = !prefill;
+  // LN1 + QKV (+ KV append at the tokens' positions)
+  const void *wqkv[3] = {lw.w[HE_PROJ_Q], lw.w[HE_PROJ_K], lw.w[HE_PROJ_V]};
+  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec);
+  // attention
+  const size_t lay = (size_t)l * h->kv_layer_elems() * h->elem;
+  if (prefill) {
+    Timed t(h, HE_KCLASS_PREFILL_ATTN, c.st);
+    c.check(launch_attn_prefill(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
+                                tok_per_seq, cf.n_heads, hd, cf.max_seq, c.st),
+            1);
+  } else {
+    const int n_keys = pos0 + 1;
+    int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
+    if (split > kMaxAttnSplit) split = kMaxAttnSplit;
+    Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
+    c.check(launch_attn_decode(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
+                               cf.n_heads, hd, cf.max_seq, n_keys, split,
+                               static_cast<float *>(h->attn_part.p), c.st),
+            split > 1 ? 2 : 1);
+  }
+  // out projection -> partials; + bo + residual; LN2
+  int s = gemm_partial(c, cls_g, h->ctx.p, d, lw.w[HE_PROJ_O], d, M, d, dec);
+  {
+    Timed t(h, HE_KCLASS_NORM, c.st);
+    c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), s, (long long)M * d, d,
+                            lw.b[HE_PROJ_O], static_cast<float *>(h->x.p), lw.ln2_g, lw.ln2_b,
+                            cf.ln_eps, h->h.p, M, d, c.st),
+            1);
+  }
+  // fc1 + b1 + ReLU
+  Epi er{};
+  er.kind = EPI_RELU;
+  er.bias[0] = lw.b[HE_PROJ_FC1];
+  er.out = h->mid.p;
+  er.ldo = cf.ffn;
+  const void *w1[1] = {lw.w[HE_PROJ_FC1]};
+  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec);
+  // fc2 -> partials; + b2 + residual; next LN
+  s = gemm_partial(c, cls_g, h->mid.p, cf.ffn, lw.w[HE_PROJ_FC2], d, M, cf.ffn, dec);
+  const bool last = l == cf.n_layers - 1;
+  const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
+  const void *bb = last ? h->lnf_b : h->layers[l + 1].ln1_b;
+  Timed t(h, HE_KCLASS_NORM, c.st);
+  c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), s, (long long)M * d, d,
+                          lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
+                          h->h.p, M, d, c.st),
+          1);
+}
+
+// LM head over B rows of h (row stride ldh elements) + greedy select for step k.
+void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
+          const int32_t *force, int32_t *out_ids, float *out_lp, const int32_t *log_map,
+          float *logits_out) {
+  he_engine *h = c.h;
+  const he_config &cf = h->cfg;
+  Timed t(h, HE_KCLASS_HEAD, c.st);
+  GemmArgs a{};
+  a.dtype = cf.dtype;
+  a.x = hrows;
+  a.ldx = ldh;
+  a.w[0] = h->tok_emb;
+  a.n_groups = 1;
+  a.group_rows = cf.vocab;
+  a.M = B;
+  a.N = cf.vocab;
+  a.K = cf.d_model;
+  a.split = 1;
+  a.epi.kind = EPI_STORE_F32;
+  a.epi.partial = static_cast<float *>(h->logits.p);
+  a.epi.ldp = cf.vocab;
+  c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+  HeadArgs ha{};
+  ha.logits = static_cast<float *>(h->logits.p);
+  ha.ldl = cf.vocab;
+  ha.vocab = cf.vocab;
+  ha.B = B;
+  ha.step = step;
+  ha.gen_len = Lgen;
+  ha.force_ids = force;
+  ha.out_ids = out_ids;
+  ha.out_lp = out_lp;
+  ha.log_map = log_map;
+  ha.logits_out = logits_out;
+  ha.embed_next = step + 1 < Lgen;
+  ha.pos = Lp + step;  // position of the token emitted at this step
+  ha.tok_emb = h->tok_emb;
+  ha.pos_emb = h->pos_emb;
+  ha.pos_offset = cf.pos_offset;
+  ha.g = h->layers[0].ln1_g;
+  ha.b = h->layers[0].ln1_b;
+  ha.eps = cf.ln_eps;
+  ha.x = static_cast<float *>(h->x.p);
+  ha.h = h->h.p;
+  ha.d = cf.d_model;
+  c.check(launch_head_select(cf.dtype, ha, c.st), 1);
+}
+
+he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int Lgen,
+                        int32_t *out_ids, float *out_lp, const int32_t *force,
+                        const int32_t *log_map, float *logits_out, cudaStream_t st) {
+  const he_config &cf = h->cfg;
+  const int d = cf.d_model;
+  Ctx c{h, st};
+  for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
+  ensure_phase_events(h);
+  cudaEventRecord(h->ph[0], st);
+  // ---- prefill: all prompt tokens of all sequences in one pass ----
+  const int M = B * Lp;
+  {
+    Timed t(h, HE_KCLASS_OTHER, st);
+    c.check(launch_embed_ln(cf.dtype, prompt, M, Lp, 0, h->tok_emb, h->pos_emb, cf.pos_offset,
+                            cf.vocab, h->layers[0].ln1_g, h->layers[0].ln1_b, cf.ln_eps,
+                            static_cast<float *>(h->x.p), h->h.p, d,
+                            static_cast<int *>(h->err.p), st),
+            1);
+  }
+  for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, M, Lp, 0, true);
+  // head on the last prompt position of every sequence (rows b*Lp + Lp-1)
+  head(c, at(h->h.p, (size_t)(Lp - 1) * d * h->elem), Lp * d, B, 0, Lp, Lgen, force, out_ids,
+       out_lp, log_map, logits_out);
+  cudaEventRecord(h->ph[1], st);
+  // ---- decode: token k is fed at position Lp + k - 1 ----
+  for (int k = 1; k < Lgen; ++k) {
+    const int t = Lp + k - 1;
+    for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, B, 1, t, false);
+    head(c, h->h.p, d, B, k, Lp, Lgen, force, out_ids, out_lp, log_map, logits_out);
+  }
+  cudaEventRecord(h->ph[2], st);
+  h->stats.generate_calls++;
+  h->stats_pending = true;
+  if (c.e != cudaSuccess) return cuda_fail(c.e, "he_generate launch");
+  return HE_OK;
+}
+
+he_status check_generate_args(he_engine *h, const void *prompt, int B, int Lp, int Lgen,
+                              const void *ids, const void *lp) {
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (!prompt || !ids || !lp) return fail(HE_ERR_ARG, "NULL buffer");
+  const he_config &c = h->cfg;
+  if (B < 1 || B > c.max_batch) return fail(HE_ERR_ARG, "B=%d outside [1, max_batch=%d]", B, c.max_batch);
+  if (Lp < 1 || Lgen < 1) return fail(HE_ERR_ARG, "Lp=%d and Lgen=%d must be >= 1", Lp, Lgen);
+  if ((long long)Lp + Lgen > c.max_seq)
+    return fail(HE_ERR_ARG, "Lp + Lgen = %lld exceeds max_seq=%d", (long long)Lp + Lgen, c.max_seq);
+  if ((long long)Lp + Lgen - 1 > c.max_pos)
+    return fail(HE_ERR_ARG, "positions up to %lld exceed max_pos=%d", (long long)Lp + Lgen - 2,
+                c.max_pos);
+  if (!h->taken) return fail(HE_ERR_STATE, "workspace is released; call he_retake_workspace");
+  return HE_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+const char *he_last_error(void) { return g_err.c_str(); }
+
+const char *he_version(void) { return "libhe 0.1 (sm_103a; tcgen05 bf16 GEMM, fp32 CUDA-core path)"; }
+
+he_status he_create(const he_config *cfg, const he_weights *w, const he_allocator *alloc,
+                    int device, he_engine **out) {
+  g_err.clear();
+  if (!out) return fail(HE_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !w) return fail(HE_ERR_ARG, "cfg or weights is NULL");
+  const he_config c = *cfg;
+  if (c.n_layers < 1 || c.d_model < 1 || c.n_heads < 1 || c.ffn < 1 || c.vocab < 1 ||
+      c.max_pos < 1 || c.pos_offset < 0 || c.max_batch < 1 || c.max_seq < 2)
+    return fail(HE_ERR_ARG, "non-positive size in config");
+  if (c.d_model % c.n_heads) return fail(HE_ERR_ARG, "d_model %% n_heads != 0");
+  const int hd = c.d_model / c.n_heads;
+  if (hd != 32 && hd != 64 && hd != 128)
+    return fail(HE_ERR_UNSUPPORTED, "head_dim %d not in {32, 64, 128}", hd);
+  if (c.dtype != HE_DTYPE_F32 && c.dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
+  if (!(c.ln_eps > 0.f)) return fail(HE_ERR_ARG, "ln_eps must be > 0");
+  if (c.d_model % 8 || c.ffn % 8) return fail(HE_ERR_UNSUPPORTED, "d_model and ffn must be multiples of 8");
+  if (c.dtype == HE_DTYPE_BF16 && (c.d_model % 128 || c.ffn % 128))
+    return fail(HE_ERR_UNSUPPORTED, "bf16 path needs d_model and ffn multiples of 128");
+  if (c.lora_targets & ~0x3Fu) return fail(HE_ERR_ARG, "unknown bits in lora_targets");
+  if (c.lora_targets && (c.lora_r < 1 || c.lora_r > 64))
+    return fail(HE_ERR_ARG, "lora_r %d outside [1, 64]", c.lora_r);
+  if ((long long)c.max_batch * c.max_seq > (1LL << 30) ||
+      (long long)c.max_batch * c.max_seq * (c.ffn > c.vocab ? c.ffn : c.vocab) > (1LL << 40))
+    return fail(HE_ERR_UNSUPPORTED, "max_batch * max_seq too large");
+  if (!w->tok_emb || !w->pos_emb || !w->lnf_g || !w->lnf_b || !w->layers)
+    return fail(HE_ERR_ARG, "NULL global weight pointer");
+  const size_t align = c.dtype == HE_DTYPE_BF16 ? 16 : 4;
+  auto misaligned = [&](const void *p) { return ((uintptr_t)p) % align != 0; };
+  if (misaligned(w->tok_emb)) return fail(HE_ERR_ARG, "tok_emb not %zu-byte aligned", align);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const he_layer_weights &lw = w->layers[l];
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      if (!lw.w[p] || !lw.b[p]) return fail(HE_ERR_ARG, "layer %d projection %d: NULL", l, p);
+      if (misaligned(lw.w[p])) return fail(HE_ERR_ARG, "layer %d projection %d: not %zu-byte aligned", l, p, align);
+      if ((c.lora_targets >> p) & 1u)
+        if (!lw.lora_a[p] || !lw.lora_b[p])
+          return fail(HE_ERR_ARG, "layer %d projection %d: NULL LoRA factor", l, p);
+    }
+    if (!lw.ln1_g || !lw.ln1_b || !lw.ln2_g || !lw.ln2_b)
+      return fail(HE_ERR_ARG, "layer %d: NULL LayerNorm parameter", l);
+  }
+  if (cudaSetDevice(device) != cudaSuccess) return fail(HE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
+  int sms = 0;
+  cudaError_t ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (ce != cudaSuccess) return cuda_fail(ce, "device query");
+  if (c.dtype == HE_DTYPE_BF16) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    if (major != 10 || minor != 3)
+      return fail(HE_ERR_UNSUPPORTED, "bf16 kernels are built for sm_103a; device is sm_%d%d", major, minor);
+  }
+  he_engine *h = new he_engine();
+  h->cfg = c;
+  h->device = device;
+  h->num_sms = sms;
+  h->elem = c.dtype == HE_DTYPE_BF16 ? 2 : 4;
+  h->tok_emb = w->tok_emb;
+  h->pos_emb = w->pos_emb;
+  h->lnf_g = w->lnf_g;
+  h->lnf_b = w->lnf_b;
+  h->layers.assign(w->layers, w->layers + c.n_layers);
+  if (alloc && alloc->alloc && alloc->free)
+    h->alloc = *alloc;
+  else
+    h->alloc = he_allocator{default_alloc, default_free, nullptr};
+  if (!get(h, h->err, 256, nullptr)) {
+    delete h;
+    return fail(HE_ERR_OOM, "error-flag allocation failed");
+  }
+  ce = cudaMemset(h->err.p, 0, 256);
+  if (ce != cudaSuccess) {
+    put(h, h->err, nullptr);
+    delete h;
+    return cuda_fail(ce, "memset");
+  }
+  he_status s = take_workspace(h, nullptr);
+  if (s != HE_OK) {
+    put(h, h->err, nullptr);
+    delete h;
+    return s;
+  }
+  *out = h;
+  return HE_OK;
+}
+
+he_status he_destroy(he_engine *h) {
+  if (!h) return HE_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_workspace(h, nullptr);
+  put(h, h->restore, nullptr);
+  put(h, h->err, nullptr);
+  for (auto &e : h->ph)
+    if (e) cudaEventDestroy(e);
+  for (auto &pool : h->prof_pool)
+    for (auto &p : pool) {
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+  delete h;
+  return HE_OK;
+}
+
+he_status he_fuse_lora(he_engine *h, void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (h->fused) return fail(HE_ERR_STATE, "LoRA is already fused");
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const he_config &c = h->cfg;
+  auto rows_of = [&](int p) { return p == HE_PROJ_FC1 ? c.ffn : c.d_model; };
+  auto cols_of = [&](int p) { return p == HE_PROJ_FC2 ? c.ffn : c.d_model; };
+  size_t total = 0;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int p = 0; p < HE_N_PROJ; ++p)
+      if ((c.lora_targets >> p) & 1u) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
+  if (!get(h, h->restore, total, st))
+    return fail(HE_ERR_OOM, "LoRA restore copy of %zu bytes failed", total);
+  ensure_phase_events(h);
+  cudaEventRecord(h->ph[3], st);
+  const float scale = c.lora_targets ? c.lora_alpha / (float)c.lora_r : 0.f;
+  size_t off = 0;
+  cudaError_t err = cudaSuccess;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const he_layer_weights &lw = h->layers[l];
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      if (!((c.lora_targets >> p) & 1u)) continue;
+      cudaError_t e = launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p],
+                                       at(h->restore.p, off), rows_of(p), cols_of(p), c.lora_r,
+                                       scale, st);
+      if (e != cudaSuccess && err == cudaSuccess) err = e;
+      h->stats.launches++;
+      off += (size_t)rows_of(p) * cols_of(p) * h->elem;
+    }
+  }
+  cudaEventRecord(h->ph[4], st);
+  h->fuse_pending = true;
+  h->fused = true;
+  h->stats.restore_bytes = total;
+  if (err != cudaSuccess) return cuda_fail(err, "LoRA fuse launch");
+  return HE_OK;
+}
+
+he_status he_unfuse_lora(he_engine *h, void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (!h->fused) return fail(HE_ERR_STATE, "LoRA is not fused");
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const he_config &c = h->cfg;
+  auto rows_of = [&](int p) { return p == HE_PROJ_FC1 ? c.ffn : c.d_model; };
+  auto cols_of = [&](int p) { return p == HE_PROJ_FC2 ? c.ffn : c.d_model; };
+  ensure_phase_events(h);
+  cudaEventRecord(h->ph[4], st);
+  size_t off = 0;
+  cudaError_t err = cudaSuccess;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      if (!((c.lora_targets >> p) & 1u)) continue;
+      const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
+      cudaError_t e = launch_copy(h->layers[l].w[p], at(h->restore.p, off), bytes, st);
+      if (e != cudaSuccess && err == cudaSuccess) err = e;
+      h->stats.launches += (bytes % 16 ? 2 : 1);
+      off += bytes;
+    }
+  cudaEventRecord(h->ph[5], st);
+  h->unfuse_pending = true;
+  put(h, h->restore, st);
+  h->fused = false;
+  h->stats.restore_bytes = 0;
+  if (err != cudaSuccess) return cuda_fail(err, "LoRA restore launch");
+  return HE_OK;
+}
+
+he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                      int32_t *out_ids, float *out_logprob, void *stream) {
+  return he_generate_ex(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob, nullptr, nullptr, 0,
+                        nullptr, stream);
+}
+
+he_status he_generate_ex(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                         int32_t *out_ids, float *out_logprob, const int32_t *force_ids,
+                         const int32_t *log_rows, int n_rows, float *logits_out, void *stream) {
+  g_err.clear();
+  he_status s = check_generate_args(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob);
+  if (s != HE_OK) return s;
+  if (n_rows < 0 || (n_rows > 0 && (!log_rows || !logits_out)))
+    return fail(HE_ERR_ARG, "n_rows > 0 needs log_rows and logits_out");
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t *log_map = nullptr;
+  if (n_rows > 0) {
+    std::vector<int32_t> map((size_t)Lgen * B, -1);
+    for (int i = 0; i < n_rows; ++i) {
+      const int b = log_rows[2 * i], k = log_rows[2 * i + 1];
+      if (b < 0 || b >= B || k < 0 || k >= Lgen)
+        return fail(HE_ERR_ARG, "log_rows[%d] = (%d, %d) out of range", i, b, k);
+      map[(size_t)k * B + b] = i;
+    }
+    cudaError_t e = cudaMemcpyAsync(h->logmap.p, map.data(), map.size() * 4,
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "log map upload");
+    // the host vector dies here: make the copy complete before returning
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "log map upload");
+    log_map = static_cast<const int32_t *>(h->logmap.p);
+  }
+  return generate_impl(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob, force_ids, log_map,
+                       logits_out, st);
+}
+
+he_status he_check(he_engine *h, void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int flags = 0;
+  cudaError_t e = cudaMemcpyAsync(&flags, h->err.p, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "he_check");
+  if (flags) {
+    cudaMemsetAsync(h->err.p, 0, sizeof(int), st);
+    cudaStreamSynchronize(st);
+    if (flags & DEVERR_WAIT_TIMEOUT)
+      return fail(HE_ERR_DEVICE_CHECK, "a GEMM pipeline wait timed out (flags 0x%x)", flags);
+    return fail(HE_ERR_DEVICE_CHECK, "token id outside [0, vocab) replaced by 0 (flags 0x%x)", flags);
+  }
+  return HE_OK;
+}
+
+he_status he_generate_host(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                           int32_t *out_ids, float *out_logprob, void *stream) {
+  g_err.clear();
+  he_status s = check_generate_args(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob);
+  if (s != HE_OK) return s;
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->ids_in.p, prompt_ids, (size_t)B * Lp * 4,
+                                  cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prompt upload");
+  s = generate_impl(h, static_cast<int32_t *>(h->ids_in.p), B, Lp, Lgen,
+                    static_cast<int32_t *>(h->ids_out.p), static_cast<float *>(h->lp_out.p),
+                    nullptr, nullptr, nullptr, st);
+  if (s != HE_OK) return s;
+  e = cudaMemcpyAsync(out_ids, h->ids_out.p, (size_t)B * Lgen * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(out_logprob, h->lp_out.p, (size_t)B * Lgen * 4, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "result download");
+  return he_check(h, stream);
+}
+
+he_status he_release_workspace(he_engine *h, void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (!h->taken) return fail(HE_ERR_STATE, "workspace already released");
+  cudaSetDevice(h->device);
+  free_workspace(h, static_cast<cudaStream_t>(stream));
+  return HE_OK;
+}
+
+he_status he_retake_workspace(he_engine *h, void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (h->taken) return fail(HE_ERR_STATE, "workspace is already held");
+  cudaSetDevice(h->device);
+  return take_workspace(h, static_cast<cudaStream_t>(stream));
+}
+
+he_status he_set_profiling(he_engine *h, int enable) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  h->profiling = enable != 0;
+  return HE_OK;
+}
+
+he_status he_get_stats(he_engine *h, he_stats *s) {
+  g_err.clear();
+  if (!h || !s) return fail(HE_ERR_ARG, "NULL argument");
+  cudaSetDevice(h->device);
+  float ms = 0.f;
+  if (h->stats_pending) {
+    if (cudaEventSynchronize(h->ph[2]) != cudaSuccess) return fail(HE_ERR_CUDA, "event sync");
+    cudaEventElapsedTime(&ms, h->ph[0], h->ph[1]);
+    h->stats.prefill_ms = ms;
+    cudaEventElapsedTime(&ms, h->ph[1], h->ph[2]);
+    h->stats.decode_ms = ms;
+    for (int k = 0; k < kClasses; ++k) {
+      double tot = 0.0;
+      for (size_t i = 0; i < h->prof_used[k]; ++i) {
+        float t = 0.f;
+        cudaEventSynchronize(h->prof_pool[k][i].b);
+        cudaEventElapsedTime(&t, h->prof_pool[k][i].a, h->prof_pool[k][i].b);
+        tot += t;
+      }
+      h->stats.kclass_ms[k] = tot;
+      h->stats.kclass_launches[k] = (long long)h->prof_used[k];
+    }
+    h->stats_pending = false;
+  }
+  if (h->fuse_pending) {
+    cudaEventSynchronize(h->ph[4]);
+    cudaEventElapsedTime(&ms, h->ph[3], h->ph[4]);
+    h->stats.fuse_ms = ms;
+    h->fuse_pending = false;
+  }
+  if (h->unfuse_pending) {
+    cudaEventSynchronize(h->ph[5]);
+    cudaEventElapsedTime(&ms, h->ph[4], h->ph[5]);
+    h->stats.unfuse_ms = ms;
+    h->unfuse_pending = false;
+  }
+  *s = h->stats;
+  return HE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel-level entry (he_ops.h)
+// ---------------------------------------------------------------------------
+he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, float *y, int M, int N,
+                       int K, int split, float *scratch, void *stream) {
+  g_err.clear();
+  if (!x || !w || !y) return fail(HE_ERR_ARG, "NULL buffer");
+  if (M < 1 || N < 1 || K < 1 || ldx < K) return fail(HE_ERR_ARG, "bad sizes");
+  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
+  if (dtype == HE_DTYPE_BF16 && (K % 8 || ldx % 8))
+    return fail(HE_ERR_UNSUPPORTED, "bf16 needs K and ldx multiples of 8");
+  if (split < 1) return fail(HE_ERR_ARG, "split must be >= 1");
+  if (effective_split(K, split) != split)
+    return fail(HE_ERR_ARG, "split %d leaves an empty K slice (K=%d)", split, K);
+  if (split > 1 && !scratch) return fail(HE_ERR_ARG, "split > 1 needs scratch");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmArgs a{};
+  a.dtype = dtype;
+  a.x = x;
+  a.ldx = ldx;
+  a.w[0] = w;
+  a.n_groups = 1;
+  a.group_rows = N;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.split = split;
+  Epi e{};
+  e.kind = EPI_STORE_F32;
+  e.partial = y;
+  e.ldp = N;
+  if (split > 1) {
+    Epi pe{};
+    pe.kind = EPI_PARTIAL;
+    pe.partial = scratch;
+    pe.ldp = N;
+    pe.split_stride = (long long)M * N;
+    a.epi = pe;
+  } else {
+    a.epi = e;
+  }
+  cudaError_t r = launch_gemm(a, nullptr, st);
+  if (r == cudaSuccess && split > 1)
+    r = launch_reduce_epi(dtype, scratch, split, (long long)M * N, N, M, N, e, st);
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_linear");
+  return HE_OK;
+}
+
+}  // extern "C"

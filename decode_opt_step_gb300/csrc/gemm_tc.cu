@@ -1,0 +1,248 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// C[tok][n] = sum_k X[tok][k] * W[n][k] with both operands K-major, as nn.Linear
+// stores them.  The weight is the UMMA A operand (M = 128 output features per
+// tile) and the activations are the B operand (N = up to 256 tokens per tile):
+// in decode the token count is the batch, so a tile streams 128 weight rows once
+// for every sequence of the batch.  Accumulators live in TMEM (fp32, one lane
+// per output feature, one column per token).
+//
+// Warp roles (192 threads): warps 0-3 read TMEM and run the epilogue (warp w
+// owns TMEM lanes 32w..32w+31), warp 4 issues TMA loads into a STAGES-deep ring
+// of 128B-swizzled tiles, warp 5 owns the TMEM allocation and one elected thread
+// issues tcgen05.mma.  Every mbarrier wait is bounded; on a timeout the kernel
+// records DEVERR_WAIT_TIMEOUT, stops issuing, drains its own copies and frees
+// its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace he {
+
+namespace {
+
+constexpr int BM = 128;        // UMMA M: output features per tile
+constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;     // K per tcgen05.mma (kind::f16)
+constexpr int A_BYTES = BM * BK * 2;
+
+// UMMA shared-memory descriptor, K-major operand with 128-byte swizzle: rows of
+// 128 bytes, 8-row atoms of 1024 bytes (stride byte offset), version 1, swizzle
+// mode 2 (128B).  The leading byte offset is unused for this layout.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+constexpr uint32_t tmem_cols_for(int bn) { return bn <= 32 ? 32u : (bn <= 64 ? 64u : (bn <= 128 ? 128u : 256u)); }
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+              const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
+              int tiles_per_group, int M, int N, int kb_total, int kb_per_split, Epi epi,
+              int *dev_err) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t *smA = base;                                   // STAGES x A tile
+  uint8_t *smB = base + STAGES * A_BYTES;                // STAGES x B tile
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *accum = empty + STAGES;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x, n_tile = blockIdx.y, split = blockIdx.z;
+  const int kb0 = split * kb_per_split;
+  const int nkb = min(kb_per_split, kb_total - kb0);
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    const int group = m_tile / tiles_per_group;
+    const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
+    const int m_row = (m_tile - group * tiles_per_group) * BM;
+    prefetch_tmap(tw);
+    prefetch_tmap(&tm_x);
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      if (i >= STAGES && !mbar_wait_bounded(&empty[s], ((i / STAGES) - 1) & 1)) {
+        *abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      const int kc = (kb0 + i) * BK;
+      tma_load_2d(smA + s * A_BYTES, tw, &full[s], kc, m_row);
+      tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kc, n_tile * BN);
+      issued = i + 1;
+    }
+    // Drain: the last load issued into each stage must have landed before exit.
+    for (int i = max(0, issued - STAGES); i < issued; ++i)
+      if (!mbar_wait_bounded(&full[i % STAGES], (i / STAGES) & 1))
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+  } else if (warp == 5 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16(BN);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait_bounded(&full[s], (i / STAGES) & 1)) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(smA + s * A_BYTES);
+      const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < BK / UMMA_K; ++kk)
+        tc_mma_f16(tmem_base, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
+                   idesc, (i | kk) != 0);
+      tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
+    }
+    tc_commit(accum);        // arrives when every MMA issued above is complete
+  } else if (warp < 4) {
+    // ---------------- epilogue ----------------
+    const bool ok = mbar_wait_bounded(accum, 0);
+    if (!ok) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+    tc_fence_after();
+    const bool live = ok && !*(volatile int *)abort_flag && nkb > 0;
+    const int row = m_tile * BM + warp * 32 + lane;  // output feature n
+    const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      tmem_ld16(tl + c0, v);
+      if (live && row < N) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = n_tile * BN + c0 + j;
+          if (tok < M) epi_store<bf16>(epi, split, tok, row, v[j]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch.
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a [rows][cols] matrix with row stride `ld` elements, box
+// {64 (K), box_rows}, 128-byte swizzle, zero fill out of bounds.
+bool make_tmap(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
+  using C = Cfg<BN, STAGES>;
+  CUtensorMap tw[3], tx;
+  for (int g = 0; g < 3; ++g) {
+    const void *p = a.w[g < a.n_groups ? g : 0];
+    if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
+  }
+  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN)) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int kb_total = (a.K + BK - 1) / BK;
+  const int kb_per_split = split_kblocks(a.K, a.split);
+  if (effective_split(a.K, a.split) != a.split) return cudaErrorInvalidValue;
+  const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
+  dim3 grid(a.N / BM + (a.N % BM != 0), (a.M + BN - 1) / BN, a.split);
+  k_gemm_tc<BN, STAGES><<<grid, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, tiles_per_group,
+                                                    a.M, a.N, kb_total, kb_per_split, a.epi,
+                                                    dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
+  // Shape rules of this kernel (checked again by the engine at create time):
+  // K rows 16-byte aligned (K % 8), row groups whole tiles, pointers 16-byte aligned.
+  if (a.K <= 0 || a.K % 8 || a.ldx % 8 || a.M <= 0 || a.N <= 0) return cudaErrorInvalidValue;
+  if (a.n_groups < 1 || a.n_groups > 3) return cudaErrorInvalidValue;
+  if (a.n_groups > 1 && a.group_rows % BM) return cudaErrorInvalidValue;
+  if (a.n_groups * a.group_rows != a.N) return cudaErrorInvalidValue;
+  if (a.epi.kind == EPI_QKV && a.epi.d_model % BM) return cudaErrorInvalidValue;
+  if (a.M <= 16) return launch_bn<16, 6>(a, dev_err, st);
+  if (a.M <= 32) return launch_bn<32, 5>(a, dev_err, st);
+  if (a.M <= 64) return launch_bn<64, 4>(a, dev_err, st);
+  if (a.M <= 128) return launch_bn<128, 3>(a, dev_err, st);
+  return launch_bn<256, 4>(a, dev_err, st);
+}
+
+}  // namespace he

@@ -1,0 +1,117 @@
+// Internal launcher interface between the engine (engine.cu) and the kernels.
+// Host-side declarations only; no torch types, no exceptions.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace he {
+
+// Error flags written by kernels (the host reads them in he_check).
+enum : int {
+  DEVERR_BAD_TOKEN = 1,    // a token id outside [0, vocab) was replaced by 0
+  DEVERR_WAIT_TIMEOUT = 2  // an mbarrier wait ran out of iterations (kernel bailed out)
+};
+
+// What a GEMM (or the split-K reduction after it) does with each output
+// element C[tok][n] = sum_k X[tok][k] * W[n][k].
+enum EpiKind : int {
+  EPI_PARTIAL = 0,  // fp32 partial[split][tok][n] (bias/residual applied later, per row)
+  EPI_QKV = 1,      // n < d: q (+bq, * hd^-1/2) -> q_out[tok][n]; else k / v (+bias) -> cache
+  EPI_RELU = 2,     // out[tok][n] = relu(C + bias[n]) in the storage type
+  EPI_STORE_F32 = 3 // fp32 out[tok][n] = C (LM-head logits, kernel tests)
+};
+
+struct Epi {
+  int kind;
+  float *partial;        // EPI_PARTIAL / EPI_STORE_F32 destination
+  long long split_stride;// elements between splits of `partial`
+  int ldp;               // row stride of `partial`
+  const void *bias[3];   // QKV: bq, bk, bv; RELU: bias[0]
+  void *out;             // RELU output / QKV q output (storage type)
+  int ldo;
+  void *kc, *vc;         // QKV: this layer's K / V cache [B][H][max_seq][hd]
+  int d_model, n_heads, head_dim, max_seq;
+  int tok_per_seq;       // tokens of one sequence in this launch (Lp prefill, 1 decode)
+  int pos0;              // position of a sequence's first token in this launch
+  float q_scale;
+};
+
+struct GemmArgs {
+  int dtype;             // HE_DTYPE_F32 / HE_DTYPE_BF16
+  const void *x;         // [M][ldx] activations (tokens x K), storage type
+  int ldx;
+  const void *w[3];      // up to three row groups of `group_rows` rows, each [rows][K]
+  int n_groups, group_rows;
+  int M, N, K;           // tokens, output features (= n_groups * group_rows), reduction
+  int split;             // split-K factor (EPI_PARTIAL writes split slices)
+  Epi epi;
+};
+
+// Split-K works in blocks of 64 along K; a split covers split_kblocks(K, S)
+// consecutive blocks.  effective_split(K, S) is the number of non-empty slices,
+// which callers must pass as GemmArgs::split (the launchers reject other values).
+inline int split_kblocks(int K, int split) {
+  const int kb = (K + 63) / 64;
+  return (kb + split - 1) / split;
+}
+inline int effective_split(int K, int split) {
+  const int kb = (K + 63) / 64;
+  if (split < 1) split = 1;
+  if (split > kb) split = kb;
+  const int per = (kb + split - 1) / split;
+  return (kb + per - 1) / per;
+}
+
+// Result codes of the launchers (cudaError_t values pass through).
+cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st);
+int gemm_pick_split(const GemmArgs &a, int num_sms);  // heuristic for decode shapes
+
+cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long long split_stride,
+                              int ldp, int M, int N, const Epi &epi, cudaStream_t st);
+
+// x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type).
+cudaError_t launch_resid_ln(int dtype, const float *partial, int split, long long split_stride,
+                            int ldp, const void *bias, float *x, const void *g, const void *b,
+                            float eps, void *h, int rows, int d, cudaStream_t st);
+
+// x[tok] = E[id] + P[pos + off]; h[tok] = LN(x[tok]).  Token tok of a launch is
+// sequence tok / tok_per_seq at position pos0 + tok % tok_per_seq.
+cudaError_t launch_embed_ln(int dtype, const int32_t *ids, int n_tok, int tok_per_seq, int pos0,
+                            const void *tok_emb, const void *pos_emb, int pos_offset, int vocab,
+                            const void *g, const void *b, float eps, float *x, void *h, int d,
+                            int *dev_err, cudaStream_t st);
+
+struct HeadArgs {
+  const float *logits; int ldl; int vocab; int B;
+  int step, gen_len;
+  const int32_t *force_ids;          // [B][gen_len] or null
+  int32_t *out_ids; float *out_lp;   // [B][gen_len]
+  const int32_t *log_map;            // [gen_len][B] -> logits_out row or -1 (null = none)
+  float *logits_out;
+  int embed_next; int pos;           // embed the chosen token at position `pos` for the next pass
+  const void *tok_emb, *pos_emb; int pos_offset;
+  const void *g, *b; float eps;      // first layer's LN1
+  float *x; void *h; int d;
+};
+cudaError_t launch_head_select(int dtype, const HeadArgs &a, cudaStream_t st);
+
+// Decode attention: one query per (b, h) over keys 0..n_keys-1 of the cache.
+// part: scratch of B*H*split*(hd+2) floats when split > 1.
+cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
+                               void *ctx, int B, int H, int hd, int max_seq, int n_keys,
+                               int split, float *part, cudaStream_t st);
+int attn_decode_pick_split(int B, int H, int n_keys, int num_sms);
+
+// Prefill attention: causal within each prompt of Lp tokens (positions 0..Lp-1).
+cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const void *vc,
+                                void *ctx, int B, int Lp, int H, int hd, int max_seq,
+                                cudaStream_t st);
+
+// W <- round(W + scale * B A) after saving W's bits to `save`.
+cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,
+                             int rows, int cols, int r, float scale, cudaStream_t st);
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
+
+}  // namespace he

@@ -1,0 +1,302 @@
+// Row kernels of the generation path: embedding + LayerNorm, split-K reduction
+// with bias + residual + LayerNorm, the element-wise split-K epilogue, the
+// greedy head (argmax, log-softmax, next-token embedding), the LoRA fuse and the
+// restore copy.
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace he {
+
+namespace {
+
+// LayerNorm of the fp32 row held in shared memory `row[0..d)`: two passes
+// (mean, then the biased variance of the centred values), eps inside the root.
+template <typename T>
+__device__ void ln_store(const float *row, int d, const T *g, const T *b, float eps, T *out,
+                         float *red) {
+  float s = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) s += row[i];
+  const float mean = block_sum(s, red) / (float)d;
+  float v = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float c = row[i] - mean;
+    v += c * c;
+  }
+  const float var = block_sum(v, red) / (float)d;
+  const float rstd = 1.0f / sqrtf(var + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    out[i] = from_f<T>((row[i] - mean) * rstd * to_f<T>(g[i]) + to_f<T>(b[i]));
+}
+
+template <typename T>
+__device__ void embed_row(int id, int pos, const T *tok_emb, const T *pos_emb, int d, float *row,
+                          float *xout) {
+  const T *e = tok_emb + (long long)id * d;
+  const T *p = pos_emb + (long long)pos * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = to_f<T>(e[i]) + to_f<T>(p[i]);
+    row[i] = v;
+    xout[i] = v;
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const T *tok_emb,
+                           const T *pos_emb, int pos_offset, int vocab, const T *g, const T *b,
+                           float eps, float *x, T *h, int d, int *dev_err) {
+  extern __shared__ float row[];
+  __shared__ float red[33];
+  const int tok = blockIdx.x;
+  int id = ids[tok];
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) set_dev_error(dev_err, DEVERR_BAD_TOKEN);
+    id = 0;
+  }
+  const int pos = pos0 + tok % tok_per_seq + pos_offset;
+  embed_row<T>(id, pos, tok_emb, pos_emb, d, row, x + (long long)tok * d);
+  ln_store<T>(row, d, g, b, eps, h + (long long)tok * d, red);
+}
+
+template <typename T>
+__global__ void k_resid_ln(const float *partial, int split, long long split_stride, int ldp,
+                           const T *bias, float *x, const T *g, const T *b, float eps, T *h,
+                           int d) {
+  extern __shared__ float row[];
+  __shared__ float red[33];
+  const long long r = blockIdx.x;
+  float *xr = x + r * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < split; ++s) acc += partial[s * split_stride + r * ldp + i];
+    const float v = xr[i] + (acc + to_f<T>(bias[i]));
+    xr[i] = v;
+    row[i] = v;
+  }
+  __syncthreads();
+  ln_store<T>(row, d, g, b, eps, h + r * d, red);
+}
+
+template <typename T>
+__global__ void k_reduce_epi(const float *partial, int split, long long split_stride, int ldp,
+                             int M, int N, Epi epi) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)M * N) return;
+  const int tok = (int)(e / N), n = (int)(e % N);
+  float acc = 0.f;
+  for (int s = 0; s < split; ++s) acc += partial[s * split_stride + (long long)tok * ldp + n];
+  epi_store<T>(epi, 0, tok, n, acc);
+}
+
+// One block per sequence: greedy choice (lowest index among equal maxima),
+// log-prob of the emitted token, optional logit capture, then the embedding of
+// the emitted token at the next position followed by the first layer's LN1.
+template <typename T>
+__global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
+  extern __shared__ float row[];
+  __shared__ float red[33];
+  __shared__ float s_val[32];
+  __shared__ int s_idx[32];
+  __shared__ int s_tok;
+  const int b = blockIdx.x;
+  const float *lg = a.logits + (long long)b * a.ldl;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) {
+    const float v = lg[i];
+    if (v > best) {  // strided ascending scan: first hit of a value keeps the lowest index
+      best = v;
+      bidx = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ov > best || (ov == best && oi < bidx)) {
+      best = ov;
+      bidx = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    s_val[wid] = best;
+    s_idx[wid] = bidx;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    best = lane < nw ? s_val[lane] : -INFINITY;
+    bidx = lane < nw ? s_idx[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      if (ov > best || (ov == best && oi < bidx)) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if (lane == 0) {
+      s_val[0] = best;
+      s_idx[0] = bidx;
+    }
+  }
+  __syncthreads();
+  const float m = s_val[0];
+  const int amax = s_idx[0] == 0x7fffffff ? 0 : s_idx[0];
+  float se = 0.f;
+  for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) se += expf(lg[i] - m);
+  se = block_sum(se, red);
+  if (threadIdx.x == 0) {
+    int tok = amax;
+    if (a.force_ids) {
+      const int f = a.force_ids[(long long)b * a.gen_len + a.step];
+      if (f >= 0 && f < a.vocab) tok = f;
+    }
+    a.out_ids[(long long)b * a.gen_len + a.step] = tok;
+    a.out_lp[(long long)b * a.gen_len + a.step] = lg[tok] - (m + logf(se));
+    s_tok = tok;
+  }
+  if (a.log_map) {
+    const int r = a.log_map[(long long)a.step * a.B + b];
+    if (r >= 0)
+      for (int i = threadIdx.x; i < a.vocab; i += blockDim.x)
+        a.logits_out[(long long)r * a.vocab + i] = lg[i];
+  }
+  __syncthreads();
+  if (a.embed_next) {
+    embed_row<T>(s_tok, a.pos + a.pos_offset, static_cast<const T *>(a.tok_emb),
+                 static_cast<const T *>(a.pos_emb), a.d, row, a.x + (long long)b * a.d);
+    ln_store<T>(row, a.d, static_cast<const T *>(a.g), static_cast<const T *>(a.b), a.eps,
+                static_cast<T *>(a.h) + (long long)b * a.d, red);
+  }
+}
+
+// W <- round(W + scale * sum_j B[row][j] A[j][col]) for 8 consecutive columns
+// per thread, after copying the original bits of W to `save`.
+template <typename T>
+__global__ void k_lora_fuse(T *w, const T *A, const T *Bm, T *save, int rows, int cols, int r,
+                            float scale) {
+  const long long gidx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int gpr = cols / 8;
+  if (gidx >= (long long)rows * gpr) return;
+  const int row = (int)(gidx / gpr), c0 = (int)(gidx % gpr) * 8;
+  T *wp = w + (long long)row * cols + c0;
+  T *sp = save + (long long)row * cols + c0;
+  T wv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) wv[e] = wp[e];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sp[e] = wv[e];
+  float delta[8] = {};
+  for (int j = 0; j < r; ++j) {
+    const float bj = to_f<T>(Bm[(long long)row * r + j]);
+    const T *ap = A + (long long)j * cols + c0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, to_f<T>(ap[e]), delta[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) wp[e] = from_f<T>(to_f<T>(wv[e]) + scale * delta[e]);
+}
+
+__global__ void k_copy16(uint4 *dst, const uint4 *src, long long n16) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+__global__ void k_copy1(uint8_t *dst, const uint8_t *src, long long n) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = src[i];
+}
+
+int row_threads(int d) { return d >= 2048 ? 512 : (d >= 512 ? 256 : 128); }
+
+}  // namespace
+
+cudaError_t launch_embed_ln(int dtype, const int32_t *ids, int n_tok, int tok_per_seq, int pos0,
+                            const void *tok_emb, const void *pos_emb, int pos_offset, int vocab,
+                            const void *g, const void *b, float eps, float *x, void *h, int d,
+                            int *dev_err, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  const size_t sm = (size_t)d * sizeof(float);
+  if (dtype == 1)
+    k_embed_ln<bf16><<<n_tok, row_threads(d), sm, st>>>(
+        ids, tok_per_seq, pos0, (const bf16 *)tok_emb, (const bf16 *)pos_emb, pos_offset, vocab,
+        (const bf16 *)g, (const bf16 *)b, eps, x, (bf16 *)h, d, dev_err);
+  else
+    k_embed_ln<float><<<n_tok, row_threads(d), sm, st>>>(
+        ids, tok_per_seq, pos0, (const float *)tok_emb, (const float *)pos_emb, pos_offset, vocab,
+        (const float *)g, (const float *)b, eps, x, (float *)h, d, dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_resid_ln(int dtype, const float *partial, int split, long long split_stride,
+                            int ldp, const void *bias, float *x, const void *g, const void *b,
+                            float eps, void *h, int rows, int d, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const size_t sm = (size_t)d * sizeof(float);
+  if (dtype == 1)
+    k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, split, split_stride, ldp,
+                                                       (const bf16 *)bias, x, (const bf16 *)g,
+                                                       (const bf16 *)b, eps, (bf16 *)h, d);
+  else
+    k_resid_ln<float><<<rows, row_threads(d), sm, st>>>(partial, split, split_stride, ldp,
+                                                        (const float *)bias, x, (const float *)g,
+                                                        (const float *)b, eps, (float *)h, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long long split_stride,
+                              int ldp, int M, int N, const Epi &epi, cudaStream_t st) {
+  const long long n = (long long)M * N;
+  if (n <= 0) return cudaSuccess;
+  const int blocks = (int)((n + 255) / 256);
+  if (dtype == 1)
+    k_reduce_epi<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  else
+    k_reduce_epi<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_select(int dtype, const HeadArgs &a, cudaStream_t st) {
+  const size_t sm = (size_t)a.d * sizeof(float);
+  if (dtype == 1)
+    k_head_select<bf16><<<a.B, 1024, sm, st>>>(a);
+  else
+    k_head_select<float><<<a.B, 1024, sm, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,
+                             int rows, int cols, int r, float scale, cudaStream_t st) {
+  if (cols % 8) return cudaErrorInvalidValue;
+  const long long groups = (long long)rows * (cols / 8);
+  const int blocks = (int)((groups + 255) / 256);
+  if (dtype == 1)
+    k_lora_fuse<bf16><<<blocks, 256, 0, st>>>((bf16 *)w, (const bf16 *)a, (const bf16 *)bm,
+                                              (bf16 *)save, rows, cols, r, scale);
+  else
+    k_lora_fuse<float><<<blocks, 256, 0, st>>>((float *)w, (const float *)a, (const float *)bm,
+                                               (float *)save, rows, cols, r, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  const bool aligned = ((uintptr_t)dst % 16 == 0) && ((uintptr_t)src % 16 == 0);
+  const long long n16 = aligned ? (long long)(bytes / 16) : 0;
+  if (n16 > 0) {
+    const long long blocks = (n16 + 255) / 256;
+    k_copy16<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>((uint4 *)dst, (const uint4 *)src,
+                                                                   n16);
+  }
+  const long long done = n16 * 16, rest = (long long)bytes - done;
+  if (rest > 0)
+    k_copy1<<<(int)((rest + 255) / 256), 256, 0, st>>>((uint8_t *)dst + done,
+                                                      (const uint8_t *)src + done, rest);
+  return cudaGetLastError();
+}
+
+}  // namespace he

@@ -1,0 +1,230 @@
+/*
+ * he.h -- Hybrid-Engine experience generation for an OPT-style actor on one GPU.
+ *
+ * C ABI of libhe.so.  Plain pointers and sizes only.  All device pointers are
+ * CUDA device addresses on the engine's device; every call that takes a
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
+ * enqueues its work on it and returns before the work finishes unless stated.
+ *
+ * The operations follow these passages:
+ *  [DSC-gen]  "DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of
+ *             ChatGPT-like Models at All Scales" (paper summary), §3.4, "Step 3:
+ *             RLHF Training via PPO", item 1: the actor generates 256-token
+ *             answers to 256-token prompts token by token; the phase is bound by
+ *             memory bandwidth.
+ *  [DSC-kv]   same page, §3.4 "Inference Mode: Generation Phase Optimizations",
+ *             Optimization 2: keys and values of earlier tokens are cached,
+ *             appended each step and reused; buffers are reused across steps.
+ *  [DSC-lora] same page, §3.4 "Training Mode: ZeRO and LoRA Optimizations",
+ *             Optimization 2: a weight W is used as W + B A (B: d x r, A: r x k).
+ *  [DSC-he]   same page, §3.4 "The DeepSpeed Hybrid Engine: Architecture and
+ *             Mode Switching": one model instance; at the inference/training
+ *             switch the engine allocates or frees the KV-cache buffers.
+ *  [HE-guide] "DeepSpeed-Chat 选型指南：Hybrid Engine 驱动的 RLHF 训练全解析",
+ *             §三 (engine internals): generate() fuses LoRA into the inference
+ *             model before generation and restores it after; the KV cache and
+ *             intermediate results live in a workspace that is released after
+ *             generation and retaken before the next; §四 (config fields):
+ *             max_out_tokens, release_inference_cache.
+ *  [RLHF-ch11] "Chapter 11 System Architecture & Infrastructure at Scale",
+ *             "The Generation Bottleneck: Quantitative Analysis": generation
+ *             returns the log-probabilities of the generated tokens.
+ *
+ * Model (OPT-style pre-LN decoder; the pages name the OPT family but not its
+ * layer details, which are taken as OPT defines them): x = E_tok[id] +
+ * E_pos[t + pos_offset]; per layer h = LN1(x); q = (h Wq^T + bq) hd^-1/2,
+ * k = h Wk^T + bk, v = h Wv^T + bv; causal softmax attention per head;
+ * x += ctx Wo^T + bo; x += ReLU(LN2(x) W1^T + b1) W2^T + b2; logits =
+ * LN_f(x) E_tok^T (tied head, no bias).  LayerNorm: biased variance, eps
+ * inside the square root.  Greedy choice: argmax, lowest index on ties.
+ *
+ * Errors: every call returns an he_status.  Argument and state errors are
+ * found on the host before anything is enqueued and leave the engine as it
+ * was.  he_last_error() gives a message for the last failing call on the
+ * calling thread.  Nothing throws across this ABI.
+ */
+#ifndef HE_H
+#define HE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct he_engine he_engine; /* opaque, owned by the library */
+
+typedef enum {
+  HE_OK = 0,
+  HE_ERR_ARG = -1,          /* bad argument (NULL, out of range, inconsistent size) */
+  HE_ERR_STATE = -2,        /* call not allowed in the engine's current state */
+  HE_ERR_OOM = -3,          /* the allocator returned NULL */
+  HE_ERR_CUDA = -4,         /* a CUDA runtime/driver call or launch failed */
+  HE_ERR_UNSUPPORTED = -5,  /* shape or dtype outside what the kernels handle */
+  HE_ERR_DEVICE_CHECK = -6  /* a device-side input check failed (e.g. token id >= vocab) */
+} he_status;
+
+enum { HE_DTYPE_F32 = 0, HE_DTYPE_BF16 = 1 };
+
+/* Bit i of he_config.lora_targets: projection i carries a LoRA pair. */
+enum {
+  HE_PROJ_Q = 0, HE_PROJ_K = 1, HE_PROJ_V = 2, HE_PROJ_O = 3, HE_PROJ_FC1 = 4, HE_PROJ_FC2 = 5,
+  HE_N_PROJ = 6
+};
+
+typedef struct {
+  int n_layers, d_model, n_heads, ffn, vocab;
+  int max_pos;      /* usable positions; E_pos has max_pos + pos_offset rows */
+  int pos_offset;   /* 2 for OPT's learned positions */
+  int dtype;        /* HE_DTYPE_*: storage of every parameter, of the KV cache and of the
+                       GEMM inputs.  F32: fp32 CUDA-core kernels.  BF16: tcgen05 tensor
+                       cores with fp32 accumulation; residual stream, LayerNorm, softmax,
+                       logits and log-probs stay fp32. */
+  float ln_eps;     /* 1e-5 for OPT */
+  int max_batch;    /* workspace sizing: every he_generate has B <= max_batch */
+  int max_seq;      /* workspace sizing: Lp + Lgen <= max_seq (the KV cache length);
+                       the role of the hybrid_engine max_out_tokens field */
+  int lora_r;       /* LoRA rank r (1..64) */
+  float lora_alpha; /* the fused delta is (lora_alpha / lora_r) * B A */
+  unsigned lora_targets; /* bit mask over HE_PROJ_*; 0 = no LoRA */
+} he_config;
+
+/* One decoder layer.  Projections are [out][in] row-major (y = x W^T + b):
+ * Wq, Wk, Wv, Wo: [d][d]; W1: [ffn][d]; W2: [d][ffn].  All tensors have the
+ * config's dtype and are caller-owned device memory that must stay valid until
+ * he_destroy.  w[] is written in place by he_fuse_lora / he_unfuse_lora. */
+typedef struct {
+  void *w[HE_N_PROJ];            /* indexed by HE_PROJ_* */
+  const void *b[HE_N_PROJ];      /* biases [out] */
+  const void *ln1_g, *ln1_b, *ln2_g, *ln2_b; /* [d] */
+  const void *lora_a[HE_N_PROJ]; /* A: [r][in]  (NULL where the target bit is clear) */
+  const void *lora_b[HE_N_PROJ]; /* B: [out][r] */
+} he_layer_weights;
+
+typedef struct {
+  const void *tok_emb;   /* [vocab][d]; also the tied LM head */
+  const void *pos_emb;   /* [max_pos + pos_offset][d] */
+  const void *lnf_g, *lnf_b; /* final LayerNorm [d] */
+  const he_layer_weights *layers; /* host array of n_layers; copied by he_create */
+} he_weights;
+
+/* Device-memory allocator the engine uses for its workspace, its KV cache and
+ * the LoRA restore copy, so that released memory goes back to the caller (for
+ * example to a framework's caching allocator for the training phase).
+ * alloc returns a device pointer aligned to >= 256 bytes or NULL; free gets the
+ * same size.  `stream` is the stream the memory will be used on. */
+typedef struct {
+  void *(*alloc)(size_t bytes, void *stream, void *ctx);
+  void (*free)(void *ptr, size_t bytes, void *stream, void *ctx);
+  void *ctx;
+} he_allocator;
+
+typedef struct {
+  double fuse_ms, prefill_ms, decode_ms, unfuse_ms; /* last call of each, device time */
+  long long launches;            /* kernels launched by the library since he_create */
+  long long generate_calls;
+  size_t workspace_bytes;        /* KV cache + scratch currently held */
+  size_t kv_bytes;               /* KV cache part of it */
+  size_t restore_bytes;          /* LoRA restore copy currently held */
+  /* Per-kernel-class device time of the last he_generate, filled only while
+   * profiling is on (he_set_profiling); index by HE_KCLASS_*. */
+  double kclass_ms[8];
+  long long kclass_launches[8];
+} he_stats;
+
+enum {
+  HE_KCLASS_GEMM = 0,        /* decode projections (QKV, out, fc1, fc2) */
+  HE_KCLASS_ATTN_DECODE = 1, /* decode single-query attention (+ its combine) */
+  HE_KCLASS_NORM = 2,        /* residual + LayerNorm rows, split reductions */
+  HE_KCLASS_HEAD = 3,        /* LM head GEMM + greedy select / log-prob / next embed */
+  HE_KCLASS_PREFILL_GEMM = 4,
+  HE_KCLASS_PREFILL_ATTN = 5,
+  HE_KCLASS_OTHER = 6
+};
+
+/* Creates an engine on `device` (the CUDA ordinal; it becomes current for the
+ * calling thread).  Checks the config (d_model % n_heads == 0, head_dim in
+ * {32, 64, 128}; BF16 also needs d_model, ffn multiples of 128, vocab % 8 == 0),
+ * records the weight pointers (no copy: one model instance, [DSC-he]) and takes
+ * the workspace (KV cache [n_layers][max_batch][n_heads][max_seq][head_dim] for
+ * K and for V, plus activations) through `alloc`.  alloc == NULL uses cudaMalloc /
+ * cudaFree.  On failure *out is NULL and nothing is held. */
+he_status he_create(const he_config *cfg, const he_weights *w, const he_allocator *alloc,
+                    int device, he_engine **out);
+
+/* Frees everything the engine holds (restoring fused weights first is the
+ * caller's job: destroying a fused engine leaves the weights fused).  NULL is a no-op. */
+he_status he_destroy(he_engine *h);
+
+/* [DSC-lora], [HE-guide]: saves the bits of every targeted projection, then
+ * writes W <- round(W + (alpha/r) * B A) in place (fp32 arithmetic, round to
+ * nearest even into the storage type).  HE_ERR_STATE if already fused; the
+ * restore copy (sum of the targeted projections' sizes) is taken through the
+ * allocator (HE_ERR_OOM leaves the engine unfused and the weights untouched). */
+he_status he_fuse_lora(he_engine *h, void *stream);
+
+/* Restores the saved bits of every targeted projection (bit-exact) and frees
+ * the restore copy.  HE_ERR_STATE if not fused. */
+he_status he_unfuse_lora(he_engine *h, void *stream);
+
+/* [DSC-gen], [DSC-kv], [RLHF-ch11]: greedy generation of Lgen tokens for B
+ * prompts of Lp tokens.  prompt_ids: device int32 [B][Lp], every id in
+ * [0, vocab).  out_ids: device int32 [B][Lgen]; out_logprob: device fp32
+ * [B][Lgen], natural-log softmax of the chosen token.  One prefill pass over the
+ * prompts, then Lgen - 1 single-token passes over the KV cache; the last token
+ * is not fed back.  Requires 1 <= B <= max_batch, Lp >= 1, Lgen >= 1,
+ * Lp + Lgen <= max_seq, Lp + Lgen - 1 <= max_pos, and a taken workspace
+ * (HE_ERR_STATE after he_release_workspace).  Runs fused or unfused.  An id out
+ * of range is replaced by 0 on the device and reported by he_check. */
+he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                      int32_t *out_ids, float *out_logprob, void *stream);
+
+/* he_generate with teacher forcing and logit capture (parity checks):
+ * force_ids: device int32 [B][Lgen] or NULL; where force_ids[b][k] >= 0 step k
+ * emits and feeds back that id (its log-prob is reported) instead of the argmax.
+ * log_rows: HOST int32 pairs (b, k), n_rows of them; the fp32 logits of sequence
+ * b at step k are written to logits_out[i][0..vocab) (device, [n_rows][vocab]).
+ * n_rows may be 0 (then log_rows and logits_out may be NULL). */
+he_status he_generate_ex(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                         int32_t *out_ids, float *out_logprob, const int32_t *force_ids,
+                         const int32_t *log_rows, int n_rows, float *logits_out,
+                         void *stream);
+
+/* he_generate on HOST buffers: copies prompt_ids [B][Lp] in, generates, copies
+ * out_ids / out_logprob [B][Lgen] back and synchronises `stream` before it
+ * returns.  Also returns HE_ERR_DEVICE_CHECK if a prompt id was out of range. */
+he_status he_generate_host(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
+                           int32_t *out_ids, float *out_logprob, void *stream);
+
+/* Synchronises `stream` and reports (then clears) the device-side input check:
+ * HE_ERR_DEVICE_CHECK if an id was out of range since the last check. */
+he_status he_check(he_engine *h, void *stream);
+
+/* [HE-guide] release_inference_cache: hands the KV cache and activation
+ * workspace back to the allocator (stream-ordered on `stream`).  The LoRA restore
+ * copy is kept while fused.  HE_ERR_STATE if already released. */
+he_status he_release_workspace(he_engine *h, void *stream);
+
+/* Takes the workspace again before the next generation.  HE_ERR_STATE if held;
+ * HE_ERR_OOM leaves the engine released and usable (retry later). */
+he_status he_retake_workspace(he_engine *h, void *stream);
+
+/* Per-kernel-class event timing of he_generate (off by default; costs two
+ * events per timed launch). */
+he_status he_set_profiling(he_engine *h, int enable);
+
+/* Fills *s.  Synchronises the engine's events from the last calls first. */
+he_status he_get_stats(he_engine *h, he_stats *s);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *he_last_error(void);
+
+/* Library build identifier (static string). */
+const char *he_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HE_H */

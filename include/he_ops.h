@@ -1,0 +1,32 @@
+/*
+ * he_ops.h -- kernel-level entry points of libhe, for testing the kernels that
+ * he_generate runs on shapes of the caller's choosing.
+ */
+#ifndef HE_OPS_H
+#define HE_OPS_H
+
+#include "he.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* y[M][N] (fp32, row-major) = x[M][K] w[N][K]^T: the projection y = x W^T of
+ * every linear layer of the model ("DeepSpeed-Chat: Easy, Fast and Affordable
+ * RLHF Training of ChatGPT-like Models at All Scales", §3.4 "Inference Mode:
+ * Generation Phase Optimizations", Optimization 1: each generation step
+ * multiplies the current tokens' activations with every weight matrix).
+ * dtype HE_DTYPE_BF16 runs the tcgen05 tensor-core kernel (K and ldx multiples
+ * of 8, x and w 16-byte aligned); HE_DTYPE_F32 runs the fp32 CUDA-core kernel.
+ * x has row stride ldx >= K; w is dense [N][K].  split >= 1 splits K into
+ * slices of whole 64-wide blocks (no empty slice allowed) whose fp32 partial
+ * sums go to scratch [split][M][N] and are then added in slice order.  All
+ * pointers are device memory; asynchronous on `stream`. */
+he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, float *y, int M, int N,
+                       int K, int split, float *scratch, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HE_OPS_H */

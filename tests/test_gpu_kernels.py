@@ -1,0 +1,79 @@
+"""Kernel-level GPU tests through the C ABI (he_op_linear) on ragged shapes."""
+import numpy as np
+import pytest
+import torch
+
+import decode_opt_step_gb300 as he
+
+pytestmark = pytest.mark.gpu
+
+
+def _exact(x, w):
+    return x.double().cpu().numpy() @ w.double().cpu().numpy().T
+
+
+def _bound(x, w, K):
+    # fp32 accumulation of K products: |err| <= K * 2^-23 * sum |x_k w_k| (+ slack)
+    mag = x.abs().double().cpu().numpy() @ w.abs().double().cpu().numpy().T
+    return K * 2.0 ** -23 * mag + 1e-6
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (3, 256, 8), (16, 384, 768), (17, 200, 136),
+                                   (100, 640, 1024), (129, 128, 520), (300, 1000, 256),
+                                   (513, 384, 64)])
+def test_linear_bf16_tcgen05_matches_exact(cuda_device, M, N, K):
+    g = torch.Generator().manual_seed(M * 7919 + N * 31 + K)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w)
+    torch.cuda.synchronize()
+    ref = _exact(x, w)
+    err = np.abs(y.cpu().numpy() - ref)
+    assert (err <= _bound(x, w, K)).all(), f"max err {err.max()}"
+
+
+@pytest.mark.parametrize("split", [2, 3, 5])
+def test_linear_bf16_split_k(cuda_device, split):
+    M, N, K = 64, 512, 1280
+    g = torch.Generator().manual_seed(split)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w, split=split)
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, K)).all()
+
+
+def test_linear_bf16_strided_rows(cuda_device):
+    # x rows with a stride larger than K (the LM head reads every Lp-th row)
+    g = torch.Generator().manual_seed(5)
+    big = torch.randn(7 * 9, 256, generator=g).to(torch.bfloat16).cuda()
+    x = big[8::9]  # rows 8, 17, ... : stride 9*256
+    w = torch.randn(384, 256, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w)
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, 256)).all()
+
+
+@pytest.mark.parametrize("M,N,K,split", [(2, 384, 128, 1), (5, 100, 72, 2), (70, 130, 200, 1)])
+def test_linear_fp32_cuda_cores(cuda_device, M, N, K, split):
+    g = torch.Generator().manual_seed(M + N + K)
+    x = torch.randn(M, K, generator=g).cuda()
+    w = torch.randn(N, K, generator=g).cuda()
+    y = he.linear(x, w, split=split)
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, K)).all()
+
+
+def test_linear_rejects_bad_arguments(cuda_device):
+    x = torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(8, 12, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(he.HeError) as e:
+        he.linear(x, w)  # K = 12 is not a multiple of 8 (16-byte TMA rows)
+    assert e.value.status == he.HE_ERR_UNSUPPORTED
+    x = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(he.HeError):
+        he.linear(x, w, split=3)  # K = 64 has one block: no 3-way split
