@@ -83,7 +83,7 @@ _SIGNATURES = {
     "he_check": (c_int, [c_void_p, c_void_p]),
     "he_release_workspace": (c_int, [c_void_p, c_void_p]),
     "he_retake_workspace": (c_int, [c_void_p, c_void_p]),
-    "he_set_profiling": (c_int, [c_void_p, c_int]),
+    "he_set_profiling": (c_int, [c_void_p, c_uint]),
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
     "he_last_error": (c_char_p, []),
     "he_version": (c_char_p, []),
@@ -234,8 +234,15 @@ class Engine:
     def check(self, stream=None):
         _check(self._lib.he_check(self._h, self._s(stream)))
 
-    def set_profiling(self, on: bool):
-        _check(self._lib.he_set_profiling(self._h, 1 if on else 0))
+    def set_profiling(self, classes=()):
+        """Time the given kernel classes (names from KCLASS, or "all"); () turns it off."""
+        if classes == "all":
+            mask = 0xFF
+        else:
+            mask = 0
+            for c in classes:
+                mask |= 1 << KCLASS.index(c)
+        _check(self._lib.he_set_profiling(self._h, mask))
 
     def _prompts(self, prompts):
         torch = self._torch

@@ -9,7 +9,9 @@
 // merged by a second small kernel (no inter-CTA waiting).
 //
 // Prefill: causal attention inside each prompt, 64 queries per CTA, key blocks
-// of 64 staged in shared memory, online softmax across key blocks (CUDA cores).
+// of 64 staged in shared memory, online softmax across key blocks.  This file
+// holds the fp32 CUDA-core version; bf16 runs on tensor cores
+// (attn_prefill_mma.cu).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -298,13 +300,16 @@ cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const v
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_attn_prefill_bf16_mma(const void *q, const void *kc, const void *vc, void *ctx,
+                                         int B, int Lp, int H, int hd, int max_seq,
+                                         cudaStream_t st);
+
 cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const void *vc,
                                 void *ctx, int B, int Lp, int H, int hd, int max_seq,
                                 cudaStream_t st) {
   if (dtype == 1) {
-    if (hd == 128) return prefill_t<bf16, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-    if (hd == 64) return prefill_t<bf16, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-    if (hd == 32) return prefill_t<bf16, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    // bf16: tensor cores (attn_prefill_mma.cu)
+    return launch_attn_prefill_bf16_mma(q, kc, vc, ctx, B, Lp, H, hd, max_seq, st);
   } else {
     if (hd == 128) return prefill_t<float, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
     if (hd == 64) return prefill_t<float, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);

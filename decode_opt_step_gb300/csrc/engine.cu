@@ -59,7 +59,8 @@ struct he_engine {
   std::vector<he_layer_weights> layers;
   he_allocator alloc{};
 
-  bool taken = false, fused = false, profiling = false;
+  bool taken = false, fused = false;
+  unsigned prof_mask = 0;
   // workspace (released / retaken together)
   Buf kc, vc, x, h, q, ctx, mid, partial, logits, attn_part, ids_in, ids_out, lp_out, logmap;
   // held for the engine's lifetime
@@ -68,7 +69,7 @@ struct he_engine {
   Buf restore;
 
   he_stats stats{};
-  cudaEvent_t ph[6] = {};  // fuse begin/end ... (lazily created)
+  cudaEvent_t ph[7] = {};  // generate begin/prefill end/end, fuse begin/end, unfuse begin/end
   struct Pair { cudaEvent_t a, b; };
   std::vector<Pair> prof_pool[kClasses];
   size_t prof_used[kClasses] = {};
@@ -158,7 +159,7 @@ struct Timed {
   cudaStream_t st;
   he_engine::Pair *p = nullptr;
   Timed(he_engine *h_, int c, cudaStream_t s) : h(h_), cls(c), st(s) {
-    if (!h->profiling) return;
+    if (!((h->prof_mask >> cls) & 1u)) return;
     auto &pool = h->prof_pool[cls];
     if (h->prof_used[cls] == pool.size()) {
       he_engine::Pair np{};
@@ -611,7 +612,7 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
   auto rows_of = [&](int p) { return p == HE_PROJ_FC1 ? c.ffn : c.d_model; };
   auto cols_of = [&](int p) { return p == HE_PROJ_FC2 ? c.ffn : c.d_model; };
   ensure_phase_events(h);
-  cudaEventRecord(h->ph[4], st);
+  cudaEventRecord(h->ph[5], st);
   size_t off = 0;
   cudaError_t err = cudaSuccess;
   for (int l = 0; l < c.n_layers; ++l)
@@ -623,7 +624,7 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
       h->stats.launches += (bytes % 16 ? 2 : 1);
       off += bytes;
     }
-  cudaEventRecord(h->ph[5], st);
+  cudaEventRecord(h->ph[6], st);
   h->unfuse_pending = true;
   put(h, h->restore, st);
   h->fused = false;
@@ -726,10 +727,10 @@ he_status he_retake_workspace(he_engine *h, void *stream) {
   return take_workspace(h, static_cast<cudaStream_t>(stream));
 }
 
-he_status he_set_profiling(he_engine *h, int enable) {
+he_status he_set_profiling(he_engine *h, unsigned class_mask) {
   g_err.clear();
   if (!h) return fail(HE_ERR_ARG, "engine is NULL");
-  h->profiling = enable != 0;
+  h->prof_mask = class_mask & ((1u << kClasses) - 1);
   return HE_OK;
 }
 
@@ -764,8 +765,8 @@ he_status he_get_stats(he_engine *h, he_stats *s) {
     h->fuse_pending = false;
   }
   if (h->unfuse_pending) {
-    cudaEventSynchronize(h->ph[5]);
-    cudaEventElapsedTime(&ms, h->ph[4], h->ph[5]);
+    cudaEventSynchronize(h->ph[6]);
+    cudaEventElapsedTime(&ms, h->ph[5], h->ph[6]);
     h->stats.unfuse_ms = ms;
     h->unfuse_pending = false;
   }

@@ -19,7 +19,8 @@ constexpr int TK = 16;   // K per smem step
 template <typename T>
 __global__ void __launch_bounds__(256)
     k_gemm_simt(const T *__restrict__ x, int ldx, const T *w0, const T *w1, const T *w2,
-                int group_rows, int M, int N, int K, int kb_per_split, Epi epi) {
+                int group_rows, int M, int N, int K, int kb_per_split,
+                const __grid_constant__ Epi epi) {
   __shared__ float xs[TK][TT + 4];
   __shared__ float ws[TK][TN + 4];
   const int tok0 = blockIdx.y * TT, n0 = blockIdx.x * TN, split = blockIdx.z;
@@ -85,27 +86,32 @@ cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Split-K for the skinny decode GEMMs: enough CTAs to cover every SM about twice
-// with little wave quantisation, without cutting K below four 64-wide blocks.
+// Split-K for the skinny decode GEMMs.  A cost model picks S: one CTA per SM,
+// each SM streams ceil(units / SMs) units of 128 weight rows x K/S at a per-SM
+// rate, while the whole GEMM moves the weights plus the fp32 partial slices
+// (written and read back) at the HBM rate; the slower of the two is the time.
 int gemm_pick_split(const GemmArgs &a, int num_sms) {
-  const int bm = a.dtype == 1 ? 128 : TN;
-  const int bn = a.dtype == 1 ? (a.M <= 16 ? 16 : a.M <= 32 ? 32 : a.M <= 64 ? 64 : a.M <= 128 ? 128 : 256) : TT;
+  const bool tc = a.dtype == 1;
+  const int bm = tc ? 128 : TN;
+  const int bn = tc ? (a.M <= 16 ? 16 : a.M <= 32 ? 32 : a.M <= 64 ? 64 : a.M <= 128 ? 128 : 256) : TT;
   const long long tiles = (long long)((a.N + bm - 1) / bm) * ((a.M + bn - 1) / bn);
-  const int slots = 2 * num_sms;
-  if (tiles >= slots) return 1;
   const int kb = (a.K + 63) / 64;
+  const double esz = tc ? 2.0 : 4.0;
+  const double hbm = 6.5e12, per_sm = 80e9;
+  const double wbytes = (double)a.N * a.K * esz;
   int best = 1;
-  double best_score = -1.0;
-  for (int s = 1; s <= 16 && s * 4 <= kb; ++s) {
-    const int es = effective_split(a.K, s);
-    if (es != s) continue;
-    const long long ctas = tiles * s;
-    const double waves = (double)ctas / slots;
-    const double eff = waves / (double)((ctas + slots - 1) / slots);
-    const double fill = ctas >= num_sms ? 1.0 : (double)ctas / num_sms;
-    const double score = eff * fill - 0.01 * s;
-    if (score > best_score) {
-      best_score = score;
+  double best_t = 1e30;
+  for (int s = 1; s <= 16 && s <= kb; ++s) {
+    if (effective_split(a.K, s) != s) continue;
+    const long long units = tiles * s;
+    const long long per = (units + num_sms - 1) / num_sms;
+    const double unit_bytes = (double)bm * split_kblocks(a.K, s) * 64 * esz;
+    const double t_sm = per * unit_bytes / per_sm;
+    const double partial = s > 1 ? 2.0 * s * (double)a.M * a.N * 4.0 : 0.0;
+    const double t = (t_sm > (wbytes + partial) / hbm ? t_sm : (wbytes + partial) / hbm) +
+                     (s > 1 ? 2e-6 : 0.0);
+    if (t < best_t * 0.98) {
+      best_t = t;
       best = s;
     }
   }

@@ -57,7 +57,8 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
-              int tiles_per_group, int M, int N, int kb_total, int kb_per_split, Epi epi,
+              int tiles_per_group, int M, int N, int kb_total, int kb_per_split,
+              const __grid_constant__ Epi epi,
               int *dev_err) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -238,10 +239,12 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   if (a.n_groups > 1 && a.group_rows % BM) return cudaErrorInvalidValue;
   if (a.n_groups * a.group_rows != a.N) return cudaErrorInvalidValue;
   if (a.epi.kind == EPI_QKV && a.epi.d_model % BM) return cudaErrorInvalidValue;
-  if (a.M <= 16) return launch_bn<16, 6>(a, dev_err, st);
-  if (a.M <= 32) return launch_bn<32, 5>(a, dev_err, st);
-  if (a.M <= 64) return launch_bn<64, 4>(a, dev_err, st);
-  if (a.M <= 128) return launch_bn<128, 3>(a, dev_err, st);
+  // One CTA per SM with the deepest ring that fits (~190 KB of stages): the decode
+  // GEMMs are weight streams, so bytes in flight per SM set their bandwidth.
+  if (a.M <= 16) return launch_bn<16, 10>(a, dev_err, st);
+  if (a.M <= 32) return launch_bn<32, 9>(a, dev_err, st);
+  if (a.M <= 64) return launch_bn<64, 8>(a, dev_err, st);
+  if (a.M <= 128) return launch_bn<128, 6>(a, dev_err, st);
   return launch_bn<256, 4>(a, dev_err, st);
 }
 

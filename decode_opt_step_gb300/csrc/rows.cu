@@ -59,6 +59,34 @@ __global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const 
   ln_store<T>(row, d, g, b, eps, h + (long long)tok * d, red);
 }
 
+// Sum of the split slices of one float4 of a row, in slice order (loads of four
+// slices are issued together; the additions keep the order 0, 1, 2, ...).
+__device__ __forceinline__ float4 sum_slices(const float *p, int split, long long stride) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= split; s += 4) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4 *>(p + (s + u) * stride));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x += v[u].x;
+      acc.y += v[u].y;
+      acc.z += v[u].z;
+      acc.w += v[u].w;
+    }
+  }
+  for (; s < split; ++s) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(p + s * stride));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  return acc;
+}
+
+// One block per row (d % 4 == 0, ldp % 4 == 0): x += sum of slices + bias, then LN.
 template <typename T>
 __global__ void k_resid_ln(const float *partial, int split, long long split_stride, int ldp,
                            const T *bias, float *x, const T *g, const T *b, float eps, T *h,
@@ -66,21 +94,40 @@ __global__ void k_resid_ln(const float *partial, int split, long long split_stri
   extern __shared__ float row[];
   __shared__ float red[33];
   const long long r = blockIdx.x;
-  float *xr = x + r * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < split; ++s) acc += partial[s * split_stride + r * ldp + i];
-    const float v = xr[i] + (acc + to_f<T>(bias[i]));
+  float4 *xr = reinterpret_cast<float4 *>(x + r * d);
+  const float *pr = partial + r * ldp;
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    const float4 acc = sum_slices(pr + 4 * i, split, split_stride);
+    float4 v = xr[i];
+    v.x += acc.x + to_f<T>(bias[4 * i]);
+    v.y += acc.y + to_f<T>(bias[4 * i + 1]);
+    v.z += acc.z + to_f<T>(bias[4 * i + 2]);
+    v.w += acc.w + to_f<T>(bias[4 * i + 3]);
     xr[i] = v;
-    row[i] = v;
+    reinterpret_cast<float4 *>(row)[i] = v;
   }
   __syncthreads();
   ln_store<T>(row, d, g, b, eps, h + r * d, red);
 }
 
+// Element-wise epilogue after a split-K GEMM: four consecutive outputs per thread.
+template <typename T>
+__global__ void k_reduce_epi4(const float *partial, int split, long long split_stride, int ldp,
+                              int M, int N, const __grid_constant__ Epi epi) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int n4 = N / 4;
+  if (e >= (long long)M * n4) return;
+  const int tok = (int)(e / n4), n = (int)(e % n4) * 4;
+  const float4 acc = sum_slices(partial + (long long)tok * ldp + n, split, split_stride);
+  epi_store<T>(epi, 0, tok, n, acc.x);
+  epi_store<T>(epi, 0, tok, n + 1, acc.y);
+  epi_store<T>(epi, 0, tok, n + 2, acc.z);
+  epi_store<T>(epi, 0, tok, n + 3, acc.w);
+}
+
 template <typename T>
 __global__ void k_reduce_epi(const float *partial, int split, long long split_stride, int ldp,
-                             int M, int N, Epi epi) {
+                             int M, int N, const __grid_constant__ Epi epi) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= (long long)M * N) return;
   const int tok = (int)(e / N), n = (int)(e % N);
@@ -236,6 +283,8 @@ cudaError_t launch_resid_ln(int dtype, const float *partial, int split, long lon
                             int ldp, const void *bias, float *x, const void *g, const void *b,
                             float eps, void *h, int rows, int d, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
+  if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
+    return cudaErrorInvalidValue;
   const size_t sm = (size_t)d * sizeof(float);
   if (dtype == 1)
     k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, split, split_stride, ldp,
@@ -252,11 +301,21 @@ cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long l
                               int ldp, int M, int N, const Epi &epi, cudaStream_t st) {
   const long long n = (long long)M * N;
   if (n <= 0) return cudaSuccess;
-  const int blocks = (int)((n + 255) / 256);
-  if (dtype == 1)
-    k_reduce_epi<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
-  else
-    k_reduce_epi<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  const bool vec = N % 4 == 0 && ldp % 4 == 0 && split_stride % 4 == 0 &&
+                   (uintptr_t)partial % 16 == 0;
+  const long long work = vec ? n / 4 : n;
+  const int blocks = (int)((work + 255) / 256);
+  if (vec) {
+    if (dtype == 1)
+      k_reduce_epi4<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+    else
+      k_reduce_epi4<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  } else {
+    if (dtype == 1)
+      k_reduce_epi<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+    else
+      k_reduce_epi<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  }
   return cudaGetLastError();
 }
 

@@ -210,9 +210,10 @@ he_status he_release_workspace(he_engine *h, void *stream);
  * HE_ERR_OOM leaves the engine released and usable (retry later). */
 he_status he_retake_workspace(he_engine *h, void *stream);
 
-/* Per-kernel-class event timing of he_generate (off by default; costs two
- * events per timed launch). */
-he_status he_set_profiling(he_engine *h, int enable);
+/* Per-kernel-class event timing of he_generate: class_mask has bit c set for
+ * every HE_KCLASS_c to time (0 = off, the default).  Costs two events per
+ * timed launch; the totals of the last he_generate appear in he_stats. */
+he_status he_set_profiling(he_engine *h, unsigned class_mask);
 
 /* Fills *s.  Synchronises the engine's events from the last calls first. */
 he_status he_get_stats(he_engine *h, he_stats *s);

@@ -52,6 +52,13 @@ def test_bf16_tiny_teacher_forced(cuda_device):
     assert logit_err < BF16_LOGIT_TOL and lp_err < BF16_LP_TOL, (logit_err, lp_err)
 
 
+@pytest.mark.parametrize("heads", [2, 4, 8])  # head_dim 128, 64, 32
+def test_bf16_head_dims_and_ragged_prompt(cuda_device, heads):
+    cfg = TINY_BF16.with_(n_heads=heads, batch=2, prompt_len=131, gen_len=5, max_pos=160)
+    logit_err, lp_err = teacher_forced_check(cfg, torch)
+    assert logit_err < BF16_LOGIT_TOL and lp_err < BF16_LP_TOL, (heads, logit_err, lp_err)
+
+
 def test_bf16_ragged_batches(cuda_device):
     for b in (1, 17, 33):
         cfg = TINY_BF16.with_(batch=b, prompt_len=70, gen_len=6, max_pos=128)
