@@ -87,8 +87,9 @@ _SIGNATURES = {
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
     "he_last_error": (c_char_p, []),
     "he_version": (c_char_p, []),
-    "he_op_linear": (c_int, [c_int, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
-                             c_int, c_void_p, c_void_p]),
+    "he_op_linear": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
+                             c_int, c_int, c_void_p, c_void_p]),
+    "he_op_tile_weight": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p]),
 }
 
 _lib = None
@@ -316,8 +317,21 @@ class Engine:
             pass
 
 
-def linear(x, w, split: int = 1, stream=None):
-    """y = x w^T in fp32 through libhe's GEMM kernels (he_op_linear)."""
+def tile_weight(w, stream=None):
+    """The tiled streaming layout of a bf16 [N][K] weight (he_op_tile_weight), flat."""
+    import torch
+    lib = load_library()
+    if w.dtype != torch.bfloat16 or not w.is_contiguous():
+        raise TypeError("w must be a contiguous bf16 tensor")
+    out = torch.empty(w.numel(), dtype=torch.bfloat16, device=w.device)
+    _check(lib.he_op_tile_weight(w.data_ptr(), out.data_ptr(), w.shape[0], w.shape[1],
+                                 _stream_handle(torch, stream)))
+    return out
+
+
+def linear(x, w, split: int = 1, stream=None, w_tiled=None):
+    """y = x w^T in fp32 through libhe's GEMM kernels (he_op_linear).  With ``w_tiled``
+    (the output of tile_weight(w)) the GEMM reads the tiled layout instead of w."""
     import torch
     lib = load_library()
     M, K = x.shape
@@ -329,7 +343,8 @@ def linear(x, w, split: int = 1, stream=None):
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     scratch = torch.empty((split, M, N), dtype=torch.float32, device=x.device) if split > 1 else None
     dt = HE_DTYPE_BF16 if x.dtype == torch.bfloat16 else HE_DTYPE_F32
-    _check(lib.he_op_linear(dt, x.data_ptr(), x.stride(0), w.data_ptr(), y.data_ptr(), M, N, K,
+    wp, layout = (w.data_ptr(), 0) if w_tiled is None else (w_tiled.data_ptr(), 1)
+    _check(lib.he_op_linear(dt, x.data_ptr(), x.stride(0), wp, layout, y.data_ptr(), M, N, K,
                             split, scratch.data_ptr() if scratch is not None else None,
                             _stream_handle(torch, stream)))
     return y

@@ -60,6 +60,7 @@ struct he_engine {
   he_allocator alloc{};
 
   bool taken = false, fused = false;
+  bool tiled = false;  // projections hold the tiled layout (bf16 while fused)
   unsigned prof_mask = 0;
   // workspace (released / retaken together)
   Buf kc, vc, x, h, q, ctx, mid, partial, logits, attn_part, ids_in, ids_out, lp_out, logmap;
@@ -208,6 +209,7 @@ void gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_g
   a.M = M;
   a.N = n_groups * group_rows;
   a.K = K;
+  a.w_tiled = h->tiled;
   int split = allow_split ? gemm_pick_split(a, h->num_sms) : 1;
   if (split > kMaxGemmSplit) split = kMaxGemmSplit;
   split = effective_split(K, split);
@@ -256,6 +258,7 @@ int gemm_partial(Ctx &c, int cls, const void *x, int ldx, const void *w, int N, 
   a.n_groups = 1;
   a.group_rows = N;
   a.split = split;
+  a.w_tiled = h->tiled;
   a.epi = e;
   a.epi.split_stride = (long long)M * N;
   Timed t(h, cls, c.st);
@@ -562,6 +565,13 @@ he_status he_destroy(he_engine *h) {
   return HE_OK;
 }
 
+// Which projections the fuse saves and rewrites: bf16 rewrites all six (merged
+// where LoRA-targeted) into the tiled streaming layout; fp32 merges the targeted
+// ones in place.
+static bool fuse_touches(const he_engine *h, int p) {
+  return h->cfg.dtype == HE_DTYPE_BF16 || ((h->cfg.lora_targets >> p) & 1u);
+}
+
 he_status he_fuse_lora(he_engine *h, void *stream) {
   g_err.clear();
   if (!h) return fail(HE_ERR_ARG, "engine is NULL");
@@ -574,29 +584,45 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
   size_t total = 0;
   for (int l = 0; l < c.n_layers; ++l)
     for (int p = 0; p < HE_N_PROJ; ++p)
-      if ((c.lora_targets >> p) & 1u) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
+      if (fuse_touches(h, p)) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
   if (!get(h, h->restore, total, st))
     return fail(HE_ERR_OOM, "LoRA restore copy of %zu bytes failed", total);
   ensure_phase_events(h);
   cudaEventRecord(h->ph[3], st);
   const float scale = c.lora_targets ? c.lora_alpha / (float)c.lora_r : 0.f;
+  const bool bf = c.dtype == HE_DTYPE_BF16;
   size_t off = 0;
   cudaError_t err = cudaSuccess;
+  auto chk = [&](cudaError_t e, int n) {
+    if (e != cudaSuccess && err == cudaSuccess) err = e;
+    h->stats.launches += n;
+  };
   for (int l = 0; l < c.n_layers; ++l) {
     const he_layer_weights &lw = h->layers[l];
     for (int p = 0; p < HE_N_PROJ; ++p) {
-      if (!((c.lora_targets >> p) & 1u)) continue;
-      cudaError_t e = launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p],
-                                       at(h->restore.p, off), rows_of(p), cols_of(p), c.lora_r,
-                                       scale, st);
-      if (e != cudaSuccess && err == cudaSuccess) err = e;
-      h->stats.launches++;
-      off += (size_t)rows_of(p) * cols_of(p) * h->elem;
+      if (!fuse_touches(h, p)) continue;
+      const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
+      void *save = at(h->restore.p, off);
+      const bool lora = (c.lora_targets >> p) & 1u;
+      if (bf) {
+        // save the original bits, then write the merged weight tiled from the copy
+        chk(launch_copy(save, lw.w[p], bytes, st), bytes % 16 ? 2 : 1);
+        chk(launch_fuse_tiled(lw.w[p], save, lora ? lw.lora_a[p] : nullptr,
+                              lora ? lw.lora_b[p] : nullptr, rows_of(p), cols_of(p), c.lora_r,
+                              scale, st),
+            1);
+      } else {
+        chk(launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p], save, rows_of(p),
+                             cols_of(p), c.lora_r, scale, st),
+            1);
+      }
+      off += bytes;
     }
   }
   cudaEventRecord(h->ph[4], st);
   h->fuse_pending = true;
   h->fused = true;
+  h->tiled = bf;
   h->stats.restore_bytes = total;
   if (err != cudaSuccess) return cuda_fail(err, "LoRA fuse launch");
   return HE_OK;
@@ -617,7 +643,7 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
   cudaError_t err = cudaSuccess;
   for (int l = 0; l < c.n_layers; ++l)
     for (int p = 0; p < HE_N_PROJ; ++p) {
-      if (!((c.lora_targets >> p) & 1u)) continue;
+      if (!fuse_touches(h, p)) continue;
       const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
       cudaError_t e = launch_copy(h->layers[l].w[p], at(h->restore.p, off), bytes, st);
       if (e != cudaSuccess && err == cudaSuccess) err = e;
@@ -628,6 +654,7 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
   h->unfuse_pending = true;
   put(h, h->restore, st);
   h->fused = false;
+  h->tiled = false;
   h->stats.restore_bytes = 0;
   if (err != cudaSuccess) return cuda_fail(err, "LoRA restore launch");
   return HE_OK;
@@ -777,9 +804,24 @@ he_status he_get_stats(he_engine *h, he_stats *s) {
 // ---------------------------------------------------------------------------
 // Kernel-level entry (he_ops.h)
 // ---------------------------------------------------------------------------
-he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, float *y, int M, int N,
-                       int K, int split, float *scratch, void *stream) {
+he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream) {
   g_err.clear();
+  if (!w || !out) return fail(HE_ERR_ARG, "NULL buffer");
+  if (N < 128 || K < 64 || N % 128 || K % 64)
+    return fail(HE_ERR_UNSUPPORTED, "tiled layout needs N %% 128 == 0 and K %% 64 == 0");
+  if ((uintptr_t)w % 16 || (uintptr_t)out % 16) return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
+  cudaError_t r = launch_fuse_tiled(out, w, nullptr, nullptr, N, K, 0, 0.f,
+                                    static_cast<cudaStream_t>(stream));
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_tile_weight");
+  return HE_OK;
+}
+
+he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
+                       int M, int N, int K, int split, float *scratch, void *stream) {
+  g_err.clear();
+  if (w_layout != 0 && w_layout != 1) return fail(HE_ERR_ARG, "w_layout must be 0 or 1");
+  if (w_layout == 1 && (dtype != HE_DTYPE_BF16 || N % 128 || K % 64))
+    return fail(HE_ERR_UNSUPPORTED, "tiled weights need bf16, N %% 128 == 0, K %% 64 == 0");
   if (!x || !w || !y) return fail(HE_ERR_ARG, "NULL buffer");
   if (M < 1 || N < 1 || K < 1 || ldx < K) return fail(HE_ERR_ARG, "bad sizes");
   if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
@@ -801,6 +843,7 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, float *
   a.N = N;
   a.K = K;
   a.split = split;
+  a.w_tiled = w_layout;
   Epi e{};
   e.kind = EPI_STORE_F32;
   e.partial = y;

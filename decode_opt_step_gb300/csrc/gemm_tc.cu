@@ -16,6 +16,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -53,13 +55,17 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
 };
 
-template <int BN, int STAGES>
+struct WTiles {
+  const bf16 *p[3];  // tiled weights of each row group (ABULK)
+  int kt;            // 64-wide k tiles per 128-row tile row
+};
+
+template <int BN, int STAGES, bool ABULK>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
               int tiles_per_group, int M, int N, int kb_total, int kb_per_split,
-              const __grid_constant__ Epi epi,
-              int *dev_err) {
+              const __grid_constant__ Epi epi, WTiles wt, int *dev_err) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -100,8 +106,11 @@ __global__ void __launch_bounds__(192, 1)
     const int group = m_tile / tiles_per_group;
     const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
     const int m_row = (m_tile - group * tiles_per_group) * BM;
-    prefetch_tmap(tw);
+    if (!ABULK) prefetch_tmap(tw);
     prefetch_tmap(&tm_x);
+    // tiled weights: this CTA's k-blocks of tile row `m_row / BM` are contiguous
+    const bf16 *wtile = ABULK ? wt.p[group] + ((long long)(m_row / BM) * wt.kt + kb0) * (BM * BK)
+                              : nullptr;
     int issued = 0;
     for (int i = 0; i < nkb; ++i) {
       const int s = i % STAGES;
@@ -113,7 +122,10 @@ __global__ void __launch_bounds__(192, 1)
       if (*(volatile int *)abort_flag) break;
       mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
       const int kc = (kb0 + i) * BK;
-      tma_load_2d(smA + s * A_BYTES, tw, &full[s], kc, m_row);
+      if (ABULK)
+        bulk_load(smA + s * A_BYTES, wtile + (long long)i * (BM * BK), A_BYTES, &full[s]);
+      else
+        tma_load_2d(smA + s * A_BYTES, tw, &full[s], kc, m_row);
       tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kc, n_tile * BN);
       issued = i + 1;
     }
@@ -202,18 +214,24 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int 
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool ABULK>
 cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   using C = Cfg<BN, STAGES>;
   CUtensorMap tw[3], tx;
+  WTiles wt{};
+  memset(tw, 0, sizeof tw);
   for (int g = 0; g < 3; ++g) {
     const void *p = a.w[g < a.n_groups ? g : 0];
-    if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
+    if (ABULK)
+      wt.p[g] = static_cast<const bf16 *>(p);
+    else if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM))
+      return cudaErrorInvalidValue;
   }
+  wt.kt = a.K / BK;
   if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN)) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, ABULK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -223,9 +241,9 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   if (effective_split(a.K, a.split) != a.split) return cudaErrorInvalidValue;
   const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
   dim3 grid(a.N / BM + (a.N % BM != 0), (a.M + BN - 1) / BN, a.split);
-  k_gemm_tc<BN, STAGES><<<grid, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, tiles_per_group,
-                                                    a.M, a.N, kb_total, kb_per_split, a.epi,
-                                                    dev_err);
+  k_gemm_tc<BN, STAGES, ABULK><<<grid, 192, C::SMEM, st>>>(
+      tw[0], tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total, kb_per_split, a.epi, wt,
+      dev_err);
   return cudaGetLastError();
 }
 
@@ -241,11 +259,22 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   if (a.epi.kind == EPI_QKV && a.epi.d_model % BM) return cudaErrorInvalidValue;
   // One CTA per SM with the deepest ring that fits (~190 KB of stages): the decode
   // GEMMs are weight streams, so bytes in flight per SM set their bandwidth.
-  if (a.M <= 16) return launch_bn<16, 10>(a, dev_err, st);
-  if (a.M <= 32) return launch_bn<32, 9>(a, dev_err, st);
-  if (a.M <= 64) return launch_bn<64, 8>(a, dev_err, st);
-  if (a.M <= 128) return launch_bn<128, 6>(a, dev_err, st);
-  return launch_bn<256, 4>(a, dev_err, st);
+  if (a.w_tiled) {
+    // the tiled layout covers whole 128 x 64 tiles only
+    if (a.group_rows % BM || a.K % BK) return cudaErrorInvalidValue;
+    for (int g = 0; g < a.n_groups; ++g)
+      if ((uintptr_t)a.w[g] % 16) return cudaErrorInvalidValue;
+    if (a.M <= 16) return launch_bn<16, 10, true>(a, dev_err, st);
+    if (a.M <= 32) return launch_bn<32, 9, true>(a, dev_err, st);
+    if (a.M <= 64) return launch_bn<64, 8, true>(a, dev_err, st);
+    if (a.M <= 128) return launch_bn<128, 6, true>(a, dev_err, st);
+    return launch_bn<256, 4, true>(a, dev_err, st);
+  }
+  if (a.M <= 16) return launch_bn<16, 10, false>(a, dev_err, st);
+  if (a.M <= 32) return launch_bn<32, 9, false>(a, dev_err, st);
+  if (a.M <= 64) return launch_bn<64, 8, false>(a, dev_err, st);
+  if (a.M <= 128) return launch_bn<128, 6, false>(a, dev_err, st);
+  return launch_bn<256, 4, false>(a, dev_err, st);
 }
 
 }  // namespace he

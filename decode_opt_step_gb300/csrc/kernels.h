@@ -38,6 +38,16 @@ struct Epi {
   float q_scale;
 };
 
+// Tiled weight layout used while LoRA is fused (bf16 only): W [N][K] with
+// N % 128 == 0 and K % 64 == 0 is stored as (N/128) x (K/64) tiles of 128 x 64,
+// tile (mt, kt) contiguous at element (mt * K/64 + kt) * 8192; inside a tile, row r
+// occupies 128 bytes whose 16-byte chunk c sits at slot c ^ (r % 8) -- the image
+// the tensor cores read with 128-byte swizzling, so one bulk copy fills a stage.
+inline long long tiled_index(long long n, long long k, long long K) {
+  return ((n / 128) * (K / 64) + k / 64) * 8192 + (n % 128) * 64 +
+         ((((k % 64) / 8) ^ (n % 8)) * 8) + (k % 8);
+}
+
 struct GemmArgs {
   int dtype;             // HE_DTYPE_F32 / HE_DTYPE_BF16
   const void *x;         // [M][ldx] activations (tokens x K), storage type
@@ -46,6 +56,7 @@ struct GemmArgs {
   int n_groups, group_rows;
   int M, N, K;           // tokens, output features (= n_groups * group_rows), reduction
   int split;             // split-K factor (EPI_PARTIAL writes split slices)
+  int w_tiled;           // bf16 only: w[] hold the tiled layout above
   Epi epi;
 };
 
@@ -112,6 +123,10 @@ cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const 
 // W <- round(W + scale * B A) after saving W's bits to `save`.
 cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,
                              int rows, int cols, int r, float scale, cudaStream_t st);
+// bf16: out (tiled layout) <- round(src + scale * B A), src row-major [rows][cols];
+// A / B may be null (then a plain re-tiling).  out and src must not overlap.
+cudaError_t launch_fuse_tiled(void *out, const void *src, const void *a, const void *bm, int rows,
+                              int cols, int r, float scale, cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 
 }  // namespace he

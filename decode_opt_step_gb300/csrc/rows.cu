@@ -247,6 +247,40 @@ __global__ void k_lora_fuse(T *w, const T *A, const T *Bm, T *save, int rows, in
   for (int e = 0; e < 8; ++e) wp[e] = from_f<T>(to_f<T>(wv[e]) + scale * delta[e]);
 }
 
+// One 16-byte chunk of the tiled output per thread: chunk q of tile t holds row
+// r = (q % 1024) / 8, logical 16-byte column chunk (q % 8) ^ (r % 8).
+__global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows,
+                             int cols, int r, float scale) {
+  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nchunks = (long long)rows * cols / 8;
+  if (q >= nchunks) return;
+  const int KT = cols / 64;
+  const long long t = q >> 10;
+  const int rr = (int)((q & 1023) >> 3), slot = (int)(q & 7);
+  const int c = slot ^ (rr & 7);
+  const int n = (int)(t / KT) * 128 + rr;
+  const int k0 = (int)(t % KT) * 64 + c * 8;
+  const uint4 raw = *reinterpret_cast<const uint4 *>(src + (long long)n * cols + k0);
+  if (!A) {
+    out[q] = raw;
+    return;
+  }
+  const bf16 *wv = reinterpret_cast<const bf16 *>(&raw);
+  float delta[8] = {};
+  for (int j = 0; j < r; ++j) {
+    const float bj = __bfloat162float(Bm[(long long)n * r + j]);
+    const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
+    const bf16 *ap = reinterpret_cast<const bf16 *>(&av);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
+  }
+  uint4 res;
+  bf16 *rp = reinterpret_cast<bf16 *>(&res);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rp[e] = __float2bfloat16_rn(__bfloat162float(wv[e]) + scale * delta[e]);
+  out[q] = res;
+}
+
 __global__ void k_copy16(uint4 *dst, const uint4 *src, long long n16) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
        i += (long long)gridDim.x * blockDim.x)
@@ -339,6 +373,16 @@ cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, 
   else
     k_lora_fuse<float><<<blocks, 256, 0, st>>>((float *)w, (const float *)a, (const float *)bm,
                                                (float *)save, rows, cols, r, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fuse_tiled(void *out, const void *src, const void *a, const void *bm, int rows,
+                              int cols, int r, float scale, cudaStream_t st) {
+  if (rows % 128 || cols % 64) return cudaErrorInvalidValue;
+  const long long n = (long long)rows * cols / 8;
+  k_fuse_tiled<<<(int)((n + 255) / 256), 256, 0, st>>>((uint4 *)out, (const bf16 *)src,
+                                                      (const bf16 *)a, (const bf16 *)bm, rows,
+                                                      cols, r, scale);
   return cudaGetLastError();
 }
 

@@ -18,12 +18,27 @@ extern "C" {
  * multiplies the current tokens' activations with every weight matrix).
  * dtype HE_DTYPE_BF16 runs the tcgen05 tensor-core kernel (K and ldx multiples
  * of 8, x and w 16-byte aligned); HE_DTYPE_F32 runs the fp32 CUDA-core kernel.
- * x has row stride ldx >= K; w is dense [N][K].  split >= 1 splits K into
+ * x has row stride ldx >= K; w is dense [N][K] (w_layout 0) or in the tiled
+ * streaming layout below (w_layout 1, bf16 only).  split >= 1 splits K into
  * slices of whole 64-wide blocks (no empty slice allowed) whose fp32 partial
  * sums go to scratch [split][M][N] and are then added in slice order.  All
  * pointers are device memory; asynchronous on `stream`. */
-he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, float *y, int M, int N,
-                       int K, int split, float *scratch, void *stream);
+he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
+                       int M, int N, int K, int split, float *scratch, void *stream);
+
+/* The streaming layout he_fuse_lora writes the bf16 projections in while LoRA
+ * is fused ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of
+ * ChatGPT-like Models at All Scales", §3.4 "Inference Mode: Generation Phase
+ * Optimizations", Optimization 1: the inference kernels lay weights out for
+ * bandwidth).  w_layout 1 in he_op_linear means w holds this layout.  For a
+ * bf16 W [N][K] with N % 128 == 0 and K % 64 == 0, element (n, k) sits at index
+ *   ((n / 128) * (K / 64) + k / 64) * 8192 + (n % 128) * 64
+ *     + (((k % 64) / 8) ^ (n % 8)) * 8 + k % 8,
+ * i.e. 128 x 64 tiles stored contiguously, k-tiles of a tile row consecutive,
+ * each tile in the 128-byte-swizzled order the tensor cores read, so one bulk
+ * copy moves a whole tile.  he_op_tile_weight writes out (N*K elements, no
+ * overlap with w) from the row-major w; asynchronous on `stream`. */
+he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream);
 
 #ifdef __cplusplus
 }

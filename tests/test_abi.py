@@ -73,7 +73,8 @@ def test_argument_errors_without_gpu(lib):
     assert lib.he_retake_workspace(None, None) == he.HE_ERR_ARG
     assert lib.he_check(None, None) == he.HE_ERR_ARG
     assert lib.he_get_stats(None, None) == he.HE_ERR_ARG
-    assert lib.he_op_linear(1, None, 8, None, None, 1, 1, 8, 1, None, None) == he.HE_ERR_ARG
+    assert lib.he_op_linear(1, None, 8, None, 0, None, 1, 1, 8, 1, None, None) == he.HE_ERR_ARG
+    assert lib.he_op_tile_weight(None, None, 128, 64, None) == he.HE_ERR_ARG
     assert b"sm_103a" in lib.he_version()
 
 

@@ -77,3 +77,35 @@ def test_linear_rejects_bad_arguments(cuda_device):
     w = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(he.HeError):
         he.linear(x, w, split=3)  # K = 64 has one block: no 3-way split
+
+
+def tiled_positions(N, K):
+    """Index of element (n, k) in the tiled streaming layout (as stated in he_ops.h)."""
+    n = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    return (((n // 128) * (K // 64) + k // 64) * 8192 + (n % 128) * 64
+            + (((k % 64) // 8) ^ (n % 8)) * 8 + k % 8)
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (256, 192), (384, 1024)])
+def test_tile_weight_layout(cuda_device, N, K):
+    g = torch.Generator().manual_seed(N + K)
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    t = he.tile_weight(w)
+    torch.cuda.synchronize()
+    flat = t.view(torch.int16).cpu().numpy()
+    ref = np.empty(N * K, np.int16)
+    ref[tiled_positions(N, K).ravel()] = w.view(torch.int16).cpu().numpy().ravel()
+    assert np.array_equal(flat, ref)
+
+
+@pytest.mark.parametrize("M,N,K,split", [(1, 128, 64, 1), (17, 384, 512, 1), (128, 1280, 1024, 1),
+                                         (128, 256, 2048, 4), (300, 256, 640, 1), (64, 640, 1280, 5)])
+def test_linear_bf16_tiled_weights(cuda_device, M, N, K, split):
+    g = torch.Generator().manual_seed(M + 3 * N + 7 * K)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w, split=split, w_tiled=he.tile_weight(w))
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, K)).all(), err.max()

@@ -99,7 +99,11 @@ def test_fused_weight_is_rounded_merge(cuda_device):
         for name in ("wq", "w1", "w2"):
             a, b = inputs.lora[li][name]
             exact = merge_lora(inputs.layers[li][name], a, b, cfg.lora_alpha, cfg.lora_r)
-            got = w["layers"][li][name].float().cpu().numpy()
+            t = w["layers"][li][name]
+            # while fused, bf16 projections hold the tiled streaming layout
+            flat = t.reshape(-1).float().cpu().numpy()
+            from tests.test_gpu_kernels import tiled_positions
+            got = flat[tiled_positions(*t.shape)]
             # one bf16 rounding of the fp32 merge: relative error <= 2^-8
             assert (np.abs(got - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30).all(), name
     eng.unfuse_lora()
