@@ -331,7 +331,9 @@ def tile_weight(w, stream=None):
 
 def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     """y = x w^T in fp32 through libhe's GEMM kernels (he_op_linear).  With ``w_tiled``
-    (the output of tile_weight(w)) the GEMM reads the tiled layout instead of w."""
+    (the output of tile_weight(w)) the GEMM reads the tiled layout instead of w.
+    split >= 1: split-K; split == 0: stream-K on the default CTA count; split < 0:
+    stream-K on -split CTAs."""
     import torch
     lib = load_library()
     M, K = x.shape
@@ -341,7 +343,9 @@ def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     if x.stride(1) != 1 or not w.is_contiguous():
         raise ValueError("x rows and w must be dense")
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    scratch = torch.empty((split, M, N), dtype=torch.float32, device=x.device) if split > 1 else None
+    slices = 16 if split <= 0 else split  # split <= 0: stream-K (up to 16 slices per tile)
+    scratch = (torch.empty((slices, M, N), dtype=torch.float32, device=x.device)
+               if slices > 1 else None)
     dt = HE_DTYPE_BF16 if x.dtype == torch.bfloat16 else HE_DTYPE_F32
     wp, layout = (w.data_ptr(), 0) if w_tiled is None else (w_tiled.data_ptr(), 1)
     _check(lib.he_op_linear(dt, x.data_ptr(), x.stride(0), wp, layout, y.data_ptr(), M, N, K,

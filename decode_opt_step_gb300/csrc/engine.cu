@@ -195,9 +195,18 @@ struct Ctx {
 inline const char *at(const void *p, size_t off) { return static_cast<const char *>(p) + off; }
 inline char *at(void *p, size_t off) { return static_cast<char *>(p) + off; }
 
-// GEMM (+ split-K reduction for element-wise epilogues).
-void gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
-          int group_rows, int M, int K, Epi epi, bool allow_split) {
+// Decode projections on bf16 run the persistent stream-K kernel when the shape
+// allows (whole 128 x 64 tiles, one token tile).
+bool use_stream_k(const he_engine *h, int M, int N, int K, bool decode) {
+  return decode && h->cfg.dtype == HE_DTYPE_BF16 && M <= 256 && N % 128 == 0 && K % 64 == 0;
+}
+
+// One projection GEMM.  Element-wise epilogues (QKV, ReLU) are completed here
+// (split-K / stream-K slices reduced by a second kernel); for EPI_PARTIAL the
+// fp32 slices stay in h->partial and the returned SliceInfo tells the row
+// consumer how to add them.
+SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
+               int group_rows, int M, int K, Epi epi, bool decode) {
   he_engine *h = c.h;
   GemmArgs a{};
   a.dtype = h->cfg.dtype;
@@ -210,60 +219,39 @@ void gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_g
   a.N = n_groups * group_rows;
   a.K = K;
   a.w_tiled = h->tiled;
-  int split = allow_split ? gemm_pick_split(a, h->num_sms) : 1;
+  SliceInfo si{1, 0, 0, 0};
+  float *part = static_cast<float *>(h->partial.p);
+  const long long stride = (long long)M * a.N;
+  Timed t(h, cls, c.st);
+  if (use_stream_k(h, M, a.N, K, decode)) {
+    const int P = sk_ctas(a, h->num_sms);
+    si = SliceInfo{0, (long long)(a.N / 128) * (K / 64), K / 64, P};
+    a.split = 1;
+    a.epi = epi;
+    c.check(launch_gemm_sk(a, P, part, stride, static_cast<int *>(h->err.p), c.st), 1);
+    if (epi.kind != EPI_PARTIAL)
+      c.check(launch_sk_reduce_epi(a.dtype, part, si, stride, a.N, M, a.N, epi, c.st), 1);
+    return si;
+  }
+  int split = decode ? gemm_pick_split(a, h->num_sms) : 1;
   if (split > kMaxGemmSplit) split = kMaxGemmSplit;
   split = effective_split(K, split);
   a.split = split;
-  const bool via_partial = split > 1 && epi.kind != EPI_PARTIAL;
-  if (via_partial) {
+  si.split = split;
+  if (epi.kind == EPI_PARTIAL || split > 1) {
     Epi pe = epi;
     pe.kind = EPI_PARTIAL;
-    pe.partial = static_cast<float *>(h->partial.p);
+    pe.partial = part;
     pe.ldp = a.N;
-    pe.split_stride = (long long)M * a.N;
+    pe.split_stride = stride;
     a.epi = pe;
   } else {
     a.epi = epi;
-    if (epi.kind == EPI_PARTIAL) a.epi.split_stride = (long long)M * epi.ldp;
   }
-  {
-    Timed t(h, cls, c.st);
-    c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
-    if (via_partial)
-      c.check(launch_reduce_epi(h->cfg.dtype, static_cast<float *>(h->partial.p), split,
-                                (long long)M * a.N, a.N, M, a.N, epi, c.st),
-              1);
-  }
-}
-
-// Returns the split used for an EPI_PARTIAL GEMM (the row kernel must know it).
-int gemm_partial(Ctx &c, int cls, const void *x, int ldx, const void *w, int N, int M, int K,
-                 bool allow_split) {
-  he_engine *h = c.h;
-  GemmArgs a{};
-  a.dtype = h->cfg.dtype;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  int split = allow_split ? gemm_pick_split(a, h->num_sms) : 1;
-  if (split > kMaxGemmSplit) split = kMaxGemmSplit;
-  split = effective_split(K, split);
-  Epi e{};
-  e.kind = EPI_PARTIAL;
-  e.partial = static_cast<float *>(h->partial.p);
-  e.ldp = N;
-  a.x = x;
-  a.ldx = ldx;
-  a.w[0] = w;
-  a.n_groups = 1;
-  a.group_rows = N;
-  a.split = split;
-  a.w_tiled = h->tiled;
-  a.epi = e;
-  a.epi.split_stride = (long long)M * N;
-  Timed t(h, cls, c.st);
   c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
-  return split;
+  if (epi.kind != EPI_PARTIAL && split > 1)
+    c.check(launch_reduce_epi(a.dtype, part, split, stride, a.N, M, a.N, epi, c.st), 1);
+  return si;
 }
 
 Epi qkv_epi(he_engine *h, int layer, int tok_per_seq, int pos0) {
@@ -302,6 +290,8 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   // LN1 + QKV (+ KV append at the tokens' positions)
   const void *wqkv[3] = {lw.w[HE_PROJ_Q], lw.w[HE_PROJ_K], lw.w[HE_PROJ_V]};
   gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec);
+  Epi ep{};
+  ep.kind = EPI_PARTIAL;
   // attention
   const size_t lay = (size_t)l * h->kv_layer_elems() * h->elem;
   if (prefill) {
@@ -320,10 +310,11 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
             split > 1 ? 2 : 1);
   }
   // out projection -> partials; + bo + residual; LN2
-  int s = gemm_partial(c, cls_g, h->ctx.p, d, lw.w[HE_PROJ_O], d, M, d, dec);
+  const void *wo[1] = {lw.w[HE_PROJ_O]};
+  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec);
   {
     Timed t(h, HE_KCLASS_NORM, c.st);
-    c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), s, (long long)M * d, d,
+    c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                             lw.b[HE_PROJ_O], static_cast<float *>(h->x.p), lw.ln2_g, lw.ln2_b,
                             cf.ln_eps, h->h.p, M, d, c.st),
             1);
@@ -337,12 +328,13 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   const void *w1[1] = {lw.w[HE_PROJ_FC1]};
   gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec);
   // fc2 -> partials; + b2 + residual; next LN
-  s = gemm_partial(c, cls_g, h->mid.p, cf.ffn, lw.w[HE_PROJ_FC2], d, M, cf.ffn, dec);
+  const void *w2[1] = {lw.w[HE_PROJ_FC2]};
+  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec);
   const bool last = l == cf.n_layers - 1;
   const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
   const void *bb = last ? h->lnf_b : h->layers[l + 1].ln1_b;
   Timed t(h, HE_KCLASS_NORM, c.st);
-  c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), s, (long long)M * d, d,
+  c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                           lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
                           h->h.p, M, d, c.st),
           1);
@@ -827,11 +819,49 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
   if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
   if (dtype == HE_DTYPE_BF16 && (K % 8 || ldx % 8))
     return fail(HE_ERR_UNSUPPORTED, "bf16 needs K and ldx multiples of 8");
-  if (split < 1) return fail(HE_ERR_ARG, "split must be >= 1");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (split <= 0) {
+    // stream-K: the persistent kernel of the decode projections
+    if (dtype != HE_DTYPE_BF16 || M > 256 || N % 128 || K % 64)
+      return fail(HE_ERR_UNSUPPORTED, "stream-K needs bf16, M <= 256, N %% 128 == 0, K %% 64 == 0");
+    if (!scratch) return fail(HE_ERR_ARG, "stream-K needs scratch");
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    GemmArgs a{};
+    a.dtype = dtype;
+    a.x = x;
+    a.ldx = ldx;
+    a.w[0] = w;
+    a.n_groups = 1;
+    a.group_rows = N;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.split = 1;
+    a.w_tiled = w_layout;
+    int P = sk_ctas(a, sms);
+    if (split < 0) {
+      const long long T = N / 128, U = T * (K / 64);
+      if (-split > U || -split > 15 * T)
+        return fail(HE_ERR_ARG, "stream-K CTA count %d above min(units, 15 * tiles)", -split);
+      P = -split;
+    }
+    Epi e{};
+    e.kind = EPI_STORE_F32;
+    e.partial = y;
+    e.ldp = N;
+    a.epi = e;
+    const SliceInfo si{0, (long long)(N / 128) * (K / 64), K / 64, P};
+    cudaError_t r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
+    if (r == cudaSuccess)
+      r = launch_sk_reduce_epi(dtype, scratch, si, (long long)M * N, N, M, N, e, st);
+    if (r != cudaSuccess) return cuda_fail(r, "he_op_linear (stream-K)");
+    return HE_OK;
+  }
   if (effective_split(K, split) != split)
     return fail(HE_ERR_ARG, "split %d leaves an empty K slice (K=%d)", split, K);
   if (split > 1 && !scratch) return fail(HE_ERR_ARG, "split > 1 needs scratch");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   GemmArgs a{};
   a.dtype = dtype;
   a.x = x;

@@ -1,0 +1,294 @@
+// Persistent stream-K bf16 GEMM for the decode projections (tcgen05 + TMEM).
+//
+// In decode every SM has to stream weights all the time for the projections to
+// run at HBM speed (one SM moves about 1/152 of the HBM bandwidth), so tiles
+// are not handed out whole: the T x KB (tile, 64-wide k-block) units of one
+// GEMM are cut into P equal contiguous runs, one per CTA (P = SM count).  A run
+// crosses tile boundaries; each piece of a tile it covers is a "segment".
+// Segments accumulate in TMEM (two accumulators, so the epilogue of one segment
+// overlaps the MMAs of the next) and are written as fp32 slices
+// partial[slot][tok][n], slot = CTA index - first CTA of the tile; the consumer
+// adds the slices of a tile in slot order (sk_segments gives how many).  A tile
+// covered by a single segment gets the element-wise epilogue directly.
+//
+// Warp roles as in gemm_tc.cu: warps 0-3 epilogue, warp 4 loads (bulk copies of
+// tiled weights or TMA of row-major ones, TMA of the activations), warp 5 owns
+// TMEM and issues the MMAs.  All waits are bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace he {
+
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows);
+
+namespace {
+
+constexpr int BM = 128, BK = 64, UMMA_K = 16, A_BYTES = BM * BK * 2;
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32u : c <= 64 ? 64u : c <= 128 ? 128u : c <= 256 ? 256u : 512u; }
+
+template <int BN, int STAGES>
+struct SkCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t TMEM_COLS = pow2_cols(2 * BN);
+};
+
+struct SkArgs {
+  const bf16 *wt[3];     // tiled weights per row group (tiled == 1)
+  int tiled;
+  int tiles_per_group;   // 128-row tiles per group (multiple groups only)
+  int n_groups;
+  int M, N, KB;          // tokens, output features, 64-wide k-blocks
+  long long U;           // units = tiles * KB
+  float *slices;         // fp32 slices [slot][M][N]
+  long long slice_stride;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+              const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
+              const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, int *dev_err) {
+  using C = SkCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t *smA = base;
+  uint8_t *smB = base + STAGES * A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *acc_full = empty + STAGES;   // [2]
+  uint64_t *acc_empty = acc_full + 2;    // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = gridDim.x, c = blockIdx.x;
+  const long long u_begin = (long long)c * a.U / P, u_end = (long long)(c + 1) * a.U / P;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4 && lane == 0) {
+    // ---------------- loads ----------------
+    if (!a.tiled) {
+      prefetch_tmap(&tm_w0);
+      if (a.n_groups > 1) prefetch_tmap(&tm_w1);
+      if (a.n_groups > 2) prefetch_tmap(&tm_w2);
+    }
+    prefetch_tmap(&tm_x);
+    long long issued = 0;
+    bool stop = false;
+    for (long long u = u_begin; u < u_end && !stop; ++u) {
+      const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
+      const int group = a.n_groups > 1 ? t / a.tiles_per_group : 0;
+      const int lt = t - group * (a.n_groups > 1 ? a.tiles_per_group : 0);
+      const long long i = u - u_begin;
+      const int s = (int)(i % STAGES);
+      if (i >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      if (a.tiled) {
+        const bf16 *src = a.wt[group] + ((long long)lt * a.KB + kb) * (BM * BK);
+        bulk_load(smA + s * A_BYTES, src, A_BYTES, &full[s]);
+      } else {
+        const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
+        tma_load_2d(smA + s * A_BYTES, tw, &full[s], kb * BK, lt * BM);
+      }
+      tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kb * BK, 0);
+      issued = i + 1;
+    }
+    for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+      if (!mbar_wait_bounded(&full[i % STAGES], (uint32_t)((i / STAGES) & 1)))
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+  } else if (warp == 5 && lane == 0) {
+    // ---------------- MMA ----------------
+    constexpr uint32_t idesc = idesc_bf16(BN);
+    int seg = 0;
+    bool ok = true;
+    for (long long u = u_begin; u < u_end && ok;) {
+      const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
+      const int n = (int)min((long long)(a.KB - kb0), u_end - u);
+      const int buf = seg & 1;
+      if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc = tmem_base + (uint32_t)(buf * BN);
+      for (int j = 0; j < n; ++j) {
+        const long long i = u - u_begin + j;
+        const int s = (int)(i % STAGES);
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / STAGES) & 1)) ||
+            *(volatile int *)abort_flag) {
+          *(volatile int *)abort_flag = 1;
+          set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smA + s * A_BYTES);
+        const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+          tc_mma_f16(acc, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
+                     idesc, (j | kk) != 0);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
+      u += n;
+      ++seg;
+    }
+  } else if (warp < 4) {
+    // ---------------- epilogue ----------------
+    int seg = 0;
+    for (long long u = u_begin; u < u_end;) {
+      const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
+      const int n = (int)min((long long)(a.KB - kb0), u_end - u);
+      const int buf = seg & 1;
+      const bool ok = !*(volatile int *)abort_flag &&
+                      mbar_wait_bounded(&acc_full[buf], (uint32_t)((seg >> 1) & 1));
+      if (!ok) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+      tc_fence_after();
+      const bool live = ok && !*(volatile int *)abort_flag;
+      int cf, S;
+      sk_segments(t, a.KB, P, a.U, &cf, &S);
+      const int slot = c - cf;
+      const bool direct = S == 1 && epi.kind != EPI_PARTIAL;
+      const int row = t * BM + warp * 32 + lane;
+      const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tl + c0, v);
+        if (live && row < a.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c0 + j;
+            if (tok < a.M) {
+              if (direct)
+                epi_store<bf16>(epi, 0, tok, row, v[j]);
+              else
+                a.slices[(long long)slot * a.slice_stride + (long long)tok * a.N + row] = v[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[buf])) : "memory");
+      u += n;
+      ++seg;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slice_stride,
+                         int *dev_err, cudaStream_t st) {
+  using C = SkCfg<BN, STAGES>;
+  CUtensorMap tw[3], tx;
+  memset(tw, 0, sizeof tw);
+  SkArgs a{};
+  a.tiled = g.w_tiled;
+  a.n_groups = g.n_groups;
+  a.tiles_per_group = g.group_rows / BM;
+  for (int i = 0; i < 3; ++i) {
+    const void *p = g.w[i < g.n_groups ? i : 0];
+    if (g.w_tiled)
+      a.wt[i] = static_cast<const bf16 *>(p);
+    else if (i < g.n_groups && !make_tmap_bf16(&tw[i], p, g.group_rows, g.K, g.K, BM))
+      return cudaErrorInvalidValue;
+  }
+  if (!make_tmap_bf16(&tx, g.x, g.M, g.K, g.ldx, BN)) return cudaErrorInvalidValue;
+  a.M = g.M;
+  a.N = g.N;
+  a.KB = g.K / BK;
+  a.U = (long long)(g.N / BM) * a.KB;
+  a.slices = slices;
+  a.slice_stride = slice_stride;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_gemm_sk<BN, STAGES><<<P, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// One run per SM, at most U runs, and at most 15 runs per tile so that a tile
+// never has more than 16 slices.
+int sk_ctas(const GemmArgs &g, int num_sms) {
+  const long long T = g.N / 128, U = T * (g.K / 64);
+  long long P = num_sms;
+  if (P > U) P = U;
+  if (P > 15 * T) P = 15 * T;
+  return (int)P;
+}
+
+cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long slice_stride,
+                           int *dev_err, cudaStream_t st) {
+  // One row tile of tokens (M <= 256), whole 128 x 64 tiles, fp32 slices in epi.partial.
+  if (g.dtype != 1 || g.M < 1 || g.M > 256 || g.N % BM || g.K % BK || g.ldx % 8)
+    return cudaErrorInvalidValue;
+  if (g.n_groups < 1 || g.n_groups > 3 || g.n_groups * g.group_rows != g.N) return cudaErrorInvalidValue;
+  if (g.epi.kind == EPI_QKV && g.epi.d_model % BM) return cudaErrorInvalidValue;
+  if (!slices || P < 1 || slice_stride < (long long)g.M * g.N) return cudaErrorInvalidValue;
+  if (g.M <= 16) return launch_sk_bn<16, 10>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 32) return launch_sk_bn<32, 9>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 64) return launch_sk_bn<64, 8>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 128) return launch_sk_bn<128, 6>(g, P, slices, slice_stride, dev_err, st);
+  return launch_sk_bn<256, 4>(g, P, slices, slice_stride, dev_err, st);
+}
+
+}  // namespace he

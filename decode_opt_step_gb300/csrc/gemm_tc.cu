@@ -249,6 +249,10 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
 
 }  // namespace
 
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows) {
+  return make_tmap(m, ptr, rows, cols, ld, box_rows);
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   // Shape rules of this kernel (checked again by the engine at create time):
   // K rows 16-byte aligned (K % 8), row groups whole tiles, pointers 16-byte aligned.

@@ -75,17 +75,57 @@ inline int effective_split(int K, int split) {
   return (kb + per - 1) / per;
 }
 
+// Stream-K bookkeeping.  The U = T * KB units (tile, 64-wide k-block) of a GEMM are
+// cut into P contiguous runs, run c = [floor(c U / P), floor((c+1) U / P)), so unit x
+// belongs to run floor(((x + 1) P - 1) / U).  Tile t is covered by runs c_first..c_last;
+// run c writes its part of tile t to slice c - c_first, and S = c_last - c_first + 1
+// slices make up the tile.
+__host__ __device__ inline void sk_segments(int t, int KB, int P, long long U, int *c_first,
+                                            int *S) {
+  const long long x0 = (long long)t * KB, x1 = x0 + KB - 1;
+  const int cf = (int)(((x0 + 1) * P - 1) / U);
+  const int cl = (int)(((x1 + 1) * P - 1) / U);
+  *c_first = cf;
+  *S = cl - cf + 1;
+}
+
+// How the fp32 slices of a GEMM's output are organised for its consumer: a uniform
+// split-K (sk_U == 0: `split` slices everywhere) or stream-K (per 128-column tile).
+struct SliceInfo {
+  int split;       // uniform slice count (sk_U == 0)
+  long long sk_U;  // stream-K units, 0 if not stream-K
+  int sk_KB, sk_P;
+  __host__ __device__ int slices(int col) const {
+    if (sk_U == 0) return split;
+    int cf, S;
+    sk_segments(col / 128, sk_KB, sk_P, sk_U, &cf, &S);
+    return S;
+  }
+};
+
 // Result codes of the launchers (cudaError_t values pass through).
 cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st);
+
+// Persistent stream-K tcgen05 GEMM (bf16, M <= 256 tokens, N % 128 == 0, K % 64 == 0)
+// on P CTAs; writes fp32 slices [slot][M][N] (slot stride slice_stride) except for
+// tiles covered by one run under an element-wise a.epi, which are stored directly.
+int sk_ctas(const GemmArgs &a, int num_sms);
+cudaError_t launch_gemm_sk(const GemmArgs &a, int P, float *slices, long long slice_stride,
+                           int *dev_err, cudaStream_t st);
 int gemm_pick_split(const GemmArgs &a, int num_sms);  // heuristic for decode shapes
 
 cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long long split_stride,
                               int ldp, int M, int N, const Epi &epi, cudaStream_t st);
+// Element-wise epilogue over stream-K slices (tiles with one slice were stored already).
+cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInfo &si,
+                                 long long split_stride, int ldp, int M, int N, const Epi &epi,
+                                 cudaStream_t st);
 
 // x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type).
-cudaError_t launch_resid_ln(int dtype, const float *partial, int split, long long split_stride,
-                            int ldp, const void *bias, float *x, const void *g, const void *b,
-                            float eps, void *h, int rows, int d, cudaStream_t st);
+cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
+                            long long split_stride, int ldp, const void *bias, float *x,
+                            const void *g, const void *b, float eps, void *h, int rows, int d,
+                            cudaStream_t st);
 
 // x[tok] = E[id] + P[pos + off]; h[tok] = LN(x[tok]).  Token tok of a launch is
 // sequence tok / tok_per_seq at position pos0 + tok % tok_per_seq.

@@ -88,16 +88,16 @@ __device__ __forceinline__ float4 sum_slices(const float *p, int split, long lon
 
 // One block per row (d % 4 == 0, ldp % 4 == 0): x += sum of slices + bias, then LN.
 template <typename T>
-__global__ void k_resid_ln(const float *partial, int split, long long split_stride, int ldp,
-                           const T *bias, float *x, const T *g, const T *b, float eps, T *h,
-                           int d) {
+__global__ void k_resid_ln(const float *partial, const SliceInfo si, long long split_stride,
+                           int ldp, const T *bias, float *x, const T *g, const T *b, float eps,
+                           T *h, int d) {
   extern __shared__ float row[];
   __shared__ float red[33];
   const long long r = blockIdx.x;
   float4 *xr = reinterpret_cast<float4 *>(x + r * d);
   const float *pr = partial + r * ldp;
   for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
-    const float4 acc = sum_slices(pr + 4 * i, split, split_stride);
+    const float4 acc = sum_slices(pr + 4 * i, si.slices(4 * i), split_stride);
     float4 v = xr[i];
     v.x += acc.x + to_f<T>(bias[4 * i]);
     v.y += acc.y + to_f<T>(bias[4 * i + 1]);
@@ -119,6 +119,23 @@ __global__ void k_reduce_epi4(const float *partial, int split, long long split_s
   if (e >= (long long)M * n4) return;
   const int tok = (int)(e / n4), n = (int)(e % n4) * 4;
   const float4 acc = sum_slices(partial + (long long)tok * ldp + n, split, split_stride);
+  epi_store<T>(epi, 0, tok, n, acc.x);
+  epi_store<T>(epi, 0, tok, n + 1, acc.y);
+  epi_store<T>(epi, 0, tok, n + 2, acc.z);
+  epi_store<T>(epi, 0, tok, n + 3, acc.w);
+}
+
+// Stream-K slices: tiles with a single slice were stored by the GEMM itself.
+template <typename T>
+__global__ void k_sk_reduce_epi4(const float *partial, const SliceInfo si, long long split_stride,
+                                 int ldp, int M, int N, const __grid_constant__ Epi epi) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int n4 = N / 4;
+  if (e >= (long long)M * n4) return;
+  const int tok = (int)(e / n4), n = (int)(e % n4) * 4;
+  const int S = si.slices(n);
+  if (S == 1) return;
+  const float4 acc = sum_slices(partial + (long long)tok * ldp + n, S, split_stride);
   epi_store<T>(epi, 0, tok, n, acc.x);
   epi_store<T>(epi, 0, tok, n + 1, acc.y);
   epi_store<T>(epi, 0, tok, n + 2, acc.z);
@@ -313,19 +330,34 @@ cudaError_t launch_embed_ln(int dtype, const int32_t *ids, int n_tok, int tok_pe
   return cudaGetLastError();
 }
 
-cudaError_t launch_resid_ln(int dtype, const float *partial, int split, long long split_stride,
-                            int ldp, const void *bias, float *x, const void *g, const void *b,
-                            float eps, void *h, int rows, int d, cudaStream_t st) {
+cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInfo &si,
+                                 long long split_stride, int ldp, int M, int N, const Epi &epi,
+                                 cudaStream_t st) {
+  if (N % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16) return cudaErrorInvalidValue;
+  const long long work = (long long)M * N / 4;
+  if (work <= 0) return cudaSuccess;
+  const int blocks = (int)((work + 255) / 256);
+  if (dtype == 1)
+    k_sk_reduce_epi4<bf16><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
+  else
+    k_sk_reduce_epi4<float><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
+                            long long split_stride, int ldp, const void *bias, float *x,
+                            const void *g, const void *b, float eps, void *h, int rows, int d,
+                            cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
     return cudaErrorInvalidValue;
   const size_t sm = (size_t)d * sizeof(float);
   if (dtype == 1)
-    k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, split, split_stride, ldp,
+    k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
                                                        (const bf16 *)bias, x, (const bf16 *)g,
                                                        (const bf16 *)b, eps, (bf16 *)h, d);
   else
-    k_resid_ln<float><<<rows, row_threads(d), sm, st>>>(partial, split, split_stride, ldp,
+    k_resid_ln<float><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
                                                         (const float *)bias, x, (const float *)g,
                                                         (const float *)b, eps, (float *)h, d);
   return cudaGetLastError();

@@ -21,8 +21,12 @@ extern "C" {
  * x has row stride ldx >= K; w is dense [N][K] (w_layout 0) or in the tiled
  * streaming layout below (w_layout 1, bf16 only).  split >= 1 splits K into
  * slices of whole 64-wide blocks (no empty slice allowed) whose fp32 partial
- * sums go to scratch [split][M][N] and are then added in slice order.  All
- * pointers are device memory; asynchronous on `stream`. */
+ * sums go to scratch [split][M][N] and are then added in slice order.
+ * split <= 0 runs the persistent stream-K kernel of the decode projections
+ * (bf16, M <= 256, N % 128 == 0, K % 64 == 0): the (128-row tile, 64-wide
+ * k-block) units are cut into P equal runs, P = -split if split < 0 (at most
+ * min(units, 15 * tiles)), else the engine's choice (one per SM); scratch needs
+ * 16 * M * N floats.  All pointers are device memory; asynchronous on `stream`. */
 he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
                        int M, int N, int K, int split, float *scratch, void *stream);
 

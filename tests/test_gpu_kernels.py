@@ -109,3 +109,17 @@ def test_linear_bf16_tiled_weights(cuda_device, M, N, K, split):
     torch.cuda.synchronize()
     err = np.abs(y.cpu().numpy() - _exact(x, w))
     assert (err <= _bound(x, w, K)).all(), err.max()
+
+
+@pytest.mark.parametrize("M,N,K,ctas", [(1, 128, 64, 0), (17, 384, 320, 0), (128, 1280, 1024, 0),
+                                        (128, 640, 5120, 0), (200, 256, 512, 0), (64, 384, 640, -1),
+                                        (5, 128, 640, -10), (33, 256, 192, -6), (128, 1280, 128, -7)])
+@pytest.mark.parametrize("tiled", [False, True])
+def test_linear_bf16_stream_k(cuda_device, M, N, K, ctas, tiled):
+    g = torch.Generator().manual_seed(M * 13 + N + K)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w, split=ctas, w_tiled=he.tile_weight(w) if tiled else None)
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, K)).all(), err.max()
