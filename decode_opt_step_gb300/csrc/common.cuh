@@ -133,6 +133,16 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
       : "memory");
 }
 
+// Generic-proxy shared-memory writes made visible to the async proxy (tensor
+// cores, bulk copies) before the writer signals an mbarrier.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // L2 prefetch of one tile of a 2-D tensor map (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -225,11 +225,13 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   Timed t(h, cls, c.st);
   if (use_stream_k(h, M, a.N, K, decode)) {
     const int P = sk_ctas(a, h->num_sms);
-    si = SliceInfo{0, (long long)(a.N / 128) * (K / 64), K / 64, P};
+    const long long U = sk_units(a);
+    si = SliceInfo{0, U, (int)(U / (a.N / 128)), P};
     a.split = 1;
     a.epi = epi;
     c.check(launch_gemm_sk(a, P, part, stride, static_cast<int *>(h->err.p), c.st), 1);
-    if (epi.kind != EPI_PARTIAL)
+    // P == tiles: every tile is one run and was stored by the GEMM itself
+    if (epi.kind != EPI_PARTIAL && P != a.N / 128)
       c.check(launch_sk_reduce_epi(a.dtype, part, si, stride, a.N, M, a.N, epi, c.st), 1);
     return si;
   }
@@ -841,8 +843,8 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     a.split = 1;
     a.w_tiled = w_layout;
     int P = sk_ctas(a, sms);
+    const long long T = N / 128, U = sk_units(a);
     if (split < 0) {
-      const long long T = N / 128, U = T * (K / 64);
       if (-split > U || -split > 15 * T)
         return fail(HE_ERR_ARG, "stream-K CTA count %d above min(units, 15 * tiles)", -split);
       P = -split;
@@ -852,7 +854,7 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     e.partial = y;
     e.ldp = N;
     a.epi = e;
-    const SliceInfo si{0, (long long)(N / 128) * (K / 64), K / 64, P};
+    const SliceInfo si{0, U, (int)(U / T), P};
     cudaError_t r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
     if (r == cudaSuccess)
       r = launch_sk_reduce_epi(dtype, scratch, si, (long long)M * N, N, M, N, e, st);

@@ -11,9 +11,15 @@
 // adds the slices of a tile in slot order (sk_segments gives how many).  A tile
 // covered by a single segment gets the element-wise epilogue directly.
 //
-// Warp roles as in gemm_tc.cu: warps 0-3 epilogue, warp 4 loads (bulk copies of
-// tiled weights or TMA of row-major ones, TMA of the activations), warp 5 owns
-// TMEM and issues the MMAs.  All waits are bounded.
+// Warp roles (320 threads): warps 0-3 epilogue (warp w reads TMEM lanes
+// 32w..32w+31), warp 4 loads the weights (one bulk copy of KPS tiled 128 x 64
+// tiles per stage, or KPS TMA boxes of row-major weights), warp 5 owns TMEM and
+// issues the MMAs, warps 6-9 copy the activation tile of each stage from global
+// memory (L2-resident in decode) into shared memory with 16-byte loads, writing
+// the 128-byte-swizzled order the MMA reads.  A tensor-tiled TMA request costs
+// the SM's copy engine a fixed ~0.5 us however small it is, so the activations
+// stay off that engine and it only carries the large weight requests.  All
+// waits are bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,10 +47,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
 }
 constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32u : c <= 64 ? 64u : c <= 128 ? 128u : c <= 256 ? 256u : 512u; }
 
-template <int BN, int STAGES>
+// KPS 64-wide k-blocks per pipeline stage: with tiled weights the KPS weight
+// tiles of a stage are contiguous and arrive in one bulk copy (a bulk request
+// costs the SM's copy engine a roughly fixed time, so bigger requests stream faster).
+template <int BN, int STAGES, int KPS>
 struct SkCfg {
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_BYTES = BN * BK * 2;  // one k-block of activations
+  static constexpr int STAGE_A = KPS * A_BYTES;
+  static constexpr int STAGE_B = KPS * B_BYTES;
+  static constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
   static constexpr uint32_t TMEM_COLS = pow2_cols(2 * BN);
 };
@@ -54,23 +65,24 @@ struct SkArgs {
   int tiled;
   int tiles_per_group;   // 128-row tiles per group (multiple groups only)
   int n_groups;
-  int M, N, KB;          // tokens, output features, 64-wide k-blocks
+  int M, N, KB;          // tokens, output features, units (KPS k-blocks) per tile
   long long U;           // units = tiles * KB
   float *slices;         // fp32 slices [slot][M][N]
   long long slice_stride;
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int STAGES, int KPS>
+__global__ void __launch_bounds__(320, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
-              const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, int *dev_err) {
-  using C = SkCfg<BN, STAGES>;
+              const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const bf16 *x, int ldx,
+              int *dev_err) {
+  using C = SkCfg<BN, STAGES, KPS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t *smA = base;
-  uint8_t *smB = base + STAGES * A_BYTES;
+  uint8_t *smB = base + STAGES * C::STAGE_A;
   uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES);
   uint64_t *empty = full + STAGES;
   uint64_t *acc_full = empty + STAGES;   // [2]
@@ -84,7 +96,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 4);  // weight producer (+ bytes) and the 4 activation warps
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -110,7 +122,6 @@ __global__ void __launch_bounds__(192, 1)
       if (a.n_groups > 1) prefetch_tmap(&tm_w1);
       if (a.n_groups > 2) prefetch_tmap(&tm_w2);
     }
-    prefetch_tmap(&tm_x);
     long long issued = 0;
     bool stop = false;
     for (long long u = u_begin; u < u_end && !stop; ++u) {
@@ -125,15 +136,17 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       if (*(volatile int *)abort_flag) break;
-      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      mbar_arrive_expect_tx(&full[s], C::STAGE_A);
       if (a.tiled) {
-        const bf16 *src = a.wt[group] + ((long long)lt * a.KB + kb) * (BM * BK);
-        bulk_load(smA + s * A_BYTES, src, A_BYTES, &full[s]);
+        const bf16 *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
+        bulk_load(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s]);
       } else {
         const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
-        tma_load_2d(smA + s * A_BYTES, tw, &full[s], kb * BK, lt * BM);
+#pragma unroll
+        for (int j = 0; j < KPS; ++j)
+          tma_load_2d(smA + s * C::STAGE_A + j * A_BYTES, tw, &full[s], (kb * KPS + j) * BK,
+                      lt * BM);
       }
-      tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kb * BK, 0);
       issued = i + 1;
     }
     for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
@@ -167,17 +180,60 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smA + s * A_BYTES);
-        const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-          tc_mma_f16(acc, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
-                     idesc, (j | kk) != 0);
+        for (int q = 0; q < KPS; ++q) {
+          const uint32_t a0 = smem_u32(smA + s * C::STAGE_A + q * A_BYTES);
+          const uint32_t b0 = smem_u32(smB + s * C::STAGE_B + q * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            tc_mma_f16(acc, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
+                       idesc, (j | q | kk) != 0);
+        }
         tc_commit(&empty[s]);
       }
       tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
       u += n;
       ++seg;
+    }
+  } else if (warp >= 6) {
+    // ---------------- activations: global -> swizzled shared ----------------
+    const int lt = threadIdx.x - 6 * 32;  // 0..127
+    constexpr int CHUNKS = BN * 8;        // 16-byte chunks per k-block tile
+    constexpr int PER = CHUNKS / 128 > 0 ? CHUNKS / 128 : 1;
+    for (long long u = u_begin; u < u_end; ++u) {
+      const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
+      const long long i = u - u_begin;
+      const int s = (int)(i % STAGES);
+      if (i >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+#pragma unroll
+      for (int j = 0; j < KPS; ++j) {
+        uint4 v[PER];
+        const int k0 = (kb * KPS + j) * BK;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+          const int e = lt + q * 128;  // chunk e: row e / 8, 16-byte column e % 8
+          const int r = e >> 3, cc = e & 7;
+          v[q] = make_uint4(0, 0, 0, 0);
+          if (e < CHUNKS && r < a.M)
+            v[q] = __ldcg(reinterpret_cast<const uint4 *>(x + (long long)r * ldx + k0 + cc * 8));
+        }
+        uint8_t *dst = smB + s * C::STAGE_B + j * C::B_BYTES;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+          const int e = lt + q * 128;
+          const int r = e >> 3, cc = e & 7;
+          if (e < CHUNKS)
+            *reinterpret_cast<uint4 *>(dst + r * 128 + ((cc ^ (r & 7)) << 4)) = v[q];
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if ((lt & 31) == 0) mbar_arrive(&full[s]);
     }
   } else if (warp < 4) {
     // ---------------- epilogue ----------------
@@ -216,7 +272,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[buf])) : "memory");
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
       u += n;
       ++seg;
     }
@@ -229,10 +285,10 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KPS>
 cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slice_stride,
                          int *dev_err, cudaStream_t st) {
-  using C = SkCfg<BN, STAGES>;
+  using C = SkCfg<BN, STAGES, KPS>;
   CUtensorMap tw[3], tx;
   memset(tw, 0, sizeof tw);
   SkArgs a{};
@@ -246,30 +302,39 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
     else if (i < g.n_groups && !make_tmap_bf16(&tw[i], p, g.group_rows, g.K, g.K, BM))
       return cudaErrorInvalidValue;
   }
-  if (!make_tmap_bf16(&tx, g.x, g.M, g.K, g.ldx, BN)) return cudaErrorInvalidValue;
+  memset(&tx, 0, sizeof tx);  // activations are read with plain loads
+  if ((uintptr_t)g.x % 16) return cudaErrorInvalidValue;
   a.M = g.M;
   a.N = g.N;
-  a.KB = g.K / BK;
+  a.KB = g.K / (BK * KPS);
   a.U = (long long)(g.N / BM) * a.KB;
   a.slices = slices;
   a.slice_stride = slice_stride;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<BN, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<BN, STAGES, KPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_sk<BN, STAGES><<<P, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi, dev_err);
+  k_gemm_sk<BN, STAGES, KPS><<<P, 320, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi,
+                                                      static_cast<const bf16 *>(g.x), g.ldx,
+                                                      dev_err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// One run per SM, at most U runs, and at most 15 runs per tile so that a tile
-// never has more than 16 slices.
+int sk_kps(const GemmArgs &g) { return g.K % 128 == 0 ? 2 : 1; }
+
+long long sk_units(const GemmArgs &g) { return (long long)(g.N / 128) * (g.K / (64 * sk_kps(g))); }
+
+// Runs: whole tiles (P = T) when the tiles nearly fill the GPU, which needs no
+// reduction; otherwise one run per SM, at most U runs and at most 15 runs per
+// tile (so a tile never has more than 16 slices).
 int sk_ctas(const GemmArgs &g, int num_sms) {
-  const long long T = g.N / 128, U = T * (g.K / 64);
+  const long long T = g.N / 128, U = sk_units(g);
+  if (T <= num_sms && 10 * T >= 7LL * num_sms) return (int)T;
   long long P = num_sms;
   if (P > U) P = U;
   if (P > 15 * T) P = 15 * T;
@@ -284,11 +349,19 @@ cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long sl
   if (g.n_groups < 1 || g.n_groups > 3 || g.n_groups * g.group_rows != g.N) return cudaErrorInvalidValue;
   if (g.epi.kind == EPI_QKV && g.epi.d_model % BM) return cudaErrorInvalidValue;
   if (!slices || P < 1 || slice_stride < (long long)g.M * g.N) return cudaErrorInvalidValue;
-  if (g.M <= 16) return launch_sk_bn<16, 10>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 32) return launch_sk_bn<32, 9>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 64) return launch_sk_bn<64, 8>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 128) return launch_sk_bn<128, 6>(g, P, slices, slice_stride, dev_err, st);
-  return launch_sk_bn<256, 4>(g, P, slices, slice_stride, dev_err, st);
+  if (sk_kps(g) == 2) {
+    // two k-blocks per stage: 32 KB weight requests
+    if (g.M <= 16) return launch_sk_bn<16, 5, 2>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 32) return launch_sk_bn<32, 5, 2>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 64) return launch_sk_bn<64, 4, 2>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 128) return launch_sk_bn<128, 3, 2>(g, P, slices, slice_stride, dev_err, st);
+    return launch_sk_bn<256, 2, 2>(g, P, slices, slice_stride, dev_err, st);
+  }
+  if (g.M <= 16) return launch_sk_bn<16, 10, 1>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 32) return launch_sk_bn<32, 9, 1>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 64) return launch_sk_bn<64, 8, 1>(g, P, slices, slice_stride, dev_err, st);
+  if (g.M <= 128) return launch_sk_bn<128, 6, 1>(g, P, slices, slice_stride, dev_err, st);
+  return launch_sk_bn<256, 4, 1>(g, P, slices, slice_stride, dev_err, st);
 }
 
 }  // namespace he

@@ -109,6 +109,10 @@ cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st);
 // Persistent stream-K tcgen05 GEMM (bf16, M <= 256 tokens, N % 128 == 0, K % 64 == 0)
 // on P CTAs; writes fp32 slices [slot][M][N] (slot stride slice_stride) except for
 // tiles covered by one run under an element-wise a.epi, which are stored directly.
+// A unit is sk_kps(a) 64-wide k-blocks (2 when K % 128 == 0); sk_units = tiles x
+// units per tile.
+int sk_kps(const GemmArgs &a);
+long long sk_units(const GemmArgs &a);
 int sk_ctas(const GemmArgs &a, int num_sms);
 cudaError_t launch_gemm_sk(const GemmArgs &a, int P, float *slices, long long slice_stride,
                            int *dev_err, cudaStream_t st);
