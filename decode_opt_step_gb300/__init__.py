@@ -343,9 +343,13 @@ def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     if x.stride(1) != 1 or not w.is_contiguous():
         raise ValueError("x rows and w must be dense")
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    slices = 16 if split <= 0 else split  # split <= 0: stream-K (up to 16 slices per tile)
-    scratch = (torch.empty((slices, M, N), dtype=torch.float32, device=x.device)
-               if slices > 1 else None)
+    if split <= 0:  # stream-K: up to 16 slices per tile + the row-tiled copy of x
+        R = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+        scratch = torch.empty(16 * M * N + (R * K + 1) // 2 + 4, dtype=torch.float32,
+                              device=x.device)
+    else:
+        scratch = (torch.empty((split, M, N), dtype=torch.float32, device=x.device)
+                   if split > 1 else None)
     dt = HE_DTYPE_BF16 if x.dtype == torch.bfloat16 else HE_DTYPE_F32
     wp, layout = (w.data_ptr(), 0) if w_tiled is None else (w_tiled.data_ptr(), 1)
     _check(lib.he_op_linear(dt, x.data_ptr(), x.stride(0), wp, layout, y.data_ptr(), M, N, K,

@@ -47,7 +47,7 @@ template <> struct Vec16<float> {
 template <typename T, int HD, int UNROLL>
 __global__ void __launch_bounds__(128)
     k_attn_decode(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
-                  T *__restrict__ ctx, int H, int max_seq, int n_keys, int per_split,
+                  T *__restrict__ ctx, int ctx_rows, int H, int max_seq, int n_keys, int per_split,
                   float *__restrict__ part) {
   constexpr int VEC = Vec16<T>::N;
   constexpr int LPK = HD / VEC;       // lanes per key row
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(128)
       O = fmaf(s_o[k][dd], w, O);
     }
     if (nsplit == 1) {
-      ctx[((long long)b * H + h) * HD + dd] = from_f<T>(O / L);
+      ctx[act_index(b, h * HD + dd, H * HD, ctx_rows)] = from_f<T>(O / L);
     } else {
       float *pp = part + ((long long)bh * nsplit + sidx) * (HD + 2);
       pp[dd] = O;
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(128)
 }
 
 template <typename T, int HD>
-__global__ void k_attn_combine(const float *__restrict__ part, T *__restrict__ ctx, int H,
-                               int nsplit) {
+__global__ void k_attn_combine(const float *__restrict__ part, T *__restrict__ ctx, int ctx_rows,
+                               int H, int nsplit) {
   const int bh = blockIdx.x, dd = threadIdx.x;
   const float *pp = part + (long long)bh * nsplit * (HD + 2);
   float M = -INFINITY;
@@ -155,7 +155,7 @@ __global__ void k_attn_combine(const float *__restrict__ part, T *__restrict__ c
     L = fmaf(pp[s * (HD + 2) + HD + 1], w, L);
     O = fmaf(pp[s * (HD + 2) + dd], w, O);
   }
-  ctx[(long long)bh * HD + dd] = from_f<T>(O / L);
+  ctx[act_index(bh / H, (bh % H) * HD + dd, H * HD, ctx_rows)] = from_f<T>(O / L);
 }
 
 // ---------------------------------------------------------------------------
@@ -243,15 +243,15 @@ __global__ void __launch_bounds__(256)
 }
 
 template <typename T, int HD>
-cudaError_t decode_t(const void *q, const void *kc, const void *vc, void *ctx, int B, int H,
-                     int max_seq, int n_keys, int split, float *part, cudaStream_t st) {
+cudaError_t decode_t(const void *q, const void *kc, const void *vc, void *ctx, int ctx_rows, int B,
+                     int H, int max_seq, int n_keys, int split, float *part, cudaStream_t st) {
   const int per = (n_keys + split - 1) / split;
   const int ns = (n_keys + per - 1) / per;
   if (ns > 1 && !part) return cudaErrorInvalidValue;
   dim3 grid(B * H, ns);
   k_attn_decode<T, HD, 4><<<grid, 128, 0, st>>>((const T *)q, (const T *)kc, (const T *)vc,
-                                                (T *)ctx, H, max_seq, n_keys, per, part);
-  if (ns > 1) k_attn_combine<T, HD><<<B * H, HD, 0, st>>>(part, (T *)ctx, H, ns);
+                                                (T *)ctx, ctx_rows, H, max_seq, n_keys, per, part);
+  if (ns > 1) k_attn_combine<T, HD><<<B * H, HD, 0, st>>>(part, (T *)ctx, ctx_rows, H, ns);
   return cudaGetLastError();
 }
 
@@ -285,17 +285,17 @@ int attn_decode_pick_split(int B, int H, int n_keys, int num_sms) {
 }
 
 cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
-                               void *ctx, int B, int H, int hd, int max_seq, int n_keys,
-                               int split, float *part, cudaStream_t st) {
+                               void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
+                               int n_keys, int split, float *part, cudaStream_t st) {
   if (n_keys <= 0 || split < 1) return cudaErrorInvalidValue;
   if (dtype == 1) {
-    if (hd == 128) return decode_t<bf16, 128>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 64) return decode_t<bf16, 64>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 32) return decode_t<bf16, 32>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 128) return decode_t<bf16, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 64) return decode_t<bf16, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 32) return decode_t<bf16, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
   } else {
-    if (hd == 128) return decode_t<float, 128>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 64) return decode_t<float, 64>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 32) return decode_t<float, 32>(q, kc, vc, ctx, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 128) return decode_t<float, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 64) return decode_t<float, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 32) return decode_t<float, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
   }
   return cudaErrorInvalidValue;
 }

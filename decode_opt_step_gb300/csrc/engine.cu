@@ -115,9 +115,13 @@ void free_workspace(he_engine *h, cudaStream_t st) {
 he_status take_workspace(he_engine *h, cudaStream_t st) {
   const he_config &c = h->cfg;
   const size_t e = h->elem, hd = c.d_model / c.n_heads;
-  const size_t max_tok = (size_t)c.max_batch * c.max_seq;
+  size_t max_tok = (size_t)c.max_batch * c.max_seq;
+  // decode buffers hold a padded token tile when they are row-tiled
+  if (c.dtype == HE_DTYPE_BF16 && (size_t)sk_token_tile(c.max_batch) > max_tok)
+    max_tok = sk_token_tile(c.max_batch);
   const size_t kv = (size_t)c.n_layers * h->kv_layer_elems() * e;
-  const size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
+  size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
+  if ((size_t)c.vocab > wide) wide = c.vocab;  // LM-head slices
   size_t part = max_tok * c.d_model;
   if ((size_t)kMaxGemmSplit * c.max_batch * wide > part) part = (size_t)kMaxGemmSplit * c.max_batch * wide;
   struct {
@@ -197,8 +201,14 @@ inline char *at(void *p, size_t off) { return static_cast<char *>(p) + off; }
 
 // Decode projections on bf16 run the persistent stream-K kernel when the shape
 // allows (whole 128 x 64 tiles, one token tile).
-bool use_stream_k(const he_engine *h, int M, int N, int K, bool decode) {
-  return decode && h->cfg.dtype == HE_DTYPE_BF16 && M <= 256 && N % 128 == 0 && K % 64 == 0;
+bool use_stream_k(const he_engine *h, int M, int N, int K, bool decode, bool tiled_w) {
+  return decode && h->cfg.dtype == HE_DTYPE_BF16 && M <= 256 && K % 64 == 0 &&
+         (!tiled_w || N % 128 == 0);
+}
+
+// Rows of the row-tiled decode activation buffers (0 = row-major).
+int act_rows(const he_engine *h, int B, bool decode) {
+  return decode && h->cfg.dtype == HE_DTYPE_BF16 ? sk_token_tile(B) : 0;
 }
 
 // One projection GEMM.  Element-wise epilogues (QKV, ReLU) are completed here
@@ -206,7 +216,7 @@ bool use_stream_k(const he_engine *h, int M, int N, int K, bool decode) {
 // fp32 slices stay in h->partial and the returned SliceInfo tells the row
 // consumer how to add them.
 SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
-               int group_rows, int M, int K, Epi epi, bool decode) {
+               int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w) {
   he_engine *h = c.h;
   GemmArgs a{};
   a.dtype = h->cfg.dtype;
@@ -218,20 +228,20 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   a.M = M;
   a.N = n_groups * group_rows;
   a.K = K;
-  a.w_tiled = h->tiled;
+  a.w_tiled = tiled_w;
   SliceInfo si{1, 0, 0, 0};
   float *part = static_cast<float *>(h->partial.p);
   const long long stride = (long long)M * a.N;
   Timed t(h, cls, c.st);
-  if (use_stream_k(h, M, a.N, K, decode)) {
+  if (use_stream_k(h, M, a.N, K, decode, tiled_w)) {
     const int P = sk_ctas(a, h->num_sms);
-    const long long U = sk_units(a);
-    si = SliceInfo{0, U, (int)(U / (a.N / 128)), P};
+    const long long U = sk_units(a), T = (a.N + 127) / 128;
+    si = SliceInfo{0, U, (int)(U / T), P};
     a.split = 1;
     a.epi = epi;
     c.check(launch_gemm_sk(a, P, part, stride, static_cast<int *>(h->err.p), c.st), 1);
     // P == tiles: every tile is one run and was stored by the GEMM itself
-    if (epi.kind != EPI_PARTIAL && P != a.N / 128)
+    if (epi.kind != EPI_PARTIAL && P != T)
       c.check(launch_sk_reduce_epi(a.dtype, part, si, stride, a.N, M, a.N, epi, c.st), 1);
     return si;
   }
@@ -289,9 +299,11 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   const int d = cf.d_model, hd = d / cf.n_heads;
   const int cls_g = prefill ? HE_KCLASS_PREFILL_GEMM : HE_KCLASS_GEMM;
   const bool dec = !prefill;
+  const int R = act_rows(h, B, dec);  // decode: h, ctx, mid are row-tiled with R rows
+  const bool tw = h->tiled;
   // LN1 + QKV (+ KV append at the tokens' positions)
   const void *wqkv[3] = {lw.w[HE_PROJ_Q], lw.w[HE_PROJ_K], lw.w[HE_PROJ_V]};
-  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec);
+  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw);
   Epi ep{};
   ep.kind = EPI_PARTIAL;
   // attention
@@ -306,19 +318,19 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
     int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
     if (split > kMaxAttnSplit) split = kMaxAttnSplit;
     Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
-    c.check(launch_attn_decode(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
-                               cf.n_heads, hd, cf.max_seq, n_keys, split,
+    c.check(launch_attn_decode(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, R,
+                               B, cf.n_heads, hd, cf.max_seq, n_keys, split,
                                static_cast<float *>(h->attn_part.p), c.st),
             split > 1 ? 2 : 1);
   }
   // out projection -> partials; + bo + residual; LN2
   const void *wo[1] = {lw.w[HE_PROJ_O]};
-  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec);
+  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw);
   {
     Timed t(h, HE_KCLASS_NORM, c.st);
     c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                             lw.b[HE_PROJ_O], static_cast<float *>(h->x.p), lw.ln2_g, lw.ln2_b,
-                            cf.ln_eps, h->h.p, M, d, c.st),
+                            cf.ln_eps, h->h.p, R, M, d, c.st),
             1);
   }
   // fc1 + b1 + ReLU
@@ -327,43 +339,65 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   er.bias[0] = lw.b[HE_PROJ_FC1];
   er.out = h->mid.p;
   er.ldo = cf.ffn;
+  er.out_rows = R;
   const void *w1[1] = {lw.w[HE_PROJ_FC1]};
-  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec);
+  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw);
   // fc2 -> partials; + b2 + residual; next LN
   const void *w2[1] = {lw.w[HE_PROJ_FC2]};
-  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec);
+  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw);
   const bool last = l == cf.n_layers - 1;
   const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
   const void *bb = last ? h->lnf_b : h->layers[l + 1].ln1_b;
   Timed t(h, HE_KCLASS_NORM, c.st);
   c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                           lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
-                          h->h.p, M, d, c.st),
+                          h->h.p, R, M, d, c.st),
           1);
 }
 
-// LM head over B rows of h (row stride ldh elements) + greedy select for step k.
+// LM head over B rows of h + greedy select for step k.  Step 0 (after the prefill)
+// reads row-major h rows b*Lp + Lp-1 (row stride ldh); decode steps read the
+// row-tiled h through the stream-K kernel.  The chosen token is embedded and
+// normalised into the row-tiled decode h for the next step.
 void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
           const int32_t *force, int32_t *out_ids, float *out_lp, const int32_t *log_map,
           float *logits_out) {
   he_engine *h = c.h;
   const he_config &cf = h->cfg;
+  const bool dec = step > 0;
+  const int R = act_rows(h, B, true);
+  Epi el{};
+  el.kind = EPI_STORE_F32;
+  el.partial = static_cast<float *>(h->logits.p);
+  el.ldp = cf.vocab;
+  if (dec && use_stream_k(h, B, cf.vocab, cf.d_model, true, false)) {
+    const void *we[1] = {h->tok_emb};
+    gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false);
+  } else {
+    Timed t(h, HE_KCLASS_HEAD, c.st);
+    GemmArgs a{};
+    a.dtype = cf.dtype;
+    a.x = hrows;
+    a.ldx = ldh;
+    a.w[0] = h->tok_emb;
+    a.n_groups = 1;
+    a.group_rows = cf.vocab;
+    a.M = B;
+    a.N = cf.vocab;
+    a.K = cf.d_model;
+    a.split = 1;
+    a.epi = el;
+    c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+  }
+  if (!dec && R > 0) {
+    // from here on h, ctx and mid hold row-tiled decode tiles whose padding rows
+    // (B..R-1) must read as zero
+    const size_t e = h->elem;
+    c.check(launch_zero(h->h.p, (size_t)R * cf.d_model * e, c.st), 1);
+    c.check(launch_zero(h->ctx.p, (size_t)R * cf.d_model * e, c.st), 1);
+    c.check(launch_zero(h->mid.p, (size_t)R * cf.ffn * e, c.st), 1);
+  }
   Timed t(h, HE_KCLASS_HEAD, c.st);
-  GemmArgs a{};
-  a.dtype = cf.dtype;
-  a.x = hrows;
-  a.ldx = ldh;
-  a.w[0] = h->tok_emb;
-  a.n_groups = 1;
-  a.group_rows = cf.vocab;
-  a.M = B;
-  a.N = cf.vocab;
-  a.K = cf.d_model;
-  a.split = 1;
-  a.epi.kind = EPI_STORE_F32;
-  a.epi.partial = static_cast<float *>(h->logits.p);
-  a.epi.ldp = cf.vocab;
-  c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
   HeadArgs ha{};
   ha.logits = static_cast<float *>(h->logits.p);
   ha.ldl = cf.vocab;
@@ -387,6 +421,7 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   ha.x = static_cast<float *>(h->x.p);
   ha.h = h->h.p;
   ha.d = cf.d_model;
+  ha.h_rows = R;
   c.check(launch_head_select(cf.dtype, ha, c.st), 1);
 }
 
@@ -824,8 +859,8 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (split <= 0) {
     // stream-K: the persistent kernel of the decode projections
-    if (dtype != HE_DTYPE_BF16 || M > 256 || N % 128 || K % 64)
-      return fail(HE_ERR_UNSUPPORTED, "stream-K needs bf16, M <= 256, N %% 128 == 0, K %% 64 == 0");
+    if (dtype != HE_DTYPE_BF16 || M > 256 || K % 64 || (w_layout == 1 && N % 128))
+      return fail(HE_ERR_UNSUPPORTED, "stream-K needs bf16, M <= 256, K %% 64 == 0 (and N %% 128 == 0 for tiled weights)");
     if (!scratch) return fail(HE_ERR_ARG, "stream-K needs scratch");
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -843,7 +878,7 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     a.split = 1;
     a.w_tiled = w_layout;
     int P = sk_ctas(a, sms);
-    const long long T = N / 128, U = sk_units(a);
+    const long long T = (N + 127) / 128, U = sk_units(a);
     if (split < 0) {
       if (-split > U || -split > 15 * T)
         return fail(HE_ERR_ARG, "stream-K CTA count %d above min(units, 15 * tiles)", -split);
@@ -854,8 +889,12 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     e.partial = y;
     e.ldp = N;
     a.epi = e;
+    // the stream-K kernel reads row-tiled activations: tile x behind the slices
+    void *xt = scratch + (size_t)16 * M * N;
+    a.x = xt;
+    cudaError_t r = launch_tile_act(x, M, K, ldx, sk_token_tile(M), xt, st);
     const SliceInfo si{0, U, (int)(U / T), P};
-    cudaError_t r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
+    if (r == cudaSuccess) r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
     if (r == cudaSuccess)
       r = launch_sk_reduce_epi(dtype, scratch, si, (long long)M * N, N, M, N, e, st);
     if (r != cudaSuccess) return cuda_fail(r, "he_op_linear (stream-K)");

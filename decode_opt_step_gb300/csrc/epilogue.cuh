@@ -18,7 +18,7 @@ __device__ __forceinline__ void epi_store(const Epi &e, int s, int tok, int n, f
       break;
     case EPI_RELU: {
       float v = acc + to_f<T>(static_cast<const T *>(e.bias[0])[n]);
-      static_cast<T *>(e.out)[(long long)tok * e.ldo + n] = from_f<T>(fmaxf(v, 0.f));
+      static_cast<T *>(e.out)[act_index(tok, n, e.ldo, e.out_rows)] = from_f<T>(fmaxf(v, 0.f));
       break;
     }
     case EPI_QKV: {

@@ -11,15 +11,13 @@
 // adds the slices of a tile in slot order (sk_segments gives how many).  A tile
 // covered by a single segment gets the element-wise epilogue directly.
 //
-// Warp roles (320 threads): warps 0-3 epilogue (warp w reads TMEM lanes
-// 32w..32w+31), warp 4 loads the weights (one bulk copy of KPS tiled 128 x 64
-// tiles per stage, or KPS TMA boxes of row-major weights), warp 5 owns TMEM and
-// issues the MMAs, warps 6-9 copy the activation tile of each stage from global
-// memory (L2-resident in decode) into shared memory with 16-byte loads, writing
-// the 128-byte-swizzled order the MMA reads.  A tensor-tiled TMA request costs
-// the SM's copy engine a fixed ~0.5 us however small it is, so the activations
-// stay off that engine and it only carries the large weight requests.  All
-// waits are bounded.
+// Warp roles (192 threads): warps 0-3 epilogue (warp w reads TMEM lanes
+// 32w..32w+31), warp 4 loads (per stage one bulk copy of KPS tiled 128 x 64
+// weight tiles, or KPS TMA boxes of row-major weights, plus one bulk copy of the
+// KPS row-tiled activation k-blocks), warp 5 owns TMEM and issues the MMAs.
+// The SM's copy engine spends a roughly fixed time per request (about 0.3 us for
+// a bulk copy, 0.55 us for a tensor-tiled box, nearly independent of size up to
+// 32 KB), so a stage is two large bulk requests.  All waits are bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -72,7 +70,7 @@ struct SkArgs {
 };
 
 template <int BN, int STAGES, int KPS>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(192, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const bf16 *x, int ldx,
@@ -96,7 +94,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 4);  // weight producer (+ bytes) and the 4 activation warps
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -136,7 +134,7 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       if (*(volatile int *)abort_flag) break;
-      mbar_arrive_expect_tx(&full[s], C::STAGE_A);
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
       if (a.tiled) {
         const bf16 *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
         bulk_load(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s]);
@@ -147,6 +145,8 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_2d(smA + s * C::STAGE_A + j * A_BYTES, tw, &full[s], (kb * KPS + j) * BK,
                       lt * BM);
       }
+      // the stage's activation k-blocks: one contiguous block of the row-tiled input
+      bulk_load(smB + s * C::STAGE_B, x + (long long)kb * KPS * BN * BK, C::STAGE_B, &full[s]);
       issued = i + 1;
     }
     for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
@@ -194,46 +194,6 @@ __global__ void __launch_bounds__(320, 1)
       tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
       u += n;
       ++seg;
-    }
-  } else if (warp >= 6) {
-    // ---------------- activations: global -> swizzled shared ----------------
-    const int lt = threadIdx.x - 6 * 32;  // 0..127
-    constexpr int CHUNKS = BN * 8;        // 16-byte chunks per k-block tile
-    constexpr int PER = CHUNKS / 128 > 0 ? CHUNKS / 128 : 1;
-    for (long long u = u_begin; u < u_end; ++u) {
-      const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
-      const long long i = u - u_begin;
-      const int s = (int)(i % STAGES);
-      if (i >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
-        *(volatile int *)abort_flag = 1;
-        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
-        break;
-      }
-      if (*(volatile int *)abort_flag) break;
-#pragma unroll
-      for (int j = 0; j < KPS; ++j) {
-        uint4 v[PER];
-        const int k0 = (kb * KPS + j) * BK;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) {
-          const int e = lt + q * 128;  // chunk e: row e / 8, 16-byte column e % 8
-          const int r = e >> 3, cc = e & 7;
-          v[q] = make_uint4(0, 0, 0, 0);
-          if (e < CHUNKS && r < a.M)
-            v[q] = __ldcg(reinterpret_cast<const uint4 *>(x + (long long)r * ldx + k0 + cc * 8));
-        }
-        uint8_t *dst = smB + s * C::STAGE_B + j * C::B_BYTES;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) {
-          const int e = lt + q * 128;
-          const int r = e >> 3, cc = e & 7;
-          if (e < CHUNKS)
-            *reinterpret_cast<uint4 *>(dst + r * 128 + ((cc ^ (r & 7)) << 4)) = v[q];
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if ((lt & 31) == 0) mbar_arrive(&full[s]);
     }
   } else if (warp < 4) {
     // ---------------- epilogue ----------------
@@ -294,7 +254,7 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   SkArgs a{};
   a.tiled = g.w_tiled;
   a.n_groups = g.n_groups;
-  a.tiles_per_group = g.group_rows / BM;
+  a.tiles_per_group = g.n_groups > 1 ? g.group_rows / BM : 1;
   for (int i = 0; i < 3; ++i) {
     const void *p = g.w[i < g.n_groups ? i : 0];
     if (g.w_tiled)
@@ -302,12 +262,12 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
     else if (i < g.n_groups && !make_tmap_bf16(&tw[i], p, g.group_rows, g.K, g.K, BM))
       return cudaErrorInvalidValue;
   }
-  memset(&tx, 0, sizeof tx);  // activations are read with plain loads
+  memset(&tx, 0, sizeof tx);  // activations arrive by bulk copy (row-tiled layout)
   if ((uintptr_t)g.x % 16) return cudaErrorInvalidValue;
   a.M = g.M;
   a.N = g.N;
   a.KB = g.K / (BK * KPS);
-  a.U = (long long)(g.N / BM) * a.KB;
+  a.U = (long long)((g.N + BM - 1) / BM) * a.KB;
   a.slices = slices;
   a.slice_stride = slice_stride;
   static bool attr = false;
@@ -317,7 +277,7 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_sk<BN, STAGES, KPS><<<P, 320, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi,
+  k_gemm_sk<BN, STAGES, KPS><<<P, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi,
                                                       static_cast<const bf16 *>(g.x), g.ldx,
                                                       dev_err);
   return cudaGetLastError();
@@ -327,13 +287,15 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
 
 int sk_kps(const GemmArgs &g) { return g.K % 128 == 0 ? 2 : 1; }
 
-long long sk_units(const GemmArgs &g) { return (long long)(g.N / 128) * (g.K / (64 * sk_kps(g))); }
+long long sk_units(const GemmArgs &g) {
+  return (long long)((g.N + 127) / 128) * (g.K / (64 * sk_kps(g)));
+}
 
 // Runs: whole tiles (P = T) when the tiles nearly fill the GPU, which needs no
 // reduction; otherwise one run per SM, at most U runs and at most 15 runs per
 // tile (so a tile never has more than 16 slices).
 int sk_ctas(const GemmArgs &g, int num_sms) {
-  const long long T = g.N / 128, U = sk_units(g);
+  const long long T = (g.N + 127) / 128, U = sk_units(g);
   if (T <= num_sms && 10 * T >= 7LL * num_sms) return (int)T;
   long long P = num_sms;
   if (P > U) P = U;
@@ -344,8 +306,8 @@ int sk_ctas(const GemmArgs &g, int num_sms) {
 cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long slice_stride,
                            int *dev_err, cudaStream_t st) {
   // One row tile of tokens (M <= 256), whole 128 x 64 tiles, fp32 slices in epi.partial.
-  if (g.dtype != 1 || g.M < 1 || g.M > 256 || g.N % BM || g.K % BK || g.ldx % 8)
-    return cudaErrorInvalidValue;
+  if (g.dtype != 1 || g.M < 1 || g.M > 256 || g.K % BK) return cudaErrorInvalidValue;
+  if (g.w_tiled && (g.group_rows % BM)) return cudaErrorInvalidValue;
   if (g.n_groups < 1 || g.n_groups > 3 || g.n_groups * g.group_rows != g.N) return cudaErrorInvalidValue;
   if (g.epi.kind == EPI_QKV && g.epi.d_model % BM) return cudaErrorInvalidValue;
   if (!slices || P < 1 || slice_stride < (long long)g.M * g.N) return cudaErrorInvalidValue;

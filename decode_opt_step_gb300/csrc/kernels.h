@@ -31,6 +31,7 @@ struct Epi {
   const void *bias[3];   // QKV: bq, bk, bv; RELU: bias[0]
   void *out;             // RELU output / QKV q output (storage type)
   int ldo;
+  int out_rows;          // RELU output row-tiled with this R (0 = row-major, stride ldo)
   void *kc, *vc;         // QKV: this layer's K / V cache [B][H][max_seq][hd]
   int d_model, n_heads, head_dim, max_seq;
   int tok_per_seq;       // tokens of one sequence in this launch (Lp prefill, 1 decode)
@@ -47,6 +48,17 @@ inline long long tiled_index(long long n, long long k, long long K) {
   return ((n / 128) * (K / 64) + k / 64) * 8192 + (n % 128) * 64 +
          ((((k % 64) / 8) ^ (n % 8)) * 8) + (k % 8);
 }
+
+// Decode activations that feed the stream-K GEMM are stored row-tiled: for a
+// buffer of R rows (R = the GEMM's token tile, sk_token_tile(M)) and K columns,
+// element (r, k) sits at ((k / 64) * R + r) * 64 + (((k % 64) / 8) ^ (r % 8)) * 8
+// + k % 8, so the KPS k-blocks of a pipeline stage are one contiguous, already
+// swizzled block.  R == 0 means row-major with row stride K.
+__host__ __device__ inline long long act_index(int r, int k, int K, int R) {
+  if (R == 0) return (long long)r * K + k;
+  return ((long long)(k >> 6) * R + r) * 64 + ((((k & 63) >> 3) ^ (r & 7)) << 3) + (k & 7);
+}
+inline int sk_token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
 struct GemmArgs {
   int dtype;             // HE_DTYPE_F32 / HE_DTYPE_BF16
@@ -106,9 +118,10 @@ struct SliceInfo {
 // Result codes of the launchers (cudaError_t values pass through).
 cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st);
 
-// Persistent stream-K tcgen05 GEMM (bf16, M <= 256 tokens, N % 128 == 0, K % 64 == 0)
-// on P CTAs; writes fp32 slices [slot][M][N] (slot stride slice_stride) except for
-// tiles covered by one run under an element-wise a.epi, which are stored directly.
+// Persistent stream-K tcgen05 GEMM (bf16, M <= 256 tokens, K % 64 == 0; a.x row-tiled
+// with R = sk_token_tile(M); N % 128 == 0 for tiled weights, any N for row-major
+// weights) on P CTAs; writes fp32 slices [slot][M][N] (slot stride slice_stride)
+// except for tiles covered by one run under an element-wise a.epi, stored directly.
 // A unit is sk_kps(a) 64-wide k-blocks (2 when K % 128 == 0); sk_units = tiles x
 // units per tile.
 int sk_kps(const GemmArgs &a);
@@ -125,11 +138,16 @@ cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInf
                                  long long split_stride, int ldp, int M, int N, const Epi &epi,
                                  cudaStream_t st);
 
-// x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type).
+// x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type,
+// row-tiled with h_rows rows when h_rows > 0).
 cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
-                            const void *g, const void *b, float eps, void *h, int rows, int d,
+                            const void *g, const void *b, float eps, void *h, int h_rows,
+                            int rows, int d, cudaStream_t st);
+// out (row-tiled, R rows) <- x rows 0..M-1 (row stride ldx), rows M..R-1 zero.  bf16.
+cudaError_t launch_tile_act(const void *x, int M, int K, int ldx, int R, void *out,
                             cudaStream_t st);
+cudaError_t launch_zero(void *p, size_t bytes, cudaStream_t st);
 
 // x[tok] = E[id] + P[pos + off]; h[tok] = LN(x[tok]).  Token tok of a launch is
 // sequence tok / tok_per_seq at position pos0 + tok % tok_per_seq.
@@ -149,14 +167,16 @@ struct HeadArgs {
   const void *tok_emb, *pos_emb; int pos_offset;
   const void *g, *b; float eps;      // first layer's LN1
   float *x; void *h; int d;
+  int h_rows;                        // h row-tiled with this R (0 = row-major)
 };
 cudaError_t launch_head_select(int dtype, const HeadArgs &a, cudaStream_t st);
 
 // Decode attention: one query per (b, h) over keys 0..n_keys-1 of the cache.
 // part: scratch of B*H*split*(hd+2) floats when split > 1.
+// ctx is row-tiled with ctx_rows rows when ctx_rows > 0.
 cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
-                               void *ctx, int B, int H, int hd, int max_seq, int n_keys,
-                               int split, float *part, cudaStream_t st);
+                               void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
+                               int n_keys, int split, float *part, cudaStream_t st);
 int attn_decode_pick_split(int B, int H, int n_keys, int num_sms);
 
 // Prefill attention: causal within each prompt of Lp tokens (positions 0..Lp-1).

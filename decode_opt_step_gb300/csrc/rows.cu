@@ -13,8 +13,8 @@ namespace {
 // LayerNorm of the fp32 row held in shared memory `row[0..d)`: two passes
 // (mean, then the biased variance of the centred values), eps inside the root.
 template <typename T>
-__device__ void ln_store(const float *row, int d, const T *g, const T *b, float eps, T *out,
-                         float *red) {
+__device__ void ln_store(const float *row, int d, const T *g, const T *b, float eps, T *h, int r,
+                         int R, float *red) {
   float s = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) s += row[i];
   const float mean = block_sum(s, red) / (float)d;
@@ -26,7 +26,7 @@ __device__ void ln_store(const float *row, int d, const T *g, const T *b, float 
   const float var = block_sum(v, red) / (float)d;
   const float rstd = 1.0f / sqrtf(var + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x)
-    out[i] = from_f<T>((row[i] - mean) * rstd * to_f<T>(g[i]) + to_f<T>(b[i]));
+    h[act_index(r, i, d, R)] = from_f<T>((row[i] - mean) * rstd * to_f<T>(g[i]) + to_f<T>(b[i]));
 }
 
 template <typename T>
@@ -56,7 +56,7 @@ __global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const 
   }
   const int pos = pos0 + tok % tok_per_seq + pos_offset;
   embed_row<T>(id, pos, tok_emb, pos_emb, d, row, x + (long long)tok * d);
-  ln_store<T>(row, d, g, b, eps, h + (long long)tok * d, red);
+  ln_store<T>(row, d, g, b, eps, h, tok, 0, red);
 }
 
 // Sum of the split slices of one float4 of a row, in slice order (loads of four
@@ -90,7 +90,7 @@ __device__ __forceinline__ float4 sum_slices(const float *p, int split, long lon
 template <typename T>
 __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long split_stride,
                            int ldp, const T *bias, float *x, const T *g, const T *b, float eps,
-                           T *h, int d) {
+                           T *h, int h_rows, int d) {
   extern __shared__ float row[];
   __shared__ float red[33];
   const long long r = blockIdx.x;
@@ -107,7 +107,7 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
     reinterpret_cast<float4 *>(row)[i] = v;
   }
   __syncthreads();
-  ln_store<T>(row, d, g, b, eps, h + r * d, red);
+  ln_store<T>(row, d, g, b, eps, h, (int)r, h_rows, red);
 }
 
 // Element-wise epilogue after a split-K GEMM: four consecutive outputs per thread.
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
     embed_row<T>(s_tok, a.pos + a.pos_offset, static_cast<const T *>(a.tok_emb),
                  static_cast<const T *>(a.pos_emb), a.d, row, a.x + (long long)b * a.d);
     ln_store<T>(row, a.d, static_cast<const T *>(a.g), static_cast<const T *>(a.b), a.eps,
-                static_cast<T *>(a.h) + (long long)b * a.d, red);
+                static_cast<T *>(a.h), b, a.h_rows, red);
   }
 }
 
@@ -298,6 +298,19 @@ __global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const b
   out[q] = res;
 }
 
+__global__ void k_tile_act(const bf16 *x, int M, int K, int ldx, int R, bf16 *out) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)R * K) return;
+  const int r = (int)(e / K), k = (int)(e % K);
+  out[act_index(r, k, K, R)] = r < M ? x[(long long)r * ldx + k] : __float2bfloat16_rn(0.f);
+}
+
+__global__ void k_zero16(uint4 *p, long long n16) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+
 __global__ void k_copy16(uint4 *dst, const uint4 *src, long long n16) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
        i += (long long)gridDim.x * blockDim.x)
@@ -346,8 +359,8 @@ cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInf
 
 cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
-                            const void *g, const void *b, float eps, void *h, int rows, int d,
-                            cudaStream_t st) {
+                            const void *g, const void *b, float eps, void *h, int h_rows,
+                            int rows, int d, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
     return cudaErrorInvalidValue;
@@ -355,11 +368,11 @@ cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si
   if (dtype == 1)
     k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
                                                        (const bf16 *)bias, x, (const bf16 *)g,
-                                                       (const bf16 *)b, eps, (bf16 *)h, d);
+                                                       (const bf16 *)b, eps, (bf16 *)h, h_rows, d);
   else
     k_resid_ln<float><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
                                                         (const float *)bias, x, (const float *)g,
-                                                        (const float *)b, eps, (float *)h, d);
+                                                        (const float *)b, eps, (float *)h, h_rows, d);
   return cudaGetLastError();
 }
 
@@ -415,6 +428,23 @@ cudaError_t launch_fuse_tiled(void *out, const void *src, const void *a, const v
   k_fuse_tiled<<<(int)((n + 255) / 256), 256, 0, st>>>((uint4 *)out, (const bf16 *)src,
                                                       (const bf16 *)a, (const bf16 *)bm, rows,
                                                       cols, r, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_act(const void *x, int M, int K, int ldx, int R, void *out,
+                            cudaStream_t st) {
+  if (K % 64 || R < M) return cudaErrorInvalidValue;
+  const long long n = (long long)R * K;
+  k_tile_act<<<(int)((n + 255) / 256), 256, 0, st>>>((const bf16 *)x, M, K, ldx, R, (bf16 *)out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero(void *p, size_t bytes, cudaStream_t st) {
+  if (bytes % 16 || (uintptr_t)p % 16) return cudaErrorInvalidValue;
+  const long long n16 = (long long)(bytes / 16);
+  if (n16 == 0) return cudaSuccess;
+  const long long blocks = (n16 + 255) / 256;
+  k_zero16<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>((uint4 *)p, n16);
   return cudaGetLastError();
 }
 

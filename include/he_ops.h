@@ -23,10 +23,12 @@ extern "C" {
  * slices of whole 64-wide blocks (no empty slice allowed) whose fp32 partial
  * sums go to scratch [split][M][N] and are then added in slice order.
  * split <= 0 runs the persistent stream-K kernel of the decode projections
- * (bf16, M <= 256, N % 128 == 0, K % 64 == 0): the (128-row tile, 64-wide
- * k-block) units are cut into P equal runs, P = -split if split < 0 (at most
- * min(units, 15 * tiles)), else the engine's choice (one per SM); scratch needs
- * 16 * M * N floats.  All pointers are device memory; asynchronous on `stream`. */
+ * (bf16, M <= 256, K % 64 == 0, N % 128 == 0 with tiled weights): the
+ * (128-row tile, k-block) units are cut into P equal runs, P = -split if
+ * split < 0 (at most min(units, 15 * tiles)), else the engine's choice (one per
+ * SM); scratch needs 16 * M * N floats followed by R * K bf16 (R = M rounded up
+ * to 16, 32, 64, 128 or 256) for the row-tiled copy of x that kernel reads.
+ * All pointers are device memory; asynchronous on `stream`. */
 he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
                        int M, int N, int K, int split, float *scratch, void *stream);
 

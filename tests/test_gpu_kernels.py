@@ -124,3 +124,15 @@ def test_linear_bf16_stream_k(cuda_device, M, N, K, ctas, tiled):
     torch.cuda.synchronize()
     err = np.abs(y.cpu().numpy() - _exact(x, w))
     assert (err <= _bound(x, w, K)).all(), err.max()
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 50272 // 8, 512), (3, 1000, 256), (64, 200, 1024)])
+def test_linear_bf16_stream_k_ragged_rows(cuda_device, M, N, K):
+    # row-major weights with N not a multiple of 128 (the LM head's vocabulary)
+    g = torch.Generator().manual_seed(M + N)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    y = he.linear(x, w, split=0)
+    torch.cuda.synchronize()
+    err = np.abs(y.cpu().numpy() - _exact(x, w))
+    assert (err <= _bound(x, w, K)).all(), err.max()
