@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "row_epilogue.cuh"
 
 namespace he {
 
@@ -213,22 +214,14 @@ __global__ void __launch_bounds__(192, 1)
       const bool direct = S == 1 && epi.kind != EPI_PARTIAL;
       const int row = t * BM + warp * 32 + lane;
       const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      constexpr int W = BN >= 32 ? 32 : 16;
+      const RowEpi re = row_epi_prepare(epi, row < a.N ? row : 0, direct ? nullptr : a.slices,
+                                        a.slice_stride, slot, a.N);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tl + c0, v);
-        if (live && row < a.N) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = c0 + j;
-            if (tok < a.M) {
-              if (direct)
-                epi_store<bf16>(epi, 0, tok, row, v[j]);
-              else
-                a.slices[(long long)slot * a.slice_stride + (long long)tok * a.N + row] = v[j];
-            }
-          }
-        }
+      for (int c0 = 0; c0 < BN; c0 += W) {
+        float v[W];
+        tmem_load_cols<W>(tl + c0, v);
+        if (live && row < a.N && c0 < a.M) row_epi_store<W>(re, c0, min(W, a.M - c0), v);
       }
       tc_fence_before();
       __syncwarp();

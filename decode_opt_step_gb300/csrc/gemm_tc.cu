@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "row_epilogue.cuh"
 
 namespace he {
 
@@ -162,17 +163,17 @@ __global__ void __launch_bounds__(192, 1)
     const bool live = ok && !*(volatile int *)abort_flag && nkb > 0;
     const int row = m_tile * BM + warp * 32 + lane;  // output feature n
     const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16);
+    constexpr int W = BN >= 32 ? 32 : 16;
+    const bool part = epi.kind == EPI_PARTIAL;
+    const RowEpi re = row_epi_prepare(epi, row < N ? row : 0, part ? epi.partial : nullptr,
+                                      epi.split_stride, split, epi.ldp);
+    const int tok_base = n_tile * BN;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      tmem_ld16(tl + c0, v);
-      if (live && row < N) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int tok = n_tile * BN + c0 + j;
-          if (tok < M) epi_store<bf16>(epi, split, tok, row, v[j]);
-        }
-      }
+    for (int c0 = 0; c0 < BN; c0 += W) {
+      float v[W];
+      tmem_load_cols<W>(tl + c0, v);
+      if (live && row < N && tok_base + c0 < M)
+        row_epi_store<W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
     }
   }
   tc_fence_before();
