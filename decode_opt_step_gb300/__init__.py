@@ -90,6 +90,8 @@ _SIGNATURES = {
     "he_op_linear": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
                              c_int, c_int, c_void_p, c_void_p]),
     "he_op_tile_weight": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p]),
+    "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                  c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
 }
 
 _lib = None
@@ -315,6 +317,22 @@ class Engine:
             self.close()
         except Exception:
             pass
+
+
+def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
+    """Decode attention through he_op_attn_decode: q [B][H*hd], kc/vc [B][H][T][hd]."""
+    import torch
+    lib = load_library()
+    B, H, T, hd = kc.shape
+    ctx = torch.empty((B, H * hd), dtype=q.dtype, device=q.device)
+    part = (torch.empty(B * H * split * (hd + 2), dtype=torch.float32, device=q.device)
+            if split > 1 else None)
+    dt = HE_DTYPE_BF16 if q.dtype == torch.bfloat16 else HE_DTYPE_F32
+    _check(lib.he_op_attn_decode(dt, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), ctx.data_ptr(),
+                                 B, H, hd, T, n_keys, split,
+                                 part.data_ptr() if part is not None else None,
+                                 _stream_handle(torch, stream)))
+    return ctx
 
 
 def tile_weight(w, stream=None):

@@ -833,6 +833,22 @@ he_status he_get_stats(he_engine *h, he_stats *s) {
 // ---------------------------------------------------------------------------
 // Kernel-level entry (he_ops.h)
 // ---------------------------------------------------------------------------
+he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void *vc, void *ctx,
+                            int B, int H, int hd, int max_seq, int n_keys, int split, float *part,
+                            void *stream) {
+  g_err.clear();
+  if (!q || !kc || !vc || !ctx) return fail(HE_ERR_ARG, "NULL buffer");
+  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
+  if (B < 1 || H < 1 || n_keys < 1 || n_keys > max_seq || split < 1 || split > n_keys)
+    return fail(HE_ERR_ARG, "bad sizes");
+  if (hd != 32 && hd != 64 && hd != 128) return fail(HE_ERR_UNSUPPORTED, "head_dim %d", hd);
+  if (split > 1 && !part) return fail(HE_ERR_ARG, "split > 1 needs part");
+  cudaError_t r = launch_attn_decode(dtype, q, kc, vc, ctx, 0, B, H, hd, max_seq, n_keys, split,
+                                     part, static_cast<cudaStream_t>(stream));
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_attn_decode");
+  return HE_OK;
+}
+
 he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream) {
   g_err.clear();
   if (!w || !out) return fail(HE_ERR_ARG, "NULL buffer");

@@ -46,6 +46,20 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
  * overlap with w) from the row-major w; asynchronous on `stream`. */
 he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream);
 
+/* Single-query attention of one decode step over the KV cache
+ * ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of ChatGPT-like
+ * Models at All Scales", §3.4 "Inference Mode: Generation Phase Optimizations",
+ * Optimizations 1 and 2: attention specialised for one new query against a
+ * long cached context, keys and values read from the cache).
+ * q: [B][H*hd] (already scaled by hd^-1/2); kc, vc: [B][H][max_seq][hd];
+ * ctx: [B][H*hd] row-major out; keys/values 0..n_keys-1 are used.  split >= 1
+ * cuts the keys of each (b, h) into that many slices merged afterwards (part:
+ * B*H*split*(hd+2) floats when split > 1).  dtype F32 or BF16 (fp32 softmax and
+ * accumulation either way); hd in {32, 64, 128}.  Asynchronous on `stream`. */
+he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void *vc, void *ctx,
+                            int B, int H, int hd, int max_seq, int n_keys, int split, float *part,
+                            void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -136,3 +136,23 @@ def test_linear_bf16_stream_k_ragged_rows(cuda_device, M, N, K):
     torch.cuda.synchronize()
     err = np.abs(y.cpu().numpy() - _exact(x, w))
     assert (err <= _bound(x, w, K)).all(), err.max()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B,H,hd,T,n,split", [(2, 4, 32, 40, 17, 1), (3, 5, 64, 300, 257, 1),
+                                              (1, 2, 128, 512, 511, 4), (4, 3, 128, 64, 1, 1),
+                                              (2, 2, 64, 200, 133, 3)])
+def test_attn_decode_matches_softmax(cuda_device, dtype, B, H, hd, T, n, split):
+    g = torch.Generator().manual_seed(B * 100 + n)
+    q = (torch.randn(B, H * hd, generator=g) * hd ** -0.5).to(dtype).cuda()
+    kc = torch.randn(B, H, T, hd, generator=g).to(dtype).cuda()
+    vc = torch.randn(B, H, T, hd, generator=g).to(dtype).cuda()
+    ctx = he.attn_decode(q, kc, vc, n, split)
+    torch.cuda.synchronize()
+    qd = q.double().cpu().view(B, H, 1, hd)
+    kd, vd = kc.double().cpu()[:, :, :n], vc.double().cpu()[:, :, :n]
+    p = torch.softmax(qd @ kd.transpose(-1, -2), -1)
+    ref = (p @ vd).view(B, H * hd).numpy()
+    got = ctx.double().cpu().numpy()
+    tol = 1e-5 if dtype == torch.float32 else 1e-2  # bf16 output rounding
+    np.testing.assert_allclose(got, ref, atol=tol, rtol=tol)
