@@ -197,6 +197,17 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max(value: float, dist, device=None) -> float:
+    """Max of a per-rank float over all ranks (plain value without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload_config(cfg):
     return {"workload": f"{cfg.name} greedy generation",
             "layers": cfg.n_layers, "d_model": cfg.d_model, "heads": cfg.n_heads,
@@ -299,10 +310,7 @@ def main():
     wall_ms = start.elapsed_time(end)
     launches = eng.stats()["launches"] - l0
     eng.set_profiling(())
-    t = torch.tensor([wall_ms], device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    wall_ms = float(t.item())
+    wall_ms = reduce_max(wall_ms, dist, dev)
     ms_per_step = wall_ms / args.steps
     tokens = B * Lgen * world
     value = tokens / (ms_per_step / 1000.0)
@@ -320,11 +328,8 @@ def main():
             eng.release_workspace()
             eng.retake_workspace()
         barrier()
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        te = torch.tensor([e2e_s], device=dev)
-        if dist is not None:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": tokens / float(te.item()), "unit": "tokens/s",
+        e2e_s = reduce_max((time.perf_counter() - t0) / args.steps, dist, dev)
+        e2e = {"value": tokens / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": B * Lp * 4, "d2h_bytes_per_step": B * Lgen * 8}
 
     # ---- roofline of the dominant kernel and the decode phase ----
@@ -341,7 +346,8 @@ def main():
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
     pk = per_kernel[dom]
     traffic = None
-    roofline = {"bound": "hbm", "kernel": "k_attn_decode" if dom == "attn_decode" else "k_gemm_tc",
+    roofline = {"bound": "hbm",
+                "kernel": "k_attn_decode" if dom == "attn_decode" else "k_gemm_sk (decode projections)",
                 "achieved": pk["gbs"], "peak": hbm_peak, "unit": "GB/s",
                 "frac": pk["gbs"] / hbm_peak if pk["gbs"] else None, "traffic": traffic,
                 "peak_kind": f"{peak_kind} HBM copy bandwidth"}

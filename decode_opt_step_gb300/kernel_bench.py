@@ -1,0 +1,71 @@
+"""Microbenchmark of single kernels at the OPT-13B decode shapes (B = 128).
+
+    python -m decode_opt_step_gb300.kernel_bench [attn_decode|gemm_sk|all] [--iters N]
+
+Small, self-contained cases (a few GB on the device) that run one kernel of the
+generation path the way a decode step does, for profiling one kernel at a time:
+
+* attn_decode: one decode-attention launch, B=128, 40 heads of 128, 384 cached
+  keys (1.0 GB of K and V, above the 126 MB L2);
+* gemm_sk: the fc1 projection, 128 tokens x 5120 -> 20480, tiled weights,
+  stream-K over one CTA per SM (210 MB of weights, two copies alternated).
+
+Prints the CUDA-event time per launch and the algorithmic GB/s.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import decode_opt_step_gb300 as he
+
+
+def _time(fn, iters):
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def attn_decode(iters):
+    B, H, hd, T, n = 128, 40, 128, 512, 384
+    q = (torch.randn(B, H * hd, device="cuda") * hd ** -0.5).to(torch.bfloat16)
+    kc = torch.randn(B, H, T, hd, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(B, H, T, hd, device="cuda").to(torch.bfloat16)
+    ms = _time(lambda i: he.attn_decode(q, kc, vc, n), iters)
+    byts = 2 * B * H * n * hd * 2
+    print(f"attn_decode B={B} H={H} hd={hd} keys={n}: {ms * 1e3:.1f} us/launch, "
+          f"{byts / (ms / 1e3) / 1e9:.0f} GB/s")
+
+
+def gemm_sk(iters):
+    M, N, K = 128, 20480, 5120
+    ws = [torch.randn(N, K, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    wt = [he.tile_weight(w) for w in ws]
+    x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    ms = _time(lambda i: he.linear(x, ws[i % 2], split=0, w_tiled=wt[i % 2]), iters)
+    print(f"gemm_sk M={M} N={N} K={K} (with the op's input tiling and slice reduction): "
+          f"{ms * 1e3:.1f} us/call, {N * K * 2 / (ms / 1e3) / 1e9:.0f} GB/s of weights")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", nargs="?", default="all", choices=["attn_decode", "gemm_sk", "all"])
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+    torch.cuda.set_device(0)
+    if args.case in ("attn_decode", "all"):
+        attn_decode(args.iters)
+    if args.case in ("gemm_sk", "all"):
+        gemm_sk(args.iters)
+
+
+if __name__ == "__main__":
+    main()
