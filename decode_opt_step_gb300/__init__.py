@@ -20,7 +20,7 @@ _LIB_PATH = Path(__file__).resolve().parent / "libhe.so"
 
 HE_OK, HE_ERR_ARG, HE_ERR_STATE, HE_ERR_OOM = 0, -1, -2, -3
 HE_ERR_CUDA, HE_ERR_UNSUPPORTED, HE_ERR_DEVICE_CHECK = -4, -5, -6
-HE_DTYPE_F32, HE_DTYPE_BF16 = 0, 1
+HE_DTYPE_F32, HE_DTYPE_BF16, HE_DTYPE_F16 = 0, 1, 2
 PROJ = ("wq", "wk", "wv", "wo", "w1", "w2")
 BIAS = ("bq", "bk", "bv", "bo", "b1", "b2")
 KCLASS = ("gemm", "attn_decode", "norm", "head", "prefill_gemm", "prefill_attn", "other", "spare")
@@ -319,6 +319,11 @@ class Engine:
             pass
 
 
+def _dtype_code(torch, dt):
+    return {torch.float32: HE_DTYPE_F32, torch.bfloat16: HE_DTYPE_BF16,
+            torch.float16: HE_DTYPE_F16}[dt]
+
+
 def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
     """Decode attention through he_op_attn_decode: q [B][H*hd], kc/vc [B][H][T][hd]."""
     import torch
@@ -327,7 +332,7 @@ def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
     ctx = torch.empty((B, H * hd), dtype=q.dtype, device=q.device)
     part = (torch.empty(B * H * split * (hd + 2), dtype=torch.float32, device=q.device)
             if split > 1 else None)
-    dt = HE_DTYPE_BF16 if q.dtype == torch.bfloat16 else HE_DTYPE_F32
+    dt = _dtype_code(torch, q.dtype)
     _check(lib.he_op_attn_decode(dt, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), ctx.data_ptr(),
                                  B, H, hd, T, n_keys, split,
                                  part.data_ptr() if part is not None else None,
@@ -336,12 +341,12 @@ def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
 
 
 def tile_weight(w, stream=None):
-    """The tiled streaming layout of a bf16 [N][K] weight (he_op_tile_weight), flat."""
+    """The tiled streaming layout of a 16-bit [N][K] weight (he_op_tile_weight), flat."""
     import torch
     lib = load_library()
-    if w.dtype != torch.bfloat16 or not w.is_contiguous():
-        raise TypeError("w must be a contiguous bf16 tensor")
-    out = torch.empty(w.numel(), dtype=torch.bfloat16, device=w.device)
+    if w.dtype not in (torch.bfloat16, torch.float16) or not w.is_contiguous():
+        raise TypeError("w must be a contiguous bf16 or fp16 tensor")
+    out = torch.empty(w.numel(), dtype=w.dtype, device=w.device)
     _check(lib.he_op_tile_weight(w.data_ptr(), out.data_ptr(), w.shape[0], w.shape[1],
                                  _stream_handle(torch, stream)))
     return out
@@ -356,8 +361,8 @@ def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     lib = load_library()
     M, K = x.shape
     N = w.shape[0]
-    if x.dtype != w.dtype or x.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("x and w must both be bf16 or both fp32")
+    if x.dtype != w.dtype or x.dtype not in (torch.bfloat16, torch.float16, torch.float32):
+        raise TypeError("x and w must have the same type: bf16, fp16 or fp32")
     if x.stride(1) != 1 or not w.is_contiguous():
         raise ValueError("x rows and w must be dense")
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
@@ -368,7 +373,7 @@ def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     else:
         scratch = (torch.empty((split, M, N), dtype=torch.float32, device=x.device)
                    if split > 1 else None)
-    dt = HE_DTYPE_BF16 if x.dtype == torch.bfloat16 else HE_DTYPE_F32
+    dt = _dtype_code(torch, x.dtype)
     wp, layout = (w.data_ptr(), 0) if w_tiled is None else (w_tiled.data_ptr(), 1)
     _check(lib.he_op_linear(dt, x.data_ptr(), x.stride(0), wp, layout, y.data_ptr(), M, N, K,
                             split, scratch.data_ptr() if scratch is not None else None,

@@ -10,7 +10,7 @@
 //
 // Prefill: causal attention inside each prompt, 64 queries per CTA, key blocks
 // of 64 staged in shared memory, online softmax across key blocks.  This file
-// holds the fp32 CUDA-core version; bf16 runs on tensor cores
+// holds the fp32 CUDA-core version; the 16-bit types run on tensor cores
 // (attn_prefill_mma.cu).
 #include "common.cuh"
 #include "kernels.h"
@@ -28,6 +28,19 @@ template <> struct Vec16<bf16> {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <> struct Vec16<f16> {
+  static constexpr int N = 8;
+  __device__ static void load(const f16 *p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(h[i]);
       v[2 * i] = f.x;
       v[2 * i + 1] = f.y;
     }
@@ -284,37 +297,35 @@ int attn_decode_pick_split(int B, int H, int n_keys, int num_sms) {
   return (n_keys + per - 1) / per;
 }
 
-cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
+cudaError_t launch_attn_decode(int act, const void *q, const void *kc, const void *vc,
                                void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
                                int n_keys, int split, float *part, cudaStream_t st) {
   if (n_keys <= 0 || split < 1) return cudaErrorInvalidValue;
-  if (dtype == 1) {
-    if (hd == 128) return decode_t<bf16, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 64) return decode_t<bf16, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 32) return decode_t<bf16, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-  } else {
-    if (hd == 128) return decode_t<float, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 64) return decode_t<float, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 32) return decode_t<float, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-  }
+  auto run = [&](auto tag) -> cudaError_t {
+    using T = decltype(tag);
+    if (hd == 128) return decode_t<T, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 64) return decode_t<T, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 32) return decode_t<T, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    return cudaErrorInvalidValue;
+  };
+  if (act == ACT_BF16) return run(bf16{});
+  if (act == ACT_F16) return run(f16{});
+  if (act == ACT_F32) return run(0.f);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_prefill_bf16_mma(const void *q, const void *kc, const void *vc, void *ctx,
-                                         int B, int Lp, int H, int hd, int max_seq,
-                                         cudaStream_t st);
+cudaError_t launch_attn_prefill_mma(int act, const void *q, const void *kc, const void *vc,
+                                    void *ctx, int B, int Lp, int H, int hd, int max_seq,
+                                    cudaStream_t st);
 
-cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const void *vc,
+cudaError_t launch_attn_prefill(int act, const void *q, const void *kc, const void *vc,
                                 void *ctx, int B, int Lp, int H, int hd, int max_seq,
                                 cudaStream_t st) {
-  if (dtype == 1) {
-    // bf16: tensor cores (attn_prefill_mma.cu)
-    return launch_attn_prefill_bf16_mma(q, kc, vc, ctx, B, Lp, H, hd, max_seq, st);
-  } else {
-    if (hd == 128) return prefill_t<float, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-    if (hd == 64) return prefill_t<float, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-    if (hd == 32) return prefill_t<float, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-  }
+  if (act != ACT_F32)  // 16-bit types: tensor cores (attn_prefill_mma.cu)
+    return launch_attn_prefill_mma(act, q, kc, vc, ctx, B, Lp, H, hd, max_seq, st);
+  if (hd == 128) return prefill_t<float, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+  if (hd == 64) return prefill_t<float, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+  if (hd == 32) return prefill_t<float, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
   return cudaErrorInvalidValue;
 }
 

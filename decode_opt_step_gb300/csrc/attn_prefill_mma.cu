@@ -1,10 +1,12 @@
-// Prefill (causal) attention for bf16 on tensor cores (mma.sync m16n8k16, fp32
+// Prefill (causal) attention for bf16 or fp16 on tensor cores (mma.sync m16n8k16, fp32
 // accumulation), flash-style: one CTA = 4 warps = 64 queries of one (b, h); key
 // and value blocks of 64 rows are staged in shared memory (rows padded by 16
 // bytes so ldmatrix reads are conflict-free); scores, the running softmax and
 // the output stay in registers.  Scores S = Q K^T use ldmatrix fragments of Q
 // (A, row-major) and K (B, "col" = K rows); the probabilities are re-packed from
 // the S accumulators into A fragments for O += P V, with V read by ldmatrix.trans.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,23 +24,38 @@ __device__ __forceinline__ void ldm_x4_t(uint32_t (&r)[4], const void *p) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(p)));
 }
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+template <typename T>
+__device__ __forceinline__ void mma_16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                       uint32_t b1) {
+  if constexpr (std::is_same<T, bf16>::value)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (std::is_same<T, bf16>::value) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
 }
 
 // Copies a [64][HD] bf16 tile (rows r0.., row stride `ld` elements, rows >= nrows
 // zero) into shared memory with row stride HD + 8.
 template <int HD>
-__device__ __forceinline__ void load_tile(bf16 *dst, const bf16 *src, long long ld, int nrows) {
+__device__ __forceinline__ void load_tile(uint16_t *dst, const uint16_t *src, long long ld,
+                                          int nrows) {
   constexpr int CH = HD / 8;  // 16-byte chunks per row
   for (int e = threadIdx.x; e < 64 * CH; e += 128) {
     const int r = e / CH, c = e - r * CH;
@@ -48,18 +65,18 @@ __device__ __forceinline__ void load_tile(bf16 *dst, const bf16 *src, long long 
   }
 }
 
-template <int HD>
+template <typename T, int HD>
 __global__ void __launch_bounds__(128)
-    k_attn_prefill_mma(const bf16 *__restrict__ q, const bf16 *__restrict__ kc,
-                       const bf16 *__restrict__ vc, bf16 *__restrict__ ctx, int H, int Lp,
+    k_attn_prefill_mma(const uint16_t *__restrict__ q, const uint16_t *__restrict__ kc,
+                       const uint16_t *__restrict__ vc, T *__restrict__ ctx, int H, int Lp,
                        int max_seq) {
   constexpr int LD = HD + 8;
   constexpr int KS = HD / 16;  // k-steps of Q K^T
   constexpr int DT = HD / 8;   // 8-wide output tiles
   extern __shared__ __align__(16) uint8_t smraw[];
-  bf16 *qs = reinterpret_cast<bf16 *>(smraw);
-  bf16 *ks = qs + 64 * LD;
-  bf16 *vs = ks + 64 * LD;
+  uint16_t *qs = reinterpret_cast<uint16_t *>(smraw);
+  uint16_t *ks = qs + 64 * LD;
+  uint16_t *vs = ks + 64 * LD;
   const int qb = blockIdx.x, bh = blockIdx.y;
   const int b = bh / H, h = bh - b * H;
   const int d = H * HD;
@@ -102,8 +119,8 @@ __global__ void __launch_bounds__(128)
         const int r = jp * 16 + (lane & 7) + 8 * (lane >> 4);
         const int c = kk * 16 + 8 * ((lane >> 3) & 1);
         ldm_x4(kf, ks + r * LD + c);
-        mma_bf16(s[2 * jp], qa[kk], kf[0], kf[1]);
-        mma_bf16(s[2 * jp + 1], qa[kk], kf[2], kf[3]);
+        mma_16<T>(s[2 * jp], qa[kk], kf[0], kf[1]);
+        mma_16<T>(s[2 * jp + 1], qa[kk], kf[2], kf[3]);
       }
     }
     // causal mask and running max
@@ -149,18 +166,18 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
-      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      pa[0] = pack2<T>(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack2<T>(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack2<T>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack2<T>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
 #pragma unroll
       for (int dp = 0; dp < DT / 2; ++dp) {  // pairs of 8-wide output tiles
         uint32_t vf[4];
         const int r = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
         const int c = dp * 16 + 8 * (lane >> 4);
         ldm_x4_t(vf, vs + r * LD + c);
-        mma_bf16(o[2 * dp], pa, vf[0], vf[1]);
-        mma_bf16(o[2 * dp + 1], pa, vf[2], vf[3]);
+        mma_16<T>(o[2 * dp], pa, vf[0], vf[1]);
+        mma_16<T>(o[2 * dp + 1], pa, vf[2], vf[3]);
       }
     }
   }
@@ -173,39 +190,45 @@ __global__ void __launch_bounds__(128)
   for (int i = 0; i < DT; ++i) {
     const int c = h * HD + i * 8 + 2 * tg;
     if (tq0 < Lp)
-      *reinterpret_cast<__nv_bfloat162 *>(ctx + ((long long)b * Lp + tq0) * d + c) =
-          __floats2bfloat162_rn(o[i][0] * i0, o[i][1] * i0);
+      *reinterpret_cast<uint32_t *>(ctx + ((long long)b * Lp + tq0) * d + c) =
+          pack2<T>(o[i][0] * i0, o[i][1] * i0);
     if (tq1 < Lp)
-      *reinterpret_cast<__nv_bfloat162 *>(ctx + ((long long)b * Lp + tq1) * d + c) =
-          __floats2bfloat162_rn(o[i][2] * i1, o[i][3] * i1);
+      *reinterpret_cast<uint32_t *>(ctx + ((long long)b * Lp + tq1) * d + c) =
+          pack2<T>(o[i][2] * i1, o[i][3] * i1);
   }
 }
 
-template <int HD>
+template <typename T, int HD>
 cudaError_t run(const void *q, const void *kc, const void *vc, void *ctx, int B, int Lp, int H,
                 int max_seq, cudaStream_t st) {
-  const size_t sm = (size_t)3 * 64 * (HD + 8) * sizeof(bf16);
+  const size_t sm = (size_t)3 * 64 * (HD + 8) * sizeof(uint16_t);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_mma<HD>,
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_mma<T, HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   dim3 grid((Lp + 63) / 64, B * H);
-  k_attn_prefill_mma<HD><<<grid, 128, sm, st>>>((const bf16 *)q, (const bf16 *)kc,
-                                                (const bf16 *)vc, (bf16 *)ctx, H, Lp, max_seq);
+  k_attn_prefill_mma<T, HD><<<grid, 128, sm, st>>>((const uint16_t *)q, (const uint16_t *)kc,
+                                                   (const uint16_t *)vc, (T *)ctx, H, Lp, max_seq);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_prefill_bf16_mma(const void *q, const void *kc, const void *vc, void *ctx,
-                                         int B, int Lp, int H, int hd, int max_seq,
-                                         cudaStream_t st) {
-  if (hd == 128) return run<128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-  if (hd == 64) return run<64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
-  if (hd == 32) return run<32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+cudaError_t launch_attn_prefill_mma(int act, const void *q, const void *kc, const void *vc,
+                                    void *ctx, int B, int Lp, int H, int hd, int max_seq,
+                                    cudaStream_t st) {
+  auto go = [&](auto tag) -> cudaError_t {
+    using T = decltype(tag);
+    if (hd == 128) return run<T, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 64) return run<T, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    if (hd == 32) return run<T, 32>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
+    return cudaErrorInvalidValue;
+  };
+  if (act == ACT_BF16) return go(bf16{});
+  if (act == ACT_F16) return go(f16{});
   return cudaErrorInvalidValue;
 }
 

@@ -1,23 +1,29 @@
 // Shared device helpers for the generation kernels (sm_103a).
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kernels.h"
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // ---------------------------------------------------------------------------
-// Element conversions.  T is the storage type of parameters / KV / GEMM inputs.
+// Element conversions.  PT is the storage type of the caller's parameters (float
+// or bf16); CT the type of activations, KV cache and GEMM operands (float, bf16,
+// or fp16 while LoRA is fused on the bf16 path).
 // ---------------------------------------------------------------------------
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float to_f<f16>(f16 v) { return __half2float(v); }
 
 template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ f16 from_f<f16>(float v) { return __float2half_rn(v); }
 
 __device__ __forceinline__ void set_dev_error(int *flag, int bit) {
   if (flag) atomicOr(flag, bit);

@@ -60,7 +60,8 @@ struct he_engine {
   he_allocator alloc{};
 
   bool taken = false, fused = false;
-  bool tiled = false;  // projections hold the tiled layout (bf16 while fused)
+  bool tiled = false;  // projections hold the tiled layout (bf16 path while fused)
+  int act = 0;         // activation type of the generation in flight (ActType)
   unsigned prof_mask = 0;
   // workspace (released / retaken together)
   Buf kc, vc, x, h, q, ctx, mid, partial, logits, attn_part, ids_in, ids_out, lp_out, logmap;
@@ -216,10 +217,11 @@ int act_rows(const he_engine *h, int B, bool decode) {
 // fp32 slices stay in h->partial and the returned SliceInfo tells the row
 // consumer how to add them.
 SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
-               int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w) {
+               int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w, int act) {
   he_engine *h = c.h;
   GemmArgs a{};
   a.dtype = h->cfg.dtype;
+  a.act = act;
   a.x = x;
   a.ldx = ldx;
   for (int g = 0; g < n_groups; ++g) a.w[g] = w[g];
@@ -242,7 +244,7 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
     c.check(launch_gemm_sk(a, P, part, stride, static_cast<int *>(h->err.p), c.st), 1);
     // P == tiles: every tile is one run and was stored by the GEMM itself
     if (epi.kind != EPI_PARTIAL && P != T)
-      c.check(launch_sk_reduce_epi(a.dtype, part, si, stride, a.N, M, a.N, epi, c.st), 1);
+      c.check(launch_sk_reduce_epi(a.dtype, a.act, part, si, stride, a.N, M, a.N, epi, c.st), 1);
     return si;
   }
   int split = decode ? gemm_pick_split(a, h->num_sms) : 1;
@@ -262,7 +264,7 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   }
   c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
   if (epi.kind != EPI_PARTIAL && split > 1)
-    c.check(launch_reduce_epi(a.dtype, part, split, stride, a.N, M, a.N, epi, c.st), 1);
+    c.check(launch_reduce_epi(a.dtype, a.act, part, split, stride, a.N, M, a.N, epi, c.st), 1);
   return si;
 }
 
@@ -301,16 +303,20 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   const bool dec = !prefill;
   const int R = act_rows(h, B, dec);  // decode: h, ctx, mid are row-tiled with R rows
   const bool tw = h->tiled;
+  const int act = h->act;
+  // the last layer's final LayerNorm feeds the LM head, whose weight is the caller's
+  // embedding table: that output is written in the parameter type
+  const int out_act = l == cf.n_layers - 1 ? cf.dtype : act;
   // LN1 + QKV (+ KV append at the tokens' positions)
   const void *wqkv[3] = {lw.w[HE_PROJ_Q], lw.w[HE_PROJ_K], lw.w[HE_PROJ_V]};
-  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw);
+  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw, act);
   Epi ep{};
   ep.kind = EPI_PARTIAL;
   // attention
   const size_t lay = (size_t)l * h->kv_layer_elems() * h->elem;
   if (prefill) {
     Timed t(h, HE_KCLASS_PREFILL_ATTN, c.st);
-    c.check(launch_attn_prefill(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
+    c.check(launch_attn_prefill(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
                                 tok_per_seq, cf.n_heads, hd, cf.max_seq, c.st),
             1);
   } else {
@@ -318,17 +324,17 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
     int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
     if (split > kMaxAttnSplit) split = kMaxAttnSplit;
     Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
-    c.check(launch_attn_decode(cf.dtype, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, R,
+    c.check(launch_attn_decode(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, R,
                                B, cf.n_heads, hd, cf.max_seq, n_keys, split,
                                static_cast<float *>(h->attn_part.p), c.st),
             split > 1 ? 2 : 1);
   }
   // out projection -> partials; + bo + residual; LN2
   const void *wo[1] = {lw.w[HE_PROJ_O]};
-  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw);
+  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw, act);
   {
     Timed t(h, HE_KCLASS_NORM, c.st);
-    c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
+    c.check(launch_resid_ln(cf.dtype, act, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                             lw.b[HE_PROJ_O], static_cast<float *>(h->x.p), lw.ln2_g, lw.ln2_b,
                             cf.ln_eps, h->h.p, R, M, d, c.st),
             1);
@@ -341,15 +347,15 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   er.ldo = cf.ffn;
   er.out_rows = R;
   const void *w1[1] = {lw.w[HE_PROJ_FC1]};
-  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw);
+  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw, act);
   // fc2 -> partials; + b2 + residual; next LN
   const void *w2[1] = {lw.w[HE_PROJ_FC2]};
-  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw);
+  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw, act);
   const bool last = l == cf.n_layers - 1;
   const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
   const void *bb = last ? h->lnf_b : h->layers[l + 1].ln1_b;
   Timed t(h, HE_KCLASS_NORM, c.st);
-  c.check(launch_resid_ln(cf.dtype, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
+  c.check(launch_resid_ln(cf.dtype, out_act, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                           lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
                           h->h.p, R, M, d, c.st),
           1);
@@ -372,11 +378,12 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   el.ldp = cf.vocab;
   if (dec && use_stream_k(h, B, cf.vocab, cf.d_model, true, false)) {
     const void *we[1] = {h->tok_emb};
-    gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false);
+    gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false, cf.dtype);
   } else {
     Timed t(h, HE_KCLASS_HEAD, c.st);
     GemmArgs a{};
     a.dtype = cf.dtype;
+    a.act = cf.dtype;  // the head reads the caller's embedding table
     a.x = hrows;
     a.ldx = ldh;
     a.w[0] = h->tok_emb;
@@ -422,7 +429,7 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   ha.h = h->h.p;
   ha.d = cf.d_model;
   ha.h_rows = R;
-  c.check(launch_head_select(cf.dtype, ha, c.st), 1);
+  c.check(launch_head_select(cf.dtype, h->act, ha, c.st), 1);
 }
 
 he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int Lgen,
@@ -431,6 +438,9 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   const he_config &cf = h->cfg;
   const int d = cf.d_model;
   Ctx c{h, st};
+  // activation type: fp32 workload -> fp32; bf16 workload -> fp16 while fused (the
+  // fused weights are fp16), else bf16 (the caller's bf16 weights as they are)
+  h->act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
   for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
   ensure_phase_events(h);
   cudaEventRecord(h->ph[0], st);
@@ -438,7 +448,7 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   const int M = B * Lp;
   {
     Timed t(h, HE_KCLASS_OTHER, st);
-    c.check(launch_embed_ln(cf.dtype, prompt, M, Lp, 0, h->tok_emb, h->pos_emb, cf.pos_offset,
+    c.check(launch_embed_ln(cf.dtype, h->act, prompt, M, Lp, 0, h->tok_emb, h->pos_emb, cf.pos_offset,
                             cf.vocab, h->layers[0].ln1_g, h->layers[0].ln1_b, cf.ln_eps,
                             static_cast<float *>(h->x.p), h->h.p, d,
                             static_cast<int *>(h->err.p), st),
@@ -636,7 +646,7 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
       if (bf) {
         // save the original bits, then write the merged weight tiled from the copy
         chk(launch_copy(save, lw.w[p], bytes, st), bytes % 16 ? 2 : 1);
-        chk(launch_fuse_tiled(lw.w[p], save, lora ? lw.lora_a[p] : nullptr,
+        chk(launch_fuse_tiled(lw.w[p], ACT_F16, save, lora ? lw.lora_a[p] : nullptr,
                               lora ? lw.lora_b[p] : nullptr, rows_of(p), cols_of(p), c.lora_r,
                               scale, st),
             1);
@@ -838,7 +848,8 @@ he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void
                             void *stream) {
   g_err.clear();
   if (!q || !kc || !vc || !ctx) return fail(HE_ERR_ARG, "NULL buffer");
-  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
+  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16 && dtype != HE_DTYPE_F16)
+    return fail(HE_ERR_ARG, "bad dtype");
   if (B < 1 || H < 1 || n_keys < 1 || n_keys > max_seq || split < 1 || split > n_keys)
     return fail(HE_ERR_ARG, "bad sizes");
   if (hd != 32 && hd != 64 && hd != 128) return fail(HE_ERR_UNSUPPORTED, "head_dim %d", hd);
@@ -855,7 +866,7 @@ he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream
   if (N < 128 || K < 64 || N % 128 || K % 64)
     return fail(HE_ERR_UNSUPPORTED, "tiled layout needs N %% 128 == 0 and K %% 64 == 0");
   if ((uintptr_t)w % 16 || (uintptr_t)out % 16) return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
-  cudaError_t r = launch_fuse_tiled(out, w, nullptr, nullptr, N, K, 0, 0.f,
+  cudaError_t r = launch_fuse_tiled(out, ACT_BF16, w, nullptr, nullptr, N, K, 0, 0.f,
                                     static_cast<cudaStream_t>(stream));
   if (r != cudaSuccess) return cuda_fail(r, "he_op_tile_weight");
   return HE_OK;
@@ -865,24 +876,26 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
                        int M, int N, int K, int split, float *scratch, void *stream) {
   g_err.clear();
   if (w_layout != 0 && w_layout != 1) return fail(HE_ERR_ARG, "w_layout must be 0 or 1");
-  if (w_layout == 1 && (dtype != HE_DTYPE_BF16 || N % 128 || K % 64))
-    return fail(HE_ERR_UNSUPPORTED, "tiled weights need bf16, N %% 128 == 0, K %% 64 == 0");
+  if (w_layout == 1 && (dtype == HE_DTYPE_F32 || N % 128 || K % 64))
+    return fail(HE_ERR_UNSUPPORTED, "tiled weights need a 16-bit type, N %% 128 == 0, K %% 64 == 0");
   if (!x || !w || !y) return fail(HE_ERR_ARG, "NULL buffer");
   if (M < 1 || N < 1 || K < 1 || ldx < K) return fail(HE_ERR_ARG, "bad sizes");
-  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16) return fail(HE_ERR_ARG, "bad dtype");
-  if (dtype == HE_DTYPE_BF16 && (K % 8 || ldx % 8))
-    return fail(HE_ERR_UNSUPPORTED, "bf16 needs K and ldx multiples of 8");
+  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16 && dtype != HE_DTYPE_F16)
+    return fail(HE_ERR_ARG, "bad dtype");
+  if (dtype != HE_DTYPE_F32 && (K % 8 || ldx % 8))
+    return fail(HE_ERR_UNSUPPORTED, "16-bit types need K and ldx multiples of 8");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (split <= 0) {
     // stream-K: the persistent kernel of the decode projections
-    if (dtype != HE_DTYPE_BF16 || M > 256 || K % 64 || (w_layout == 1 && N % 128))
-      return fail(HE_ERR_UNSUPPORTED, "stream-K needs bf16, M <= 256, K %% 64 == 0 (and N %% 128 == 0 for tiled weights)");
+    if (dtype == HE_DTYPE_F32 || M > 256 || K % 64 || (w_layout == 1 && N % 128))
+      return fail(HE_ERR_UNSUPPORTED, "stream-K needs a 16-bit type, M <= 256, K %% 64 == 0 (and N %% 128 == 0 for tiled weights)");
     if (!scratch) return fail(HE_ERR_ARG, "stream-K needs scratch");
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     GemmArgs a{};
-    a.dtype = dtype;
+    a.dtype = HE_DTYPE_BF16;
+    a.act = dtype;
     a.x = x;
     a.ldx = ldx;
     a.w[0] = w;
@@ -912,7 +925,7 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     const SliceInfo si{0, U, (int)(U / T), P};
     if (r == cudaSuccess) r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
     if (r == cudaSuccess)
-      r = launch_sk_reduce_epi(dtype, scratch, si, (long long)M * N, N, M, N, e, st);
+      r = launch_sk_reduce_epi(HE_DTYPE_BF16, dtype, scratch, si, (long long)M * N, N, M, N, e, st);
     if (r != cudaSuccess) return cuda_fail(r, "he_op_linear (stream-K)");
     return HE_OK;
   }
@@ -920,7 +933,8 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     return fail(HE_ERR_ARG, "split %d leaves an empty K slice (K=%d)", split, K);
   if (split > 1 && !scratch) return fail(HE_ERR_ARG, "split > 1 needs scratch");
   GemmArgs a{};
-  a.dtype = dtype;
+  a.dtype = dtype == HE_DTYPE_F32 ? HE_DTYPE_F32 : HE_DTYPE_BF16;
+  a.act = dtype;
   a.x = x;
   a.ldx = ldx;
   a.w[0] = w;
@@ -947,7 +961,8 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
   }
   cudaError_t r = launch_gemm(a, nullptr, st);
   if (r == cudaSuccess && split > 1)
-    r = launch_reduce_epi(dtype, scratch, split, (long long)M * N, N, M, N, e, st);
+    r = launch_reduce_epi(dtype == HE_DTYPE_F32 ? HE_DTYPE_F32 : HE_DTYPE_BF16, dtype, scratch, split,
+                          (long long)M * N, N, M, N, e, st);
   if (r != cudaSuccess) return cuda_fail(r, "he_op_linear");
   return HE_OK;
 }

@@ -64,14 +64,14 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int tok = tok0 + ty * 4 + i, n = n0 + tx * 4 + j;
-      if (tok < M && n < N) epi_store<T>(epi, split, tok, n, acc[i][j]);
+      if (tok < M && n < N) epi_store<T, T>(epi, split, tok, n, acc[i][j]);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st) {
-  if (a.dtype == 1) return launch_gemm_tc(a, dev_err, st);
+  if (a.act != ACT_F32) return launch_gemm_tc(a, dev_err, st);
   if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.n_groups < 1 || a.n_groups > 3)
     return cudaErrorInvalidValue;
   if (a.n_groups * a.group_rows != a.N) return cudaErrorInvalidValue;
@@ -91,7 +91,7 @@ cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st) {
 // rate, while the whole GEMM moves the weights plus the fp32 partial slices
 // (written and read back) at the HBM rate; the slower of the two is the time.
 int gemm_pick_split(const GemmArgs &a, int num_sms) {
-  const bool tc = a.dtype == 1;
+  const bool tc = a.act != ACT_F32;
   const int bm = tc ? 128 : TN;
   const int bn = tc ? (a.M <= 16 ? 16 : a.M <= 32 ? 32 : a.M <= 64 ? 64 : a.M <= 128 ? 128 : 256) : TT;
   const long long tiles = (long long)((a.N + bm - 1) / bm) * ((a.M + bn - 1) / bn);

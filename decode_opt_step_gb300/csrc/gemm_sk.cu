@@ -22,6 +22,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -30,7 +31,8 @@
 
 namespace he {
 
-bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows);
+bool make_tmap_16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows,
+                  bool fp16);
 
 namespace {
 
@@ -40,8 +42,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
          (2ull << 61);
 }
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+template <typename CT>
+__host__ __device__ constexpr uint32_t idesc_f16kind(int n) {
+  constexpr uint32_t fmt = std::is_same<CT, bf16>::value ? 1u : 0u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
 constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32u : c <= 64 ? 64u : c <= 128 ? 128u : c <= 256 ? 256u : 512u; }
@@ -60,7 +64,7 @@ struct SkCfg {
 };
 
 struct SkArgs {
-  const bf16 *wt[3];     // tiled weights per row group (tiled == 1)
+  const uint16_t *wt[3]; // tiled weights per row group (tiled == 1), 16-bit elements
   int tiled;
   int tiles_per_group;   // 128-row tiles per group (multiple groups only)
   int n_groups;
@@ -70,12 +74,12 @@ struct SkArgs {
   long long slice_stride;
 };
 
-template <int BN, int STAGES, int KPS>
+template <typename CT, int BN, int STAGES, int KPS>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
-              const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const bf16 *x, int ldx,
-              int *dev_err) {
+              const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const uint16_t *x,
+              int ldx, int *dev_err) {
   using C = SkCfg<BN, STAGES, KPS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(192, 1)
       if (*(volatile int *)abort_flag) break;
       mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
       if (a.tiled) {
-        const bf16 *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
+        const uint16_t *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
         bulk_load(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s]);
       } else {
         const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(192, 1)
         set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
   } else if (warp == 5 && lane == 0) {
     // ---------------- MMA ----------------
-    constexpr uint32_t idesc = idesc_bf16(BN);
+    constexpr uint32_t idesc = idesc_f16kind<CT>(BN);
     int seg = 0;
     bool ok = true;
     for (long long u = u_begin; u < u_end && ok;) {
@@ -215,13 +219,14 @@ __global__ void __launch_bounds__(192, 1)
       const int row = t * BM + warp * 32 + lane;
       const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
       constexpr int W = BN >= 32 ? 32 : 16;
-      const RowEpi re = row_epi_prepare(epi, row < a.N ? row : 0, direct ? nullptr : a.slices,
-                                        a.slice_stride, slot, a.N);
+      const RowEpi<CT> re = row_epi_prepare<CT>(epi, row < a.N ? row : 0,
+                                                direct ? nullptr : a.slices, a.slice_stride, slot,
+                                                a.N);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += W) {
         float v[W];
         tmem_load_cols<W>(tl + c0, v);
-        if (live && row < a.N && c0 < a.M) row_epi_store<W>(re, c0, min(W, a.M - c0), v);
+        if (live && row < a.N && c0 < a.M) row_epi_store<CT, W>(re, c0, min(W, a.M - c0), v);
       }
       tc_fence_before();
       __syncwarp();
@@ -238,10 +243,11 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int BN, int STAGES, int KPS>
+template <typename CT, int BN, int STAGES, int KPS>
 cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slice_stride,
                          int *dev_err, cudaStream_t st) {
   using C = SkCfg<BN, STAGES, KPS>;
+  constexpr bool fp16 = !std::is_same<CT, bf16>::value;
   CUtensorMap tw[3], tx;
   memset(tw, 0, sizeof tw);
   SkArgs a{};
@@ -251,8 +257,8 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   for (int i = 0; i < 3; ++i) {
     const void *p = g.w[i < g.n_groups ? i : 0];
     if (g.w_tiled)
-      a.wt[i] = static_cast<const bf16 *>(p);
-    else if (i < g.n_groups && !make_tmap_bf16(&tw[i], p, g.group_rows, g.K, g.K, BM))
+      a.wt[i] = static_cast<const uint16_t *>(p);
+    else if (i < g.n_groups && !make_tmap_16(&tw[i], p, g.group_rows, g.K, g.K, BM, fp16))
       return cudaErrorInvalidValue;
   }
   memset(&tx, 0, sizeof tx);  // activations arrive by bulk copy (row-tiled layout)
@@ -265,14 +271,13 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.slice_stride = slice_stride;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<BN, STAGES, KPS>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<CT, BN, STAGES, KPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_sk<BN, STAGES, KPS><<<P, 192, C::SMEM, st>>>(tw[0], tw[1], tw[2], tx, a, g.epi,
-                                                      static_cast<const bf16 *>(g.x), g.ldx,
-                                                      dev_err);
+  k_gemm_sk<CT, BN, STAGES, KPS><<<P, 192, C::SMEM, st>>>(
+      tw[0], tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
   return cudaGetLastError();
 }
 
@@ -299,24 +304,30 @@ int sk_ctas(const GemmArgs &g, int num_sms) {
 cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long slice_stride,
                            int *dev_err, cudaStream_t st) {
   // One row tile of tokens (M <= 256), whole 128 x 64 tiles, fp32 slices in epi.partial.
-  if (g.dtype != 1 || g.M < 1 || g.M > 256 || g.K % BK) return cudaErrorInvalidValue;
+  if ((g.act != ACT_BF16 && g.act != ACT_F16) || g.M < 1 || g.M > 256 || g.K % BK)
+    return cudaErrorInvalidValue;
   if (g.w_tiled && (g.group_rows % BM)) return cudaErrorInvalidValue;
   if (g.n_groups < 1 || g.n_groups > 3 || g.n_groups * g.group_rows != g.N) return cudaErrorInvalidValue;
   if (g.epi.kind == EPI_QKV && g.epi.d_model % BM) return cudaErrorInvalidValue;
   if (!slices || P < 1 || slice_stride < (long long)g.M * g.N) return cudaErrorInvalidValue;
-  if (sk_kps(g) == 2) {
-    // two k-blocks per stage: 32 KB weight requests
-    if (g.M <= 16) return launch_sk_bn<16, 5, 2>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 32) return launch_sk_bn<32, 5, 2>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 64) return launch_sk_bn<64, 4, 2>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 128) return launch_sk_bn<128, 3, 2>(g, P, slices, slice_stride, dev_err, st);
-    return launch_sk_bn<256, 2, 2>(g, P, slices, slice_stride, dev_err, st);
-  }
-  if (g.M <= 16) return launch_sk_bn<16, 10, 1>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 32) return launch_sk_bn<32, 9, 1>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 64) return launch_sk_bn<64, 8, 1>(g, P, slices, slice_stride, dev_err, st);
-  if (g.M <= 128) return launch_sk_bn<128, 6, 1>(g, P, slices, slice_stride, dev_err, st);
-  return launch_sk_bn<256, 4, 1>(g, P, slices, slice_stride, dev_err, st);
+  auto pick = [&](auto ct) -> cudaError_t {
+    using CT = decltype(ct);
+    if (sk_kps(g) == 2) {
+      // two k-blocks per stage: 32 KB weight requests
+      if (g.M <= 16) return launch_sk_bn<CT, 16, 5, 2>(g, P, slices, slice_stride, dev_err, st);
+      if (g.M <= 32) return launch_sk_bn<CT, 32, 5, 2>(g, P, slices, slice_stride, dev_err, st);
+      if (g.M <= 64) return launch_sk_bn<CT, 64, 4, 2>(g, P, slices, slice_stride, dev_err, st);
+      if (g.M <= 128) return launch_sk_bn<CT, 128, 3, 2>(g, P, slices, slice_stride, dev_err, st);
+      return launch_sk_bn<CT, 256, 2, 2>(g, P, slices, slice_stride, dev_err, st);
+    }
+    if (g.M <= 16) return launch_sk_bn<CT, 16, 10, 1>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 32) return launch_sk_bn<CT, 32, 9, 1>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 64) return launch_sk_bn<CT, 64, 8, 1>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 128) return launch_sk_bn<CT, 128, 6, 1>(g, P, slices, slice_stride, dev_err, st);
+    return launch_sk_bn<CT, 256, 4, 1>(g, P, slices, slice_stride, dev_err, st);
+  };
+  if (g.act == ACT_BF16) return pick(bf16{});
+  return pick(f16{});
 }
 
 }  // namespace he

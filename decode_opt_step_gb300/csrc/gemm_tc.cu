@@ -17,6 +17,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -40,9 +41,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
          (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor, kind::f16: D fp32, A and B both bf16 (format 1) or both
+// fp16 (format 0), both K-major, M = 128.
+template <typename CT>
+__host__ __device__ constexpr uint32_t idesc_f16kind(int n) {
+  constexpr uint32_t fmt = std::is_same<CT, bf16>::value ? 1u : 0u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -57,11 +61,11 @@ struct Cfg {
 };
 
 struct WTiles {
-  const bf16 *p[3];  // tiled weights of each row group (ABULK)
-  int kt;            // 64-wide k tiles per 128-row tile row
+  const uint16_t *p[3];  // tiled weights of each row group (ABULK), 16-bit elements
+  int kt;                // 64-wide k tiles per 128-row tile row
 };
 
-template <int BN, int STAGES, bool ABULK>
+template <typename CT, int BN, int STAGES, bool ABULK>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
@@ -110,8 +114,8 @@ __global__ void __launch_bounds__(192, 1)
     if (!ABULK) prefetch_tmap(tw);
     prefetch_tmap(&tm_x);
     // tiled weights: this CTA's k-blocks of tile row `m_row / BM` are contiguous
-    const bf16 *wtile = ABULK ? wt.p[group] + ((long long)(m_row / BM) * wt.kt + kb0) * (BM * BK)
-                              : nullptr;
+    const uint16_t *wtile =
+        ABULK ? wt.p[group] + ((long long)(m_row / BM) * wt.kt + kb0) * (BM * BK) : nullptr;
     int issued = 0;
     for (int i = 0; i < nkb; ++i) {
       const int s = i % STAGES;
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(192, 1)
         set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
   } else if (warp == 5 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = idesc_bf16(BN);
+    constexpr uint32_t idesc = idesc_f16kind<CT>(BN);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % STAGES;
       if (!mbar_wait_bounded(&full[s], (i / STAGES) & 1)) {
@@ -165,15 +169,15 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16);
     constexpr int W = BN >= 32 ? 32 : 16;
     const bool part = epi.kind == EPI_PARTIAL;
-    const RowEpi re = row_epi_prepare(epi, row < N ? row : 0, part ? epi.partial : nullptr,
-                                      epi.split_stride, split, epi.ldp);
+    const RowEpi<CT> re = row_epi_prepare<CT>(epi, row < N ? row : 0, part ? epi.partial : nullptr,
+                                              epi.split_stride, split, epi.ldp);
     const int tok_base = n_tile * BN;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += W) {
       float v[W];
       tmem_load_cols<W>(tl + c0, v);
       if (live && row < N && tok_base + c0 < M)
-        row_epi_store<W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
+        row_epi_store<CT, W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
     }
   }
   tc_fence_before();
@@ -202,20 +206,27 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2-D bf16 map over a [rows][cols] matrix with row stride `ld` elements, box
 // {64 (K), box_rows}, 128-byte swizzle, zero fill out of bounds.
-bool make_tmap(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows) {
+bool make_tmap(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+  CUresult r = enc(m, dt, 2, const_cast<void *>(ptr), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool ABULK>
+template <typename CT>
+constexpr CUtensorMapDataType tmap_type() {
+  return std::is_same<CT, bf16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+template <typename CT, int BN, int STAGES, bool ABULK>
 cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   using C = Cfg<BN, STAGES>;
   CUtensorMap tw[3], tx;
@@ -224,15 +235,15 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   for (int g = 0; g < 3; ++g) {
     const void *p = a.w[g < a.n_groups ? g : 0];
     if (ABULK)
-      wt.p[g] = static_cast<const bf16 *>(p);
-    else if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM))
+      wt.p[g] = static_cast<const uint16_t *>(p);
+    else if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM, tmap_type<CT>()))
       return cudaErrorInvalidValue;
   }
   wt.kt = a.K / BK;
-  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN, tmap_type<CT>())) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, ABULK>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<CT, BN, STAGES, ABULK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -242,7 +253,7 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   if (effective_split(a.K, a.split) != a.split) return cudaErrorInvalidValue;
   const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
   dim3 grid(a.N / BM + (a.N % BM != 0), (a.M + BN - 1) / BN, a.split);
-  k_gemm_tc<BN, STAGES, ABULK><<<grid, 192, C::SMEM, st>>>(
+  k_gemm_tc<CT, BN, STAGES, ABULK><<<grid, 192, C::SMEM, st>>>(
       tw[0], tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total, kb_per_split, a.epi, wt,
       dev_err);
   return cudaGetLastError();
@@ -250,8 +261,10 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
 
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows) {
-  return make_tmap(m, ptr, rows, cols, ld, box_rows);
+bool make_tmap_16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows,
+                  bool fp16) {
+  return make_tmap(m, ptr, rows, cols, ld, box_rows,
+                   fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
@@ -269,17 +282,25 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
     if (a.group_rows % BM || a.K % BK) return cudaErrorInvalidValue;
     for (int g = 0; g < a.n_groups; ++g)
       if ((uintptr_t)a.w[g] % 16) return cudaErrorInvalidValue;
-    if (a.M <= 16) return launch_bn<16, 10, true>(a, dev_err, st);
-    if (a.M <= 32) return launch_bn<32, 9, true>(a, dev_err, st);
-    if (a.M <= 64) return launch_bn<64, 8, true>(a, dev_err, st);
-    if (a.M <= 128) return launch_bn<128, 6, true>(a, dev_err, st);
-    return launch_bn<256, 4, true>(a, dev_err, st);
   }
-  if (a.M <= 16) return launch_bn<16, 10, false>(a, dev_err, st);
-  if (a.M <= 32) return launch_bn<32, 9, false>(a, dev_err, st);
-  if (a.M <= 64) return launch_bn<64, 8, false>(a, dev_err, st);
-  if (a.M <= 128) return launch_bn<128, 6, false>(a, dev_err, st);
-  return launch_bn<256, 4, false>(a, dev_err, st);
+  auto pick = [&](auto ct) -> cudaError_t {
+    using CT = decltype(ct);
+    if (a.w_tiled) {
+      if (a.M <= 16) return launch_bn<CT, 16, 10, true>(a, dev_err, st);
+      if (a.M <= 32) return launch_bn<CT, 32, 9, true>(a, dev_err, st);
+      if (a.M <= 64) return launch_bn<CT, 64, 8, true>(a, dev_err, st);
+      if (a.M <= 128) return launch_bn<CT, 128, 6, true>(a, dev_err, st);
+      return launch_bn<CT, 256, 4, true>(a, dev_err, st);
+    }
+    if (a.M <= 16) return launch_bn<CT, 16, 10, false>(a, dev_err, st);
+    if (a.M <= 32) return launch_bn<CT, 32, 9, false>(a, dev_err, st);
+    if (a.M <= 64) return launch_bn<CT, 64, 8, false>(a, dev_err, st);
+    if (a.M <= 128) return launch_bn<CT, 128, 6, false>(a, dev_err, st);
+    return launch_bn<CT, 256, 4, false>(a, dev_err, st);
+  };
+  if (a.act == ACT_BF16) return pick(bf16{});
+  if (a.act == ACT_F16) return pick(f16{});
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace he

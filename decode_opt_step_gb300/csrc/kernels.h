@@ -8,6 +8,30 @@
 
 namespace he {
 
+// Activation / operand types (values 0 and 1 double as the parameter dtype).
+enum ActType : int { ACT_F32 = 0, ACT_BF16 = 1, ACT_F16 = 2 };
+
+// Host dispatch over the (parameter type PT, activation type CT) pairs the
+// library runs: (float, float), (bf16, bf16) and (bf16, fp16).
+#define HE_DISPATCH_PT_CT(pt, ct, ...)                        \
+  do {                                                        \
+    if ((pt) == 0 && (ct) == ACT_F32) {                       \
+      using PT = float;                                       \
+      using CT = float;                                       \
+      __VA_ARGS__                                             \
+    } else if ((pt) == 1 && (ct) == ACT_BF16) {               \
+      using PT = __nv_bfloat16;                               \
+      using CT = __nv_bfloat16;                               \
+      __VA_ARGS__                                             \
+    } else if ((pt) == 1 && (ct) == ACT_F16) {                \
+      using PT = __nv_bfloat16;                               \
+      using CT = __half;                                      \
+      __VA_ARGS__                                             \
+    } else {                                                  \
+      return cudaErrorInvalidValue;                           \
+    }                                                         \
+  } while (0)
+
 // Error flags written by kernels (the host reads them in he_check).
 enum : int {
   DEVERR_BAD_TOKEN = 1,    // a token id outside [0, vocab) was replaced by 0
@@ -61,7 +85,8 @@ __host__ __device__ inline long long act_index(int r, int k, int K, int R) {
 inline int sk_token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
 struct GemmArgs {
-  int dtype;             // HE_DTYPE_F32 / HE_DTYPE_BF16
+  int dtype;             // parameter type (bias reads): HE_DTYPE_F32 / HE_DTYPE_BF16
+  int act;               // operand type of W and X and of the epilogue outputs (ActType)
   const void *x;         // [M][ldx] activations (tokens x K), storage type
   int ldx;
   const void *w[3];      // up to three row groups of `group_rows` rows, each [rows][K]
@@ -131,27 +156,29 @@ cudaError_t launch_gemm_sk(const GemmArgs &a, int P, float *slices, long long sl
                            int *dev_err, cudaStream_t st);
 int gemm_pick_split(const GemmArgs &a, int num_sms);  // heuristic for decode shapes
 
-cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long long split_stride,
-                              int ldp, int M, int N, const Epi &epi, cudaStream_t st);
+cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int split,
+                              long long split_stride, int ldp, int M, int N, const Epi &epi,
+                              cudaStream_t st);
 // Element-wise epilogue over stream-K slices (tiles with one slice were stored already).
-cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInfo &si,
+cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const SliceInfo &si,
                                  long long split_stride, int ldp, int M, int N, const Epi &epi,
                                  cudaStream_t st);
 
 // x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type,
 // row-tiled with h_rows rows when h_rows > 0).
-cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
+cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
                             const void *g, const void *b, float eps, void *h, int h_rows,
                             int rows, int d, cudaStream_t st);
-// out (row-tiled, R rows) <- x rows 0..M-1 (row stride ldx), rows M..R-1 zero.  bf16.
+// out (row-tiled, R rows) <- x rows 0..M-1 (row stride ldx), rows M..R-1 zero.
+// 16-bit elements (bf16 or fp16 bits).
 cudaError_t launch_tile_act(const void *x, int M, int K, int ldx, int R, void *out,
                             cudaStream_t st);
 cudaError_t launch_zero(void *p, size_t bytes, cudaStream_t st);
 
 // x[tok] = E[id] + P[pos + off]; h[tok] = LN(x[tok]).  Token tok of a launch is
 // sequence tok / tok_per_seq at position pos0 + tok % tok_per_seq.
-cudaError_t launch_embed_ln(int dtype, const int32_t *ids, int n_tok, int tok_per_seq, int pos0,
+cudaError_t launch_embed_ln(int dtype, int act, const int32_t *ids, int n_tok, int tok_per_seq, int pos0,
                             const void *tok_emb, const void *pos_emb, int pos_offset, int vocab,
                             const void *g, const void *b, float eps, float *x, void *h, int d,
                             int *dev_err, cudaStream_t st);
@@ -169,28 +196,31 @@ struct HeadArgs {
   float *x; void *h; int d;
   int h_rows;                        // h row-tiled with this R (0 = row-major)
 };
-cudaError_t launch_head_select(int dtype, const HeadArgs &a, cudaStream_t st);
+// h is written in `act`.
+cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st);
 
 // Decode attention: one query per (b, h) over keys 0..n_keys-1 of the cache.
 // part: scratch of B*H*split*(hd+2) floats when split > 1.
-// ctx is row-tiled with ctx_rows rows when ctx_rows > 0.
-cudaError_t launch_attn_decode(int dtype, const void *q, const void *kc, const void *vc,
+// act: type of q, K/V and ctx.  ctx is row-tiled with ctx_rows rows when ctx_rows > 0.
+cudaError_t launch_attn_decode(int act, const void *q, const void *kc, const void *vc,
                                void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
                                int n_keys, int split, float *part, cudaStream_t st);
 int attn_decode_pick_split(int B, int H, int n_keys, int num_sms);
 
 // Prefill attention: causal within each prompt of Lp tokens (positions 0..Lp-1).
-cudaError_t launch_attn_prefill(int dtype, const void *q, const void *kc, const void *vc,
+cudaError_t launch_attn_prefill(int act, const void *q, const void *kc, const void *vc,
                                 void *ctx, int B, int Lp, int H, int hd, int max_seq,
                                 cudaStream_t st);
 
 // W <- round(W + scale * B A) after saving W's bits to `save`.
 cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,
                              int rows, int cols, int r, float scale, cudaStream_t st);
-// bf16: out (tiled layout) <- round(src + scale * B A), src row-major [rows][cols];
-// A / B may be null (then a plain re-tiling).  out and src must not overlap.
-cudaError_t launch_fuse_tiled(void *out, const void *src, const void *a, const void *bm, int rows,
-                              int cols, int r, float scale, cudaStream_t st);
+// out (tiled layout, type out_act: ACT_BF16 or ACT_F16) <- round(src + scale * B A),
+// src, A, B bf16, src row-major [rows][cols]; A / B may be null (then a plain
+// re-tiling, bit-exact for ACT_BF16).  out and src must not overlap.
+cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const void *a,
+                              const void *bm, int rows, int cols, int r, float scale,
+                              cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 
 }  // namespace he

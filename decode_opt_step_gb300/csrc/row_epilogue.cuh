@@ -1,4 +1,4 @@
-// Row-wise GEMM epilogue for the tensor-core kernels.
+// Row-wise GEMM epilogue for the tensor-core kernels (bias bf16, outputs CT).
 //
 // In the tcgen05 kernels a thread owns one output feature n (a TMEM lane) and a
 // run of consecutive tokens (TMEM columns).  Everything that depends only on n
@@ -11,12 +11,13 @@
 
 namespace he {
 
+template <typename CT>
 struct RowEpi {
   int mode;          // 0 fp32 store (partial / logits / slices), 1 q, 2 k or v cache, 3 relu
   float bias, scale;
   float *f32;        // mode 0: element of token 0; token stride f32_stride
   long long f32_stride;
-  bf16 *dst;         // modes 1-3
+  CT *dst;           // modes 1-3
   long long tok_stride;  // modes 1, 2 (per sequence for 2)
   long long pos_stride;  // mode 2: per position inside a sequence
   int n, ldo, out_rows;  // mode 3 (row-tiled output when out_rows > 0)
@@ -25,9 +26,10 @@ struct RowEpi {
 
 // Constants of output row n for tokens starting at `tok0`.  slices != null means
 // "write fp32 slice `slot`" instead of the epilogue of `e`.
-__device__ __forceinline__ RowEpi row_epi_prepare(const Epi &e, int n, float *slices,
-                                                  long long slice_stride, int slot, int ldn) {
-  RowEpi r{};
+template <typename CT>
+__device__ __forceinline__ RowEpi<CT> row_epi_prepare(const Epi &e, int n, float *slices,
+                                                      long long slice_stride, int slot, int ldn) {
+  RowEpi<CT> r{};
   r.n = n;
   if (slices) {
     r.mode = 0;
@@ -49,7 +51,7 @@ __device__ __forceinline__ RowEpi row_epi_prepare(const Epi &e, int n, float *sl
     case EPI_RELU:
       r.mode = 3;
       r.bias = __bfloat162float(static_cast<const bf16 *>(e.bias[0])[n]);
-      r.dst = static_cast<bf16 *>(e.out);
+      r.dst = static_cast<CT *>(e.out);
       r.ldo = e.ldo;
       r.out_rows = e.out_rows;
       break;
@@ -60,12 +62,12 @@ __device__ __forceinline__ RowEpi row_epi_prepare(const Epi &e, int n, float *sl
       if (which == 0) {
         r.mode = 1;
         r.scale = e.q_scale;
-        r.dst = static_cast<bf16 *>(e.out) + c;
+        r.dst = static_cast<CT *>(e.out) + c;
         r.tok_stride = e.ldo;
       } else {
         r.mode = 2;
         const int hh = c / e.head_dim, dd = c - hh * e.head_dim;
-        r.dst = static_cast<bf16 *>(which == 1 ? e.kc : e.vc) +
+        r.dst = static_cast<CT *>(which == 1 ? e.kc : e.vc) +
                 ((long long)hh * e.max_seq + e.pos0) * e.head_dim + dd;
         r.tok_stride = (long long)e.n_heads * e.max_seq * e.head_dim;  // next sequence
         r.pos_stride = e.head_dim;                                      // next position
@@ -78,8 +80,8 @@ __device__ __forceinline__ RowEpi row_epi_prepare(const Epi &e, int n, float *sl
 }
 
 // Stores v[0..cnt) for tokens tok0 .. tok0 + cnt - 1 (all < M).
-template <int CNT>
-__device__ __forceinline__ void row_epi_store(const RowEpi &r, int tok0, int cnt,
+template <typename CT, int CNT>
+__device__ __forceinline__ void row_epi_store(const RowEpi<CT> &r, int tok0, int cnt,
                                               const float (&v)[CNT]) {
   switch (r.mode) {
     case 0: {
@@ -90,10 +92,10 @@ __device__ __forceinline__ void row_epi_store(const RowEpi &r, int tok0, int cnt
       break;
     }
     case 1: {
-      bf16 *p = r.dst + (long long)tok0 * r.tok_stride;
+      CT *p = r.dst + (long long)tok0 * r.tok_stride;
 #pragma unroll
       for (int j = 0; j < CNT; ++j)
-        if (j < cnt) p[(long long)j * r.tok_stride] = __float2bfloat16_rn((v[j] + r.bias) * r.scale);
+        if (j < cnt) p[(long long)j * r.tok_stride] = from_f<CT>((v[j] + r.bias) * r.scale);
       break;
     }
     case 2: {
@@ -102,7 +104,7 @@ __device__ __forceinline__ void row_epi_store(const RowEpi &r, int tok0, int cnt
       for (int j = 0; j < CNT; ++j) {
         if (j < cnt)
           r.dst[(long long)b * r.tok_stride + (long long)t * r.pos_stride] =
-              __float2bfloat16_rn(v[j] + r.bias);
+              from_f<CT>(v[j] + r.bias);
         if (++t == r.tok_per_seq) {
           t = 0;
           ++b;
@@ -115,7 +117,7 @@ __device__ __forceinline__ void row_epi_store(const RowEpi &r, int tok0, int cnt
       for (int j = 0; j < CNT; ++j)
         if (j < cnt)
           r.dst[act_index(tok0 + j, r.n, r.ldo, r.out_rows)] =
-              __float2bfloat16_rn(fmaxf(v[j] + r.bias, 0.f));
+              from_f<CT>(fmaxf(v[j] + r.bias, 0.f));
       break;
     }
   }

@@ -2,6 +2,8 @@
 // with bias + residual + LayerNorm, the element-wise split-K epilogue, the
 // greedy head (argmax, log-softmax, next-token embedding), the LoRA fuse and the
 // restore copy.
+#include <type_traits>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -12,8 +14,8 @@ namespace {
 
 // LayerNorm of the fp32 row held in shared memory `row[0..d)`: two passes
 // (mean, then the biased variance of the centred values), eps inside the root.
-template <typename T>
-__device__ void ln_store(const float *row, int d, const T *g, const T *b, float eps, T *h, int r,
+template <typename PT, typename OT>
+__device__ void ln_store(const float *row, int d, const PT *g, const PT *b, float eps, OT *h, int r,
                          int R, float *red) {
   float s = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) s += row[i];
@@ -26,26 +28,26 @@ __device__ void ln_store(const float *row, int d, const T *g, const T *b, float 
   const float var = block_sum(v, red) / (float)d;
   const float rstd = 1.0f / sqrtf(var + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x)
-    h[act_index(r, i, d, R)] = from_f<T>((row[i] - mean) * rstd * to_f<T>(g[i]) + to_f<T>(b[i]));
+    h[act_index(r, i, d, R)] = from_f<OT>((row[i] - mean) * rstd * to_f<PT>(g[i]) + to_f<PT>(b[i]));
 }
 
-template <typename T>
-__device__ void embed_row(int id, int pos, const T *tok_emb, const T *pos_emb, int d, float *row,
+template <typename PT>
+__device__ void embed_row(int id, int pos, const PT *tok_emb, const PT *pos_emb, int d, float *row,
                           float *xout) {
-  const T *e = tok_emb + (long long)id * d;
-  const T *p = pos_emb + (long long)pos * d;
+  const PT *e = tok_emb + (long long)id * d;
+  const PT *p = pos_emb + (long long)pos * d;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = to_f<T>(e[i]) + to_f<T>(p[i]);
+    const float v = to_f<PT>(e[i]) + to_f<PT>(p[i]);
     row[i] = v;
     xout[i] = v;
   }
   __syncthreads();
 }
 
-template <typename T>
-__global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const T *tok_emb,
-                           const T *pos_emb, int pos_offset, int vocab, const T *g, const T *b,
-                           float eps, float *x, T *h, int d, int *dev_err) {
+template <typename PT, typename CT>
+__global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const PT *tok_emb,
+                           const PT *pos_emb, int pos_offset, int vocab, const PT *g, const PT *b,
+                           float eps, float *x, CT *h, int d, int *dev_err) {
   extern __shared__ float row[];
   __shared__ float red[33];
   const int tok = blockIdx.x;
@@ -55,8 +57,8 @@ __global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const 
     id = 0;
   }
   const int pos = pos0 + tok % tok_per_seq + pos_offset;
-  embed_row<T>(id, pos, tok_emb, pos_emb, d, row, x + (long long)tok * d);
-  ln_store<T>(row, d, g, b, eps, h, tok, 0, red);
+  embed_row<PT>(id, pos, tok_emb, pos_emb, d, row, x + (long long)tok * d);
+  ln_store<PT, CT>(row, d, g, b, eps, h, tok, 0, red);
 }
 
 // Sum of the split slices of one float4 of a row, in slice order (loads of four
@@ -87,10 +89,10 @@ __device__ __forceinline__ float4 sum_slices(const float *p, int split, long lon
 }
 
 // One block per row (d % 4 == 0, ldp % 4 == 0): x += sum of slices + bias, then LN.
-template <typename T>
+template <typename PT, typename OT>
 __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long split_stride,
-                           int ldp, const T *bias, float *x, const T *g, const T *b, float eps,
-                           T *h, int h_rows, int d) {
+                           int ldp, const PT *bias, float *x, const PT *g, const PT *b, float eps,
+                           OT *h, int h_rows, int d) {
   extern __shared__ float row[];
   __shared__ float red[33];
   const long long r = blockIdx.x;
@@ -99,19 +101,19 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
   for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
     const float4 acc = sum_slices(pr + 4 * i, si.slices(4 * i), split_stride);
     float4 v = xr[i];
-    v.x += acc.x + to_f<T>(bias[4 * i]);
-    v.y += acc.y + to_f<T>(bias[4 * i + 1]);
-    v.z += acc.z + to_f<T>(bias[4 * i + 2]);
-    v.w += acc.w + to_f<T>(bias[4 * i + 3]);
+    v.x += acc.x + to_f<PT>(bias[4 * i]);
+    v.y += acc.y + to_f<PT>(bias[4 * i + 1]);
+    v.z += acc.z + to_f<PT>(bias[4 * i + 2]);
+    v.w += acc.w + to_f<PT>(bias[4 * i + 3]);
     xr[i] = v;
     reinterpret_cast<float4 *>(row)[i] = v;
   }
   __syncthreads();
-  ln_store<T>(row, d, g, b, eps, h, (int)r, h_rows, red);
+  ln_store<PT, OT>(row, d, g, b, eps, h, (int)r, h_rows, red);
 }
 
 // Element-wise epilogue after a split-K GEMM: four consecutive outputs per thread.
-template <typename T>
+template <typename PT, typename CT>
 __global__ void k_reduce_epi4(const float *partial, int split, long long split_stride, int ldp,
                               int M, int N, const __grid_constant__ Epi epi) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -119,14 +121,14 @@ __global__ void k_reduce_epi4(const float *partial, int split, long long split_s
   if (e >= (long long)M * n4) return;
   const int tok = (int)(e / n4), n = (int)(e % n4) * 4;
   const float4 acc = sum_slices(partial + (long long)tok * ldp + n, split, split_stride);
-  epi_store<T>(epi, 0, tok, n, acc.x);
-  epi_store<T>(epi, 0, tok, n + 1, acc.y);
-  epi_store<T>(epi, 0, tok, n + 2, acc.z);
-  epi_store<T>(epi, 0, tok, n + 3, acc.w);
+  epi_store<PT, CT>(epi, 0, tok, n, acc.x);
+  epi_store<PT, CT>(epi, 0, tok, n + 1, acc.y);
+  epi_store<PT, CT>(epi, 0, tok, n + 2, acc.z);
+  epi_store<PT, CT>(epi, 0, tok, n + 3, acc.w);
 }
 
 // Stream-K slices: tiles with a single slice were stored by the GEMM itself.
-template <typename T>
+template <typename PT, typename CT>
 __global__ void k_sk_reduce_epi4(const float *partial, const SliceInfo si, long long split_stride,
                                  int ldp, int M, int N, const __grid_constant__ Epi epi) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -136,13 +138,13 @@ __global__ void k_sk_reduce_epi4(const float *partial, const SliceInfo si, long 
   const int S = si.slices(n);
   if (S == 1) return;
   const float4 acc = sum_slices(partial + (long long)tok * ldp + n, S, split_stride);
-  epi_store<T>(epi, 0, tok, n, acc.x);
-  epi_store<T>(epi, 0, tok, n + 1, acc.y);
-  epi_store<T>(epi, 0, tok, n + 2, acc.z);
-  epi_store<T>(epi, 0, tok, n + 3, acc.w);
+  epi_store<PT, CT>(epi, 0, tok, n, acc.x);
+  epi_store<PT, CT>(epi, 0, tok, n + 1, acc.y);
+  epi_store<PT, CT>(epi, 0, tok, n + 2, acc.z);
+  epi_store<PT, CT>(epi, 0, tok, n + 3, acc.w);
 }
 
-template <typename T>
+template <typename PT, typename CT>
 __global__ void k_reduce_epi(const float *partial, int split, long long split_stride, int ldp,
                              int M, int N, const __grid_constant__ Epi epi) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -150,13 +152,13 @@ __global__ void k_reduce_epi(const float *partial, int split, long long split_st
   const int tok = (int)(e / N), n = (int)(e % N);
   float acc = 0.f;
   for (int s = 0; s < split; ++s) acc += partial[s * split_stride + (long long)tok * ldp + n];
-  epi_store<T>(epi, 0, tok, n, acc);
+  epi_store<PT, CT>(epi, 0, tok, n, acc);
 }
 
 // One block per sequence: greedy choice (lowest index among equal maxima),
 // log-prob of the emitted token, optional logit capture, then the embedding of
 // the emitted token at the next position followed by the first layer's LN1.
-template <typename T>
+template <typename PT, typename CT>
 __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   extern __shared__ float row[];
   __shared__ float red[33];
@@ -230,10 +232,10 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   }
   __syncthreads();
   if (a.embed_next) {
-    embed_row<T>(s_tok, a.pos + a.pos_offset, static_cast<const T *>(a.tok_emb),
-                 static_cast<const T *>(a.pos_emb), a.d, row, a.x + (long long)b * a.d);
-    ln_store<T>(row, a.d, static_cast<const T *>(a.g), static_cast<const T *>(a.b), a.eps,
-                static_cast<T *>(a.h), b, a.h_rows, red);
+    embed_row<PT>(s_tok, a.pos + a.pos_offset, static_cast<const PT *>(a.tok_emb),
+                  static_cast<const PT *>(a.pos_emb), a.d, row, a.x + (long long)b * a.d);
+    ln_store<PT, CT>(row, a.d, static_cast<const PT *>(a.g), static_cast<const PT *>(a.b), a.eps,
+                     static_cast<CT *>(a.h), b, a.h_rows, red);
   }
 }
 
@@ -266,6 +268,7 @@ __global__ void k_lora_fuse(T *w, const T *A, const T *Bm, T *save, int rows, in
 
 // One 16-byte chunk of the tiled output per thread: chunk q of tile t holds row
 // r = (q % 1024) / 8, logical 16-byte column chunk (q % 8) ^ (r % 8).
+template <typename OT>
 __global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows,
                              int cols, int r, float scale) {
   const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -278,12 +281,15 @@ __global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const b
   const int n = (int)(t / KT) * 128 + rr;
   const int k0 = (int)(t % KT) * 64 + c * 8;
   const uint4 raw = *reinterpret_cast<const uint4 *>(src + (long long)n * cols + k0);
-  if (!A) {
-    out[q] = raw;
-    return;
-  }
   const bf16 *wv = reinterpret_cast<const bf16 *>(&raw);
   float delta[8] = {};
+  if (!A) {
+    if constexpr (sizeof(OT) == 2 && std::is_same<OT, bf16>::value) {
+      out[q] = raw;  // plain re-tiling keeps the bits
+      return;
+    }
+    r = 0;
+  }
   for (int j = 0; j < r; ++j) {
     const float bj = __bfloat162float(Bm[(long long)n * r + j]);
     const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
@@ -292,17 +298,17 @@ __global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const b
     for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
   }
   uint4 res;
-  bf16 *rp = reinterpret_cast<bf16 *>(&res);
+  OT *rp = reinterpret_cast<OT *>(&res);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) rp[e] = __float2bfloat16_rn(__bfloat162float(wv[e]) + scale * delta[e]);
+  for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(__bfloat162float(wv[e]) + scale * delta[e]);
   out[q] = res;
 }
 
-__global__ void k_tile_act(const bf16 *x, int M, int K, int ldx, int R, bf16 *out) {
+__global__ void k_tile_act(const uint16_t *x, int M, int K, int ldx, int R, uint16_t *out) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= (long long)R * K) return;
   const int r = (int)(e / K), k = (int)(e % K);
-  out[act_index(r, k, K, R)] = r < M ? x[(long long)r * ldx + k] : __float2bfloat16_rn(0.f);
+  out[act_index(r, k, K, R)] = r < M ? x[(long long)r * ldx + k] : (uint16_t)0;
 }
 
 __global__ void k_zero16(uint4 *p, long long n16) {
@@ -326,38 +332,34 @@ int row_threads(int d) { return d >= 2048 ? 512 : (d >= 512 ? 256 : 128); }
 
 }  // namespace
 
-cudaError_t launch_embed_ln(int dtype, const int32_t *ids, int n_tok, int tok_per_seq, int pos0,
-                            const void *tok_emb, const void *pos_emb, int pos_offset, int vocab,
-                            const void *g, const void *b, float eps, float *x, void *h, int d,
-                            int *dev_err, cudaStream_t st) {
+cudaError_t launch_embed_ln(int dtype, int act, const int32_t *ids, int n_tok, int tok_per_seq,
+                            int pos0, const void *tok_emb, const void *pos_emb, int pos_offset,
+                            int vocab, const void *g, const void *b, float eps, float *x, void *h,
+                            int d, int *dev_err, cudaStream_t st) {
   if (n_tok <= 0) return cudaSuccess;
   const size_t sm = (size_t)d * sizeof(float);
-  if (dtype == 1)
-    k_embed_ln<bf16><<<n_tok, row_threads(d), sm, st>>>(
-        ids, tok_per_seq, pos0, (const bf16 *)tok_emb, (const bf16 *)pos_emb, pos_offset, vocab,
-        (const bf16 *)g, (const bf16 *)b, eps, x, (bf16 *)h, d, dev_err);
-  else
-    k_embed_ln<float><<<n_tok, row_threads(d), sm, st>>>(
-        ids, tok_per_seq, pos0, (const float *)tok_emb, (const float *)pos_emb, pos_offset, vocab,
-        (const float *)g, (const float *)b, eps, x, (float *)h, d, dev_err);
+  HE_DISPATCH_PT_CT(dtype, act, {
+    k_embed_ln<PT, CT><<<n_tok, row_threads(d), sm, st>>>(
+        ids, tok_per_seq, pos0, (const PT *)tok_emb, (const PT *)pos_emb, pos_offset, vocab,
+        (const PT *)g, (const PT *)b, eps, x, (CT *)h, d, dev_err);
+  });
   return cudaGetLastError();
 }
 
-cudaError_t launch_sk_reduce_epi(int dtype, const float *partial, const SliceInfo &si,
+cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const SliceInfo &si,
                                  long long split_stride, int ldp, int M, int N, const Epi &epi,
                                  cudaStream_t st) {
   if (N % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16) return cudaErrorInvalidValue;
   const long long work = (long long)M * N / 4;
   if (work <= 0) return cudaSuccess;
   const int blocks = (int)((work + 255) / 256);
-  if (dtype == 1)
-    k_sk_reduce_epi4<bf16><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
-  else
-    k_sk_reduce_epi4<float><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
+  HE_DISPATCH_PT_CT(dtype, act, {
+    k_sk_reduce_epi4<PT, CT><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
+  });
   return cudaGetLastError();
 }
 
-cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si,
+cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
                             const void *g, const void *b, float eps, void *h, int h_rows,
                             int rows, int d, cudaStream_t st) {
@@ -365,45 +367,35 @@ cudaError_t launch_resid_ln(int dtype, const float *partial, const SliceInfo &si
   if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
     return cudaErrorInvalidValue;
   const size_t sm = (size_t)d * sizeof(float);
-  if (dtype == 1)
-    k_resid_ln<bf16><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
-                                                       (const bf16 *)bias, x, (const bf16 *)g,
-                                                       (const bf16 *)b, eps, (bf16 *)h, h_rows, d);
-  else
-    k_resid_ln<float><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
-                                                        (const float *)bias, x, (const float *)g,
-                                                        (const float *)b, eps, (float *)h, h_rows, d);
+  HE_DISPATCH_PT_CT(dtype, out_act, {
+    k_resid_ln<PT, CT><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
+                                                          (const PT *)bias, x, (const PT *)g,
+                                                          (const PT *)b, eps, (CT *)h, h_rows, d);
+  });
   return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_epi(int dtype, const float *partial, int split, long long split_stride,
-                              int ldp, int M, int N, const Epi &epi, cudaStream_t st) {
+cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int split,
+                              long long split_stride, int ldp, int M, int N, const Epi &epi,
+                              cudaStream_t st) {
   const long long n = (long long)M * N;
   if (n <= 0) return cudaSuccess;
   const bool vec = N % 4 == 0 && ldp % 4 == 0 && split_stride % 4 == 0 &&
                    (uintptr_t)partial % 16 == 0;
   const long long work = vec ? n / 4 : n;
   const int blocks = (int)((work + 255) / 256);
-  if (vec) {
-    if (dtype == 1)
-      k_reduce_epi4<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  HE_DISPATCH_PT_CT(dtype, act, {
+    if (vec)
+      k_reduce_epi4<PT, CT><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
     else
-      k_reduce_epi4<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
-  } else {
-    if (dtype == 1)
-      k_reduce_epi<bf16><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
-    else
-      k_reduce_epi<float><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
-  }
+      k_reduce_epi<PT, CT><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+  });
   return cudaGetLastError();
 }
 
-cudaError_t launch_head_select(int dtype, const HeadArgs &a, cudaStream_t st) {
+cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st) {
   const size_t sm = (size_t)a.d * sizeof(float);
-  if (dtype == 1)
-    k_head_select<bf16><<<a.B, 1024, sm, st>>>(a);
-  else
-    k_head_select<float><<<a.B, 1024, sm, st>>>(a);
+  HE_DISPATCH_PT_CT(dtype, act, { k_head_select<PT, CT><<<a.B, 1024, sm, st>>>(a); });
   return cudaGetLastError();
 }
 
@@ -421,13 +413,20 @@ cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_fuse_tiled(void *out, const void *src, const void *a, const void *bm, int rows,
-                              int cols, int r, float scale, cudaStream_t st) {
+cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const void *a,
+                              const void *bm, int rows, int cols, int r, float scale,
+                              cudaStream_t st) {
   if (rows % 128 || cols % 64) return cudaErrorInvalidValue;
   const long long n = (long long)rows * cols / 8;
-  k_fuse_tiled<<<(int)((n + 255) / 256), 256, 0, st>>>((uint4 *)out, (const bf16 *)src,
-                                                      (const bf16 *)a, (const bf16 *)bm, rows,
-                                                      cols, r, scale);
+  const int blocks = (int)((n + 255) / 256);
+  if (out_act == ACT_F16)
+    k_fuse_tiled<f16><<<blocks, 256, 0, st>>>((uint4 *)out, (const bf16 *)src, (const bf16 *)a,
+                                              (const bf16 *)bm, rows, cols, r, scale);
+  else if (out_act == ACT_BF16)
+    k_fuse_tiled<bf16><<<blocks, 256, 0, st>>>((uint4 *)out, (const bf16 *)src, (const bf16 *)a,
+                                               (const bf16 *)bm, rows, cols, r, scale);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
@@ -435,7 +434,8 @@ cudaError_t launch_tile_act(const void *x, int M, int K, int ldx, int R, void *o
                             cudaStream_t st) {
   if (K % 64 || R < M) return cudaErrorInvalidValue;
   const long long n = (long long)R * K;
-  k_tile_act<<<(int)((n + 255) / 256), 256, 0, st>>>((const bf16 *)x, M, K, ldx, R, (bf16 *)out);
+  k_tile_act<<<(int)((n + 255) / 256), 256, 0, st>>>((const uint16_t *)x, M, K, ldx, R,
+                                                    (uint16_t *)out);
   return cudaGetLastError();
 }
 

@@ -65,7 +65,9 @@ typedef enum {
   HE_ERR_DEVICE_CHECK = -6  /* a device-side input check failed (e.g. token id >= vocab) */
 } he_status;
 
-enum { HE_DTYPE_F32 = 0, HE_DTYPE_BF16 = 1 };
+/* Element types.  he_config.dtype takes F32 or BF16; the kernel-level entries of
+ * he_ops.h also take F16. */
+enum { HE_DTYPE_F32 = 0, HE_DTYPE_BF16 = 1, HE_DTYPE_F16 = 2 };
 
 /* Bit i of he_config.lora_targets: projection i carries a LoRA pair. */
 enum {
@@ -77,10 +79,12 @@ typedef struct {
   int n_layers, d_model, n_heads, ffn, vocab;
   int max_pos;      /* usable positions; E_pos has max_pos + pos_offset rows */
   int pos_offset;   /* 2 for OPT's learned positions */
-  int dtype;        /* HE_DTYPE_*: storage of every parameter, of the KV cache and of the
-                       GEMM inputs.  F32: fp32 CUDA-core kernels.  BF16: tcgen05 tensor
-                       cores with fp32 accumulation; residual stream, LayerNorm, softmax,
-                       logits and log-probs stay fp32. */
+  int dtype;        /* HE_DTYPE_F32 or HE_DTYPE_BF16: storage type of every parameter.
+                       F32: fp32 CUDA-core kernels throughout.  BF16: tensor cores with
+                       fp32 accumulation; while LoRA is fused the merged projections are
+                       held as fp16 (see he_fuse_lora) and activations, the KV cache and
+                       GEMM operands are fp16; unfused they are bf16.  The residual
+                       stream, LayerNorm, softmax, logits and log-probs are fp32. */
   float ln_eps;     /* 1e-5 for OPT */
   int max_batch;    /* workspace sizing: every he_generate has B <= max_batch */
   int max_seq;      /* workspace sizing: Lp + Lgen <= max_seq (the KV cache length);
@@ -157,10 +161,14 @@ he_status he_create(const he_config *cfg, const he_weights *w, const he_allocato
  * caller's job: destroying a fused engine leaves the weights fused).  NULL is a no-op. */
 he_status he_destroy(he_engine *h);
 
-/* [DSC-lora], [HE-guide]: saves the bits of every targeted projection, then
- * writes W <- round(W + (alpha/r) * B A) in place (fp32 arithmetic, round to
- * nearest even into the storage type).  HE_ERR_STATE if already fused; the
- * restore copy (sum of the targeted projections' sizes) is taken through the
+/* [DSC-lora], [HE-guide]: saves the bits of the projections, then writes the
+ * merged weight W + (alpha/r) * B A (fp32 arithmetic) in place.  F32: the
+ * targeted projections, round to nearest.  BF16: all six projections of every
+ * layer are rewritten as fp16 (round to nearest even; OPT's native precision and
+ * the pages' hybrid-engine test config, fp16.enabled) in the tiled streaming
+ * layout of he_ops.h, merged where LoRA-targeted.  While fused the weight
+ * tensors hold that representation; he_unfuse_lora restores the original bits.
+ * HE_ERR_STATE if already fused; the restore copy is taken through the
  * allocator (HE_ERR_OOM leaves the engine unfused and the weights untouched). */
 he_status he_fuse_lora(he_engine *h, void *stream);
 

@@ -18,13 +18,14 @@ def _bound(x, w, K):
     return K * 2.0 ** -23 * mag + 1e-6
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (3, 256, 8), (16, 384, 768), (17, 200, 136),
                                    (100, 640, 1024), (129, 128, 520), (300, 1000, 256),
                                    (513, 384, 64)])
-def test_linear_bf16_tcgen05_matches_exact(cuda_device, M, N, K):
+def test_linear_16bit_tcgen05_matches_exact(cuda_device, M, N, K, dt):
     g = torch.Generator().manual_seed(M * 7919 + N * 31 + K)
-    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
-    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    x = torch.randn(M, K, generator=g).to(dt).cuda()
+    w = torch.randn(N, K, generator=g).to(dt).cuda()
     y = he.linear(x, w)
     torch.cuda.synchronize()
     ref = _exact(x, w)
@@ -116,10 +117,11 @@ def test_linear_bf16_tiled_weights(cuda_device, M, N, K, split):
                                         (5, 128, 640, -5), (33, 256, 192, -6), (128, 1280, 128, -7),
                                         (9, 512, 1152, -13), (16, 15360, 256, 0)])
 @pytest.mark.parametrize("tiled", [False, True])
-def test_linear_bf16_stream_k(cuda_device, M, N, K, ctas, tiled):
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_linear_16bit_stream_k(cuda_device, M, N, K, ctas, tiled, dt):
     g = torch.Generator().manual_seed(M * 13 + N + K)
-    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
-    w = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    x = torch.randn(M, K, generator=g).to(dt).cuda()
+    w = torch.randn(N, K, generator=g).to(dt).cuda()
     y = he.linear(x, w, split=ctas, w_tiled=he.tile_weight(w) if tiled else None)
     torch.cuda.synchronize()
     err = np.abs(y.cpu().numpy() - _exact(x, w))
@@ -138,7 +140,7 @@ def test_linear_bf16_stream_k_ragged_rows(cuda_device, M, N, K):
     assert (err <= _bound(x, w, K)).all(), err.max()
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("B,H,hd,T,n,split", [(2, 4, 32, 40, 17, 1), (3, 5, 64, 300, 257, 1),
                                               (1, 2, 128, 512, 511, 4), (4, 3, 128, 64, 1, 1),
                                               (2, 2, 64, 200, 133, 3)])
@@ -154,5 +156,5 @@ def test_attn_decode_matches_softmax(cuda_device, dtype, B, H, hd, T, n, split):
     p = torch.softmax(qd @ kd.transpose(-1, -2), -1)
     ref = (p @ vd).view(B, H * hd).numpy()
     got = ctx.double().cpu().numpy()
-    tol = 1e-5 if dtype == torch.float32 else 1e-2  # bf16 output rounding
+    tol = {torch.float32: 1e-5, torch.bfloat16: 1e-2, torch.float16: 2e-3}[dtype]  # output rounding
     np.testing.assert_allclose(got, ref, atol=tol, rtol=tol)
