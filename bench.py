@@ -215,7 +215,11 @@ def workload_config(cfg):
             "prompt_len": cfg.prompt_len, "gen_len": cfg.gen_len,
             "lora": f"r={cfg.lora_r} alpha={int(cfg.lora_alpha)} on q,k,v,out,fc1,fc2",
             "step": "fuse + prefill + decode + unfuse + release/retake workspace",
-            "l2": "inputs larger than L2 (weights and KV cache stream from HBM every step)"}
+            "l2": "inputs larger than L2 (weights and KV cache stream from HBM every step)",
+            "precision": ("bf16 model weights; while LoRA is fused the merged weights, "
+                          "activations and KV cache are fp16 with fp32 accumulation; "
+                          "LayerNorm, softmax, logits and log-probs fp32; the tied LM head "
+                          "reads the bf16 embedding")}
 
 
 def main():
@@ -358,7 +362,7 @@ def main():
     pf_ms = phase["prefill_ms"] / steps
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (N(0,0.02) weights and LoRA factors, uniform prompt ids)",
             "config": workload_config(cfg), "clocks": clk, "gpu_launches": launches,
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
