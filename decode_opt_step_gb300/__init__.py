@@ -92,6 +92,8 @@ _SIGNATURES = {
     "he_op_tile_weight": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p]),
     "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "he_op_attn_decode_noalloc": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                          c_int, c_int, c_int, c_int, c_int, c_void_p]),
 }
 
 _lib = None
@@ -337,6 +339,20 @@ def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
                                  B, H, hd, T, n_keys, split,
                                  part.data_ptr() if part is not None else None,
                                  _stream_handle(torch, stream)))
+    return ctx
+
+
+def attn_decode_noalloc(q, kc, vc, n_keys: int, split: int = 1, out=None, stream=None):
+    """Decode attention through he_op_attn_decode_noalloc: the split partials use the
+    library's built-in scratch, so nothing is allocated for them (``out`` may be
+    given to avoid the output allocation as well)."""
+    import torch
+    lib = load_library()
+    B, H, T, hd = kc.shape
+    ctx = out if out is not None else torch.empty((B, H * hd), dtype=q.dtype, device=q.device)
+    _check(lib.he_op_attn_decode_noalloc(_dtype_code(torch, q.dtype), q.data_ptr(), kc.data_ptr(),
+                                         vc.data_ptr(), ctx.data_ptr(), B, H, hd, T, n_keys,
+                                         split, _stream_handle(torch, stream)))
     return ctx
 
 

@@ -51,6 +51,14 @@ constexpr int kClasses = 8;
 
 }  // namespace
 
+namespace he {
+// Sets the calling thread's he_last_error message (used by entry points in other files).
+he_status set_error(he_status s, const char *msg) {
+  g_err = msg ? msg : "";
+  return s;
+}
+}  // namespace he
+
 struct he_engine {
   he_config cfg{};
   int device = 0, num_sms = 0;

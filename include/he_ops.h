@@ -60,6 +60,24 @@ he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void
                             int B, int H, int hd, int max_seq, int n_keys, int split, float *part,
                             void *stream);
 
+/* he_op_attn_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a convenience of this library.  Code being
+ * captured into a CUDA graph must not call cudaMalloc/cudaFree, pooled or
+ * budgeted runtimes cannot hand out an extra buffer on demand, and latency-bound
+ * loops avoid cudaMalloc because it may synchronise the device; such callers
+ * pass only inputs and outputs here.  Same arguments and results as
+ * he_op_attn_decode, except that the split-over-keys partial results live in a
+ * 16 MiB array built into the library (4194304 floats, held on every GPU that
+ * loads it until the process exits): B * H * split * (hd + 2) must not exceed
+ * 4194304 when split > 1, else HE_ERR_ARG.  It allocates nothing.  The first call
+ * on a device looks up that array's device address (host-side set-up); make that
+ * first call before any stream capture.  Every call shares the one array, so
+ * calls whose work overlaps on the GPU (other streams, concurrent graphs) race
+ * and must be ordered by the caller; nothing in it needs to start at zero. */
+he_status he_op_attn_decode_noalloc(int dtype, const void *q, const void *kc, const void *vc,
+                                    void *ctx, int B, int H, int hd, int max_seq, int n_keys,
+                                    int split, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
