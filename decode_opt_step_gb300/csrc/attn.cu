@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(128)
   const T *kb = kc + row0 * HD + li * VEC;
   const T *vb = vc + row0 * HD + li * VEC;
 
+  pdl_wait();
   float qv[VEC];
   Vec16<T>::load(q + ((long long)b * H + h) * HD + li * VEC, qv);
   float m = -INFINITY, l = 0.f, o[VEC];
@@ -152,11 +153,14 @@ __global__ void __launch_bounds__(128)
       }
     }
   }
+  pdl_trigger();  // many waves: the next kernel starts launching as the last ones finish
 }
 
 template <typename T, int HD>
 __global__ void k_attn_combine(const float *__restrict__ part, T *__restrict__ ctx, int ctx_rows,
                                int H, int nsplit) {
+  pdl_wait();
+  pdl_trigger();
   const int bh = blockIdx.x, dd = threadIdx.x;
   const float *pp = part + (long long)bh * nsplit * (HD + 2);
   float M = -INFINITY;
@@ -262,10 +266,13 @@ cudaError_t decode_t(const void *q, const void *kc, const void *vc, void *ctx, i
   const int ns = (n_keys + per - 1) / per;
   if (ns > 1 && !part) return cudaErrorInvalidValue;
   dim3 grid(B * H, ns);
-  k_attn_decode<T, HD, 4><<<grid, 128, 0, st>>>((const T *)q, (const T *)kc, (const T *)vc,
-                                                (T *)ctx, ctx_rows, H, max_seq, n_keys, per, part);
-  if (ns > 1) k_attn_combine<T, HD><<<B * H, HD, 0, st>>>(part, (T *)ctx, ctx_rows, H, ns);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(k_attn_decode<T, HD, 4>, grid, dim3(128), 0, st, g_pdl, (const T *)q,
+                           (const T *)kc, (const T *)vc, (T *)ctx, ctx_rows, H, max_seq, n_keys,
+                           per, part);
+  if (e == cudaSuccess && ns > 1)
+    e = launch_k(k_attn_combine<T, HD>, dim3(B * H), dim3(HD), 0, st, g_pdl, (const float *)part,
+                 (T *)ctx, ctx_rows, H, ns);
+  return e;
 }
 
 template <typename T, int HD>

@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(128)
   const int g = lane >> 2, tg = lane & 3;
   const long long row0 = ((long long)b * H + h) * max_seq;
 
+  pdl_wait();
   load_tile<HD>(qs, q + ((long long)b * Lp + qb * 64) * d + h * HD, d, Lp - qb * 64);
   __syncthreads();
   // Q fragments of this warp's 16 rows, all k-steps
@@ -210,9 +211,8 @@ cudaError_t run(const void *q, const void *kc, const void *vc, void *ctx, int B,
     attr = true;
   }
   dim3 grid((Lp + 63) / 64, B * H);
-  k_attn_prefill_mma<T, HD><<<grid, 128, sm, st>>>((const uint16_t *)q, (const uint16_t *)kc,
-                                                   (const uint16_t *)vc, (T *)ctx, H, Lp, max_seq);
-  return cudaGetLastError();
+  return launch_k(k_attn_prefill_mma<T, HD>, grid, dim3(128), sm, st, g_pdl, (const uint16_t *)q,
+                  (const uint16_t *)kc, (const uint16_t *)vc, (T *)ctx, H, Lp, max_seq);
 }
 
 }  // namespace

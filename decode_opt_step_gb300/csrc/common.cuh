@@ -248,3 +248,13 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[W]) {
     tmem_ld16(taddr, v);
   }
 }
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream is still
+// running; pdl_wait() blocks until that kernel has completed and its memory is
+// visible, pdl_trigger() lets the next kernel start launching.  Both are no-ops
+// for a kernel launched normally.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}

@@ -52,6 +52,8 @@ constexpr int kClasses = 8;
 }  // namespace
 
 namespace he {
+bool g_pdl = true;
+
 // Sets the calling thread's he_last_error message (used by entry points in other files).
 he_status set_error(he_status s, const char *msg) {
   g_err = msg ? msg : "";

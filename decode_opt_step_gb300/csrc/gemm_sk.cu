@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();  // one CTA per SM: the next kernel may start its set-up
 
   if (warp == 4 && lane == 0) {
     // ---------------- loads ----------------
@@ -126,20 +127,13 @@ __global__ void __launch_bounds__(192, 1)
       if (a.n_groups > 2) prefetch_tmap(&tm_w2);
     }
     long long issued = 0;
-    bool stop = false;
-    for (long long u = u_begin; u < u_end && !stop; ++u) {
+    // Weights do not depend on the kernel before this one: the weight part of the
+    // first stages is requested before waiting for it (programmatic dependent
+    // launch), the activation part after.
+    auto load_a = [&](long long u, int s) {
       const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
       const int group = a.n_groups > 1 ? t / a.tiles_per_group : 0;
       const int lt = t - group * (a.n_groups > 1 ? a.tiles_per_group : 0);
-      const long long i = u - u_begin;
-      const int s = (int)(i % STAGES);
-      if (i >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
-        *(volatile int *)abort_flag = 1;
-        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
-        break;
-      }
-      if (*(volatile int *)abort_flag) break;
-      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
       if (a.tiled) {
         const uint16_t *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
         bulk_load(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s]);
@@ -150,8 +144,31 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(smA + s * C::STAGE_A + j * A_BYTES, tw, &full[s], (kb * KPS + j) * BK,
                       lt * BM);
       }
-      // the stage's activation k-blocks: one contiguous block of the row-tiled input
+    };
+    auto load_b = [&](long long u, int s) {
+      const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
       bulk_load(smB + s * C::STAGE_B, x + (long long)kb * KPS * BN * BK, C::STAGE_B, &full[s]);
+    };
+    const long long pre = min((long long)STAGES, u_end - u_begin);
+    for (long long i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+      load_a(u_begin + i, (int)i);
+    }
+    pdl_wait();
+    for (long long i = 0; i < pre; ++i) load_b(u_begin + i, (int)i);
+    issued = pre;
+    for (long long u = u_begin + pre; u < u_end; ++u) {
+      const long long i = u - u_begin;
+      const int s = (int)(i % STAGES);
+      if (!mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      load_a(u, s);
+      load_b(u, s);
       issued = i + 1;
     }
     for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
@@ -202,6 +219,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp < 4) {
     // ---------------- epilogue ----------------
+    pdl_wait();  // outputs may still be read by the kernel before this one
     int seg = 0;
     for (long long u = u_begin; u < u_end;) {
       const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
@@ -276,9 +294,8 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_sk<CT, BN, STAGES, KPS><<<P, 192, C::SMEM, st>>>(
-      tw[0], tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
-  return cudaGetLastError();
+  return launch_k(k_gemm_sk<CT, BN, STAGES, KPS>, dim3(P), dim3(192), C::SMEM, st, g_pdl, tw[0],
+                  tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
 }
 
 }  // namespace

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
 
   if (warp == 4 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(192, 1)
     const int m_row = (m_tile - group * tiles_per_group) * BM;
     if (!ABULK) prefetch_tmap(tw);
     prefetch_tmap(&tm_x);
+    pdl_wait();
     // tiled weights: this CTA's k-blocks of tile row `m_row / BM` are contiguous
     const uint16_t *wtile =
         ABULK ? wt.p[group] + ((long long)(m_row / BM) * wt.kt + kb0) * (BM * BK) : nullptr;
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_commit(accum);        // arrives when every MMA issued above is complete
   } else if (warp < 4) {
     // ---------------- epilogue ----------------
+    pdl_wait();
     const bool ok = mbar_wait_bounded(accum, 0);
     if (!ok) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
     tc_fence_after();
@@ -253,10 +256,9 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   if (effective_split(a.K, a.split) != a.split) return cudaErrorInvalidValue;
   const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
   dim3 grid(a.N / BM + (a.N % BM != 0), (a.M + BN - 1) / BN, a.split);
-  k_gemm_tc<CT, BN, STAGES, ABULK><<<grid, 192, C::SMEM, st>>>(
-      tw[0], tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total, kb_per_split, a.epi, wt,
-      dev_err);
-  return cudaGetLastError();
+  return launch_k(k_gemm_tc<CT, BN, STAGES, ABULK>, grid, dim3(192), C::SMEM, st, g_pdl, tw[0],
+                  tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total, kb_per_split, a.epi, wt,
+                  dev_err);
 }
 
 }  // namespace

@@ -32,6 +32,30 @@ enum ActType : int { ACT_F32 = 0, ACT_BF16 = 1, ACT_F16 = 2 };
     }                                                         \
   } while (0)
 
+// Launch with programmatic stream serialisation (see pdl_wait in common.cuh) when
+// `pdl` is set; every kernel launched this way waits before its dependent reads
+// and writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Whether decode-path kernels are launched with programmatic dependent launch.
+extern bool g_pdl;
+
 // Error flags written by kernels (the host reads them in he_check).
 enum : int {
   DEVERR_BAD_TOKEN = 1,    // a token id outside [0, vocab) was replaced by 0

@@ -50,6 +50,8 @@ __global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const 
                            float eps, float *x, CT *h, int d, int *dev_err) {
   extern __shared__ float row[];
   __shared__ float red[33];
+  pdl_wait();
+  pdl_trigger();
   const int tok = blockIdx.x;
   int id = ids[tok];
   if (id < 0 || id >= vocab) {
@@ -95,6 +97,8 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
                            OT *h, int h_rows, int d) {
   extern __shared__ float row[];
   __shared__ float red[33];
+  pdl_wait();
+  pdl_trigger();
   const long long r = blockIdx.x;
   float4 *xr = reinterpret_cast<float4 *>(x + r * d);
   const float *pr = partial + r * ldp;
@@ -116,6 +120,8 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
 template <typename PT, typename CT>
 __global__ void k_reduce_epi4(const float *partial, int split, long long split_stride, int ldp,
                               int M, int N, const __grid_constant__ Epi epi) {
+  pdl_wait();
+  pdl_trigger();
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int n4 = N / 4;
   if (e >= (long long)M * n4) return;
@@ -131,6 +137,8 @@ __global__ void k_reduce_epi4(const float *partial, int split, long long split_s
 template <typename PT, typename CT>
 __global__ void k_sk_reduce_epi4(const float *partial, const SliceInfo si, long long split_stride,
                                  int ldp, int M, int N, const __grid_constant__ Epi epi) {
+  pdl_wait();
+  pdl_trigger();
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int n4 = N / 4;
   if (e >= (long long)M * n4) return;
@@ -147,6 +155,8 @@ __global__ void k_sk_reduce_epi4(const float *partial, const SliceInfo si, long 
 template <typename PT, typename CT>
 __global__ void k_reduce_epi(const float *partial, int split, long long split_stride, int ldp,
                              int M, int N, const __grid_constant__ Epi epi) {
+  pdl_wait();
+  pdl_trigger();
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= (long long)M * N) return;
   const int tok = (int)(e / N), n = (int)(e % N);
@@ -165,6 +175,8 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   __shared__ float s_val[32];
   __shared__ int s_idx[32];
   __shared__ int s_tok;
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const float *lg = a.logits + (long long)b * a.ldl;
   float best = -INFINITY;
@@ -339,11 +351,11 @@ cudaError_t launch_embed_ln(int dtype, int act, const int32_t *ids, int n_tok, i
   if (n_tok <= 0) return cudaSuccess;
   const size_t sm = (size_t)d * sizeof(float);
   HE_DISPATCH_PT_CT(dtype, act, {
-    k_embed_ln<PT, CT><<<n_tok, row_threads(d), sm, st>>>(
-        ids, tok_per_seq, pos0, (const PT *)tok_emb, (const PT *)pos_emb, pos_offset, vocab,
-        (const PT *)g, (const PT *)b, eps, x, (CT *)h, d, dev_err);
+    return launch_k(k_embed_ln<PT, CT>, dim3(n_tok), dim3(row_threads(d)), sm, st, g_pdl, ids,
+                    tok_per_seq, pos0, (const PT *)tok_emb, (const PT *)pos_emb, pos_offset,
+                    vocab, (const PT *)g, (const PT *)b, eps, x, (CT *)h, d, dev_err);
   });
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const SliceInfo &si,
@@ -354,9 +366,10 @@ cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const
   if (work <= 0) return cudaSuccess;
   const int blocks = (int)((work + 255) / 256);
   HE_DISPATCH_PT_CT(dtype, act, {
-    k_sk_reduce_epi4<PT, CT><<<blocks, 256, 0, st>>>(partial, si, split_stride, ldp, M, N, epi);
+    return launch_k(k_sk_reduce_epi4<PT, CT>, dim3(blocks), dim3(256), 0, st, g_pdl, partial, si,
+                    split_stride, ldp, M, N, epi);
   });
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const SliceInfo &si,
@@ -368,11 +381,11 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
     return cudaErrorInvalidValue;
   const size_t sm = (size_t)d * sizeof(float);
   HE_DISPATCH_PT_CT(dtype, out_act, {
-    k_resid_ln<PT, CT><<<rows, row_threads(d), sm, st>>>(partial, si, split_stride, ldp,
-                                                          (const PT *)bias, x, (const PT *)g,
-                                                          (const PT *)b, eps, (CT *)h, h_rows, d);
+    return launch_k(k_resid_ln<PT, CT>, dim3(rows), dim3(row_threads(d)), sm, st, g_pdl, partial,
+                    si, split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
+                    (CT *)h, h_rows, d);
   });
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int split,
@@ -386,17 +399,20 @@ cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int spli
   const int blocks = (int)((work + 255) / 256);
   HE_DISPATCH_PT_CT(dtype, act, {
     if (vec)
-      k_reduce_epi4<PT, CT><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
-    else
-      k_reduce_epi<PT, CT><<<blocks, 256, 0, st>>>(partial, split, split_stride, ldp, M, N, epi);
+      return launch_k(k_reduce_epi4<PT, CT>, dim3(blocks), dim3(256), 0, st, g_pdl, partial,
+                      split, split_stride, ldp, M, N, epi);
+    return launch_k(k_reduce_epi<PT, CT>, dim3(blocks), dim3(256), 0, st, g_pdl, partial, split,
+                    split_stride, ldp, M, N, epi);
   });
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st) {
   const size_t sm = (size_t)a.d * sizeof(float);
-  HE_DISPATCH_PT_CT(dtype, act, { k_head_select<PT, CT><<<a.B, 1024, sm, st>>>(a); });
-  return cudaGetLastError();
+  HE_DISPATCH_PT_CT(dtype, act, {
+    return launch_k(k_head_select<PT, CT>, dim3(a.B), dim3(1024), sm, st, g_pdl, a);
+  });
+  return cudaSuccess;
 }
 
 cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,
