@@ -382,10 +382,11 @@ def linear(x, w, split: int = 1, stream=None, w_tiled=None):
     if x.stride(1) != 1 or not w.is_contiguous():
         raise ValueError("x rows and w must be dense")
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    if split <= 0:  # stream-K: up to 16 slices per tile + the row-tiled copy of x
+    if split <= 0:  # stream-K: up to 16 slices per tile, row-tiled x, tile counters
         R = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
-        scratch = torch.empty(16 * M * N + (R * K + 1) // 2 + 4, dtype=torch.float32,
-                              device=x.device)
+        Np = (N + 127) // 128 * 128
+        scratch = torch.empty(16 * M * Np + (R * K + 1) // 2 + 4 + Np // 128,
+                              dtype=torch.float32, device=x.device)
     else:
         scratch = (torch.empty((split, M, N), dtype=torch.float32, device=x.device)
                    if split > 1 else None)

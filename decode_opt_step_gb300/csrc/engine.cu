@@ -77,6 +77,7 @@ struct he_engine {
   Buf kc, vc, x, h, q, ctx, mid, partial, logits, attn_part, ids_in, ids_out, lp_out, logmap;
   // held for the engine's lifetime
   Buf err;
+  Buf tilecnt;  // per-tile arrival counters of the stream-K fix-up (zero between GEMMs)
   // LoRA restore copy (held while fused)
   Buf restore;
 
@@ -114,6 +115,13 @@ void put(he_engine *h, Buf &b, cudaStream_t st) {
   b.bytes = 0;
 }
 
+// Stream-K tile counters: one int per 128-row tile of the widest projection.
+size_t tilecnt_bytes(const he_config &c) {
+  size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
+  if ((size_t)c.vocab > wide) wide = c.vocab;
+  return (wide + 127) / 128 * sizeof(int);
+}
+
 void free_workspace(he_engine *h, cudaStream_t st) {
   Buf *all[] = {&h->kc, &h->vc, &h->x, &h->h, &h->q, &h->ctx, &h->mid, &h->partial,
                 &h->logits, &h->attn_part, &h->ids_in, &h->ids_out, &h->lp_out, &h->logmap};
@@ -133,6 +141,7 @@ he_status take_workspace(he_engine *h, cudaStream_t st) {
   const size_t kv = (size_t)c.n_layers * h->kv_layer_elems() * e;
   size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
   if ((size_t)c.vocab > wide) wide = c.vocab;  // LM-head slices
+  wide = (wide + 127) / 128 * 128;             // tile-contiguous slices: whole 128-wide tiles
   size_t part = max_tok * c.d_model;
   if ((size_t)kMaxGemmSplit * c.max_batch * wide > part) part = (size_t)kMaxGemmSplit * c.max_batch * wide;
   struct {
@@ -222,8 +231,9 @@ int act_rows(const he_engine *h, int B, bool decode) {
   return decode && h->cfg.dtype == HE_DTYPE_BF16 ? sk_token_tile(B) : 0;
 }
 
-// One projection GEMM.  Element-wise epilogues (QKV, ReLU) are completed here
-// (split-K / stream-K slices reduced by a second kernel); for EPI_PARTIAL the
+// One projection GEMM.  Element-wise epilogues (QKV, ReLU, logits) are completed
+// here (stream-K: inside the GEMM by the last run of each tile; split-K: slices
+// reduced by a second kernel); for EPI_PARTIAL the
 // fp32 slices stay in h->partial and the returned SliceInfo tells the row
 // consumer how to add them.
 SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
@@ -243,17 +253,22 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   a.w_tiled = tiled_w;
   SliceInfo si{1, 0, 0, 0};
   float *part = static_cast<float *>(h->partial.p);
-  const long long stride = (long long)M * a.N;
+  long long stride = (long long)M * a.N;
   Timed t(h, cls, c.st);
   if (use_stream_k(h, M, a.N, K, decode, tiled_w)) {
-    const int P = sk_ctas(a, h->num_sms);
-    const long long U = sk_units(a), T = (a.N + 127) / 128;
-    si = SliceInfo{0, U, (int)(U / T), P};
     a.split = 1;
     a.epi = epi;
-    c.check(launch_gemm_sk(a, P, part, stride, static_cast<int *>(h->err.p), c.st), 1);
+    // element-wise epilogues finish inside the kernel (last run of each tile)
+    const bool fix = sk_fixup_ok(a);
+    const int P = sk_ctas(a, h->num_sms, fix);
+    const long long U = sk_units(a), T = (a.N + 127) / 128;
+    if (fix) stride = (long long)M * T * 128;  // tile-contiguous slices
+    si = SliceInfo{0, U, (int)(U / T), P};
+    c.check(launch_gemm_sk(a, P, part, stride, fix ? static_cast<int *>(h->tilecnt.p) : nullptr,
+                           static_cast<int *>(h->err.p), c.st),
+            1);
     // P == tiles: every tile is one run and was stored by the GEMM itself
-    if (epi.kind != EPI_PARTIAL && P != T)
+    if (epi.kind != EPI_PARTIAL && !fix && P != T)
       c.check(launch_sk_reduce_epi(a.dtype, a.act, part, si, stride, a.N, M, a.N, epi, c.st), 1);
     return si;
   }
@@ -454,6 +469,9 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
   ensure_phase_events(h);
   cudaEventRecord(h->ph[0], st);
+  // the GEMMs leave the tile counters at zero; clearing them here also recovers
+  // from a call whose GEMM gave up on a wait part-way
+  c.check(cudaMemsetAsync(h->tilecnt.p, 0, tilecnt_bytes(cf), st), 0);
   // ---- prefill: all prompt tokens of all sequences in one pass ----
   const int M = B * Lp;
   {
@@ -580,14 +598,22 @@ he_status he_create(const he_config *cfg, const he_weights *w, const he_allocato
     delete h;
     return fail(HE_ERR_OOM, "error-flag allocation failed");
   }
+  if (!get(h, h->tilecnt, tilecnt_bytes(c), nullptr)) {
+    put(h, h->err, nullptr);
+    delete h;
+    return fail(HE_ERR_OOM, "tile-counter allocation failed");
+  }
   ce = cudaMemset(h->err.p, 0, 256);
+  if (ce == cudaSuccess) ce = cudaMemset(h->tilecnt.p, 0, tilecnt_bytes(c));
   if (ce != cudaSuccess) {
+    put(h, h->tilecnt, nullptr);
     put(h, h->err, nullptr);
     delete h;
     return cuda_fail(ce, "memset");
   }
   he_status s = take_workspace(h, nullptr);
   if (s != HE_OK) {
+    put(h, h->tilecnt, nullptr);
     put(h, h->err, nullptr);
     delete h;
     return s;
@@ -602,6 +628,7 @@ he_status he_destroy(he_engine *h) {
   cudaDeviceSynchronize();
   free_workspace(h, nullptr);
   put(h, h->restore, nullptr);
+  put(h, h->tilecnt, nullptr);
   put(h, h->err, nullptr);
   for (auto &e : h->ph)
     if (e) cudaEventDestroy(e);
@@ -916,25 +943,34 @@ he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_l
     a.K = K;
     a.split = 1;
     a.w_tiled = w_layout;
-    int P = sk_ctas(a, sms);
+    Epi e{};
+    e.kind = EPI_STORE_F32;
+    e.partial = y;
+    e.ldp = N;
+    a.epi = e;
+    const bool fix = sk_fixup_ok(a);
+    int P = sk_ctas(a, sms, fix);
     const long long T = (N + 127) / 128, U = sk_units(a);
     if (split < 0) {
       if (-split > U || -split > 15 * T)
         return fail(HE_ERR_ARG, "stream-K CTA count %d above min(units, 15 * tiles)", -split);
       P = -split;
     }
-    Epi e{};
-    e.kind = EPI_STORE_F32;
-    e.partial = y;
-    e.ldp = N;
-    a.epi = e;
     // the stream-K kernel reads row-tiled activations: tile x behind the slices
-    void *xt = scratch + (size_t)16 * M * N;
+    // (16 per tile, tile-contiguous over whole 128-wide tiles), then the tile counters
+    const int R = sk_token_tile(M);
+    const long long sstride = (long long)M * T * 128;
+    void *xt = scratch + (size_t)16 * sstride;
+    int *cnt = reinterpret_cast<int *>(
+        ((uintptr_t)xt + (size_t)R * K * 2 + 15) & ~(uintptr_t)15);
     a.x = xt;
-    cudaError_t r = launch_tile_act(x, M, K, ldx, sk_token_tile(M), xt, st);
+    cudaError_t r = launch_tile_act(x, M, K, ldx, R, xt, st);
     const SliceInfo si{0, U, (int)(U / T), P};
-    if (r == cudaSuccess) r = launch_gemm_sk(a, P, scratch, (long long)M * N, nullptr, st);
+    if (r == cudaSuccess && fix) r = cudaMemsetAsync(cnt, 0, (size_t)T * sizeof(int), st);
     if (r == cudaSuccess)
+      r = launch_gemm_sk(a, P, scratch, fix ? sstride : (long long)M * N, fix ? cnt : nullptr,
+                         nullptr, st);
+    if (r == cudaSuccess && !fix)
       r = launch_sk_reduce_epi(HE_DTYPE_BF16, dtype, scratch, si, (long long)M * N, N, M, N, e, st);
     if (r != cudaSuccess) return cuda_fail(r, "he_op_linear (stream-K)");
     return HE_OK;

@@ -1,4 +1,5 @@
-// Persistent stream-K bf16 GEMM for the decode projections (tcgen05 + TMEM).
+// Persistent stream-K GEMM (bf16 or fp16 operands) for the decode projections
+// (tcgen05 + TMEM).
 //
 // In decode every SM has to stream weights all the time for the projections to
 // run at HBM speed (one SM moves about 1/152 of the HBM bandwidth), so tiles
@@ -6,9 +7,15 @@
 // GEMM are cut into P equal contiguous runs, one per CTA (P = SM count).  A run
 // crosses tile boundaries; each piece of a tile it covers is a "segment".
 // Segments accumulate in TMEM (two accumulators, so the epilogue of one segment
-// overlaps the MMAs of the next) and are written as fp32 slices
-// partial[slot][tok][n], slot = CTA index - first CTA of the tile; the consumer
-// adds the slices of a tile in slot order (sk_segments gives how many).  A tile
+// overlaps the MMAs of the next) and are written as fp32 slices, slot = CTA
+// index - first CTA of the tile (sk_segments gives how many).  For a row-wise
+// consumer (EPI_PARTIAL: residual + LayerNorm) they stay as partial[slot][tok][n]
+// and the consumer adds them in slot order.  Element-wise epilogues finish in the
+// kernel: the tile's first run (its owner; for it the tile is the last segment,
+// while the other runs' parts are their first segments) waits on a per-tile
+// counter for the other slices, adds them to its own accumulator in slot order
+// and stores the outputs; those slices are tile-contiguous,
+// partial[slot][tile][tok][128], so each arrives as one bulk copy.  A tile
 // covered by a single segment gets the element-wise epilogue directly.
 //
 // Warp roles (192 threads): warps 0-3 epilogue (warp w reads TMEM lanes
@@ -59,7 +66,7 @@ struct SkCfg {
   static constexpr int STAGE_A = KPS * A_BYTES;
   static constexpr int STAGE_B = KPS * B_BYTES;
   static constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;  // + barriers and flags
   static constexpr uint32_t TMEM_COLS = pow2_cols(2 * BN);
 };
 
@@ -70,8 +77,9 @@ struct SkArgs {
   int n_groups;
   int M, N, KB;          // tokens, output features, units (KPS k-blocks) per tile
   long long U;           // units = tiles * KB
-  float *slices;         // fp32 slices [slot][M][N]
+  float *slices;         // fp32 slices: [slot][M][N], or [slot][tile][M][128] with tile_cnt
   long long slice_stride;
+  int *tile_cnt;         // per-tile arrival counters (zero between launches); null: no fix-up
 };
 
 template <typename CT, int BN, int STAGES, int KPS>
@@ -90,8 +98,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t *empty = full + STAGES;
   uint64_t *acc_full = empty + STAGES;   // [2]
   uint64_t *acc_empty = acc_full + 2;    // [2]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+  uint64_t *fix_bar = acc_empty + 2;     // the owner's slice copies (tile_owner_epilogue)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+  int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = gridDim.x, c = blockIdx.x;
@@ -106,6 +116,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
+    mbar_init(fix_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -127,6 +138,7 @@ __global__ void __launch_bounds__(192, 1)
       if (a.n_groups > 2) prefetch_tmap(&tm_w2);
     }
     long long issued = 0;
+    const uint64_t pol = l2_evict_first_policy();  // every weight byte is read once
     // Weights do not depend on the kernel before this one: the weight part of the
     // first stages is requested before waiting for it (programmatic dependent
     // launch), the activation part after.
@@ -136,13 +148,13 @@ __global__ void __launch_bounds__(192, 1)
       const int lt = t - group * (a.n_groups > 1 ? a.tiles_per_group : 0);
       if (a.tiled) {
         const uint16_t *src = a.wt[group] + ((long long)lt * a.KB + kb) * (KPS * BM * BK);
-        bulk_load(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s]);
+        bulk_load_hint(smA + s * C::STAGE_A, src, C::STAGE_A, &full[s], pol);
       } else {
         const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
 #pragma unroll
         for (int j = 0; j < KPS; ++j)
-          tma_load_2d(smA + s * C::STAGE_A + j * A_BYTES, tw, &full[s], (kb * KPS + j) * BK,
-                      lt * BM);
+          tma_load_2d_hint(smA + s * C::STAGE_A + j * A_BYTES, tw, &full[s], (kb * KPS + j) * BK,
+                           lt * BM, pol);
       }
     };
     auto load_b = [&](long long u, int s) {
@@ -219,7 +231,20 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp < 4) {
     // ---------------- epilogue ----------------
+    // With a.tile_cnt (element-wise epilogues) a tile split over S runs is finished
+    // inside the kernel by its owner, the run holding its first k-blocks (slot 0;
+    // for that run it is always the last segment, reached at the end of its
+    // range): the other runs (whose part is their first segment, done early) write
+    // fp32 slices and count themselves in the tile's counter; the owner waits for
+    // the count, adds the slices to its own accumulator in slot order, applies the
+    // epilogue and clears the counter.  The owner's staged reduction reuses the
+    // pipeline's shared memory, free after the CTA's last MMA.  Without
+    // a.tile_cnt, tiles of one run are stored directly and the others are left as
+    // slices for a second kernel.
     pdl_wait();  // outputs may still be read by the kernel before this one
+    const bool fix = a.tile_cnt != nullptr && epi.kind != EPI_PARTIAL;
+    constexpr int W = BN >= 32 ? 32 : 16;
+    constexpr int kStageAvail = STAGES * C::STAGE_BYTES;
     int seg = 0;
     for (long long u = u_begin; u < u_end;) {
       const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
@@ -233,22 +258,60 @@ __global__ void __launch_bounds__(192, 1)
       int cf, S;
       sk_segments(t, a.KB, P, a.U, &cf, &S);
       const int slot = c - cf;
-      const bool direct = S == 1 && epi.kind != EPI_PARTIAL;
       const int row = t * BM + warp * 32 + lane;
       const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
-      constexpr int W = BN >= 32 ? 32 : 16;
-      const RowEpi<CT> re = row_epi_prepare<CT>(epi, row < a.N ? row : 0,
-                                                direct ? nullptr : a.slices, a.slice_stride, slot,
-                                                a.N);
+      // (all conditions below are uniform over the four epilogue warps)
+      const bool staged = fix && slot == 0 && u + n == u_end &&
+                          tile_stage_tokens(S, a.M, W, tile_out_bytes(epi.kind, (int)sizeof(CT)),
+                                            kStageAvail) >= W;
+      if (staged) {
+        tile_owner_epilogue<CT, W>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N,
+                                   a.M, t, S, tl, live, &a.tile_cnt[t], base, kStageAvail,
+                                   fix_bar, last_flag, dev_err);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      } else {
+        const bool direct = S == 1 && epi.kind != EPI_PARTIAL;
+        RowEpi<CT> re = row_epi_prepare<CT>(epi, row < a.N ? row : 0,
+                                            direct ? nullptr : a.slices, a.slice_stride, slot,
+                                            a.N);
+        if (fix && !direct) {  // tile-contiguous slices: [slot][tile][M][128]
+          re.f32 = a.slices + slot * a.slice_stride + (size_t)t * a.M * BM + (row - t * BM);
+          re.f32_stride = BM;
+        }
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += W) {
-        float v[W];
-        tmem_load_cols<W>(tl + c0, v);
-        if (live && row < a.N && c0 < a.M) row_epi_store<CT, W>(re, c0, min(W, a.M - c0), v);
+        for (int c0 = 0; c0 < BN; c0 += W) {
+          float v[W];
+          tmem_load_cols<W>(tl + c0, v);
+          if (live && row < a.N && c0 < a.M) row_epi_store<CT, W>(re, c0, min(W, a.M - c0), v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        if (fix && S > 1) {
+          // this run's slice is complete: count it (release), every run of the
+          // tile including an owner without room for the staged reduction
+          __threadfence();
+          epi_bar_sync();
+          if (threadIdx.x == 0 && live) atomicAdd(&a.tile_cnt[t], 1);
+          if (slot == 0) {
+            // owner: wait for all S slices, then reduce them through registers
+            if (threadIdx.x == 0) {
+              bool ok2 = live && wait_count_at_least(&a.tile_cnt[t], S);
+              if (live && !ok2) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+              *last_flag = ok2;
+            }
+            epi_bar_sync();
+            if (*last_flag) {
+              __threadfence();
+              tile_fixup<CT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N, a.M, t,
+                             S, threadIdx.x);
+              if (threadIdx.x == 0) a.tile_cnt[t] = 0;
+            }
+          }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
       u += n;
       ++seg;
     }
@@ -263,7 +326,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <typename CT, int BN, int STAGES, int KPS>
 cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slice_stride,
-                         int *dev_err, cudaStream_t st) {
+                         int *tile_cnt, int *dev_err, cudaStream_t st) {
   using C = SkCfg<BN, STAGES, KPS>;
   constexpr bool fp16 = !std::is_same<CT, bf16>::value;
   CUtensorMap tw[3], tx;
@@ -287,6 +350,7 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.U = (long long)((g.N + BM - 1) / BM) * a.KB;
   a.slices = slices;
   a.slice_stride = slice_stride;
+  a.tile_cnt = tile_cnt;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<CT, BN, STAGES, KPS>,
@@ -306,20 +370,37 @@ long long sk_units(const GemmArgs &g) {
   return (long long)((g.N + 127) / 128) * (g.K / (64 * sk_kps(g)));
 }
 
-// Runs: whole tiles (P = T) when the tiles nearly fill the GPU, which needs no
-// reduction; otherwise one run per SM, at most U runs and at most 15 runs per
-// tile (so a tile never has more than 16 slices).
-int sk_ctas(const GemmArgs &g, int num_sms) {
+// Runs: one per SM, at most U runs and at most 15 runs per tile (so a tile never
+// has more than 16 slices).  Without the in-kernel fix-up, whole tiles (P = T)
+// when the tiles nearly fill the GPU, which needs no reduction.
+int sk_ctas(const GemmArgs &g, int num_sms, bool fixup) {
   const long long T = (g.N + 127) / 128, U = sk_units(g);
-  if (T <= num_sms && 10 * T >= 7LL * num_sms) return (int)T;
+  if (!fixup && T <= num_sms && 10 * T >= 7LL * num_sms) return (int)T;
   long long P = num_sms;
   if (P > U) P = U;
   if (P > 15 * T) P = 15 * T;
   return (int)P;
 }
 
+// The in-kernel completion stores 16-byte groups of outputs (4 fp32 or 8 16-bit).
+bool sk_fixup_ok(const GemmArgs &g) {
+  const Epi &e = g.epi;
+  auto al = [](const void *p) { return (uintptr_t)p % 16 == 0; };
+  switch (e.kind) {
+    case EPI_STORE_F32:
+      return g.N % 4 == 0 && e.ldp % 4 == 0 && al(e.partial);
+    case EPI_RELU:
+      return g.N % 8 == 0 && al(e.out) && (e.out_rows > 0 || e.ldo % 8 == 0);
+    case EPI_QKV:
+      return g.N % 8 == 0 && e.head_dim % 8 == 0 && e.ldo % 8 == 0 && al(e.out) && al(e.kc) &&
+             al(e.vc);
+    default:
+      return false;
+  }
+}
+
 cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long slice_stride,
-                           int *dev_err, cudaStream_t st) {
+                           int *tile_cnt, int *dev_err, cudaStream_t st) {
   // One row tile of tokens (M <= 256), whole 128 x 64 tiles, fp32 slices in epi.partial.
   if ((g.act != ACT_BF16 && g.act != ACT_F16) || g.M < 1 || g.M > 256 || g.K % BK)
     return cudaErrorInvalidValue;
@@ -327,21 +408,27 @@ cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long sl
   if (g.n_groups < 1 || g.n_groups > 3 || g.n_groups * g.group_rows != g.N) return cudaErrorInvalidValue;
   if (g.epi.kind == EPI_QKV && g.epi.d_model % BM) return cudaErrorInvalidValue;
   if (!slices || P < 1 || slice_stride < (long long)g.M * g.N) return cudaErrorInvalidValue;
+  if (tile_cnt && (!sk_fixup_ok(g) || (uintptr_t)slices % 16 ||
+                   slice_stride < (long long)g.M * ((g.N + BM - 1) / BM) * BM))
+    return cudaErrorInvalidValue;
   auto pick = [&](auto ct) -> cudaError_t {
     using CT = decltype(ct);
+#define HE_SK(BN, ST, KPS) \
+  return launch_sk_bn<CT, BN, ST, KPS>(g, P, slices, slice_stride, tile_cnt, dev_err, st)
     if (sk_kps(g) == 2) {
       // two k-blocks per stage: 32 KB weight requests
-      if (g.M <= 16) return launch_sk_bn<CT, 16, 5, 2>(g, P, slices, slice_stride, dev_err, st);
-      if (g.M <= 32) return launch_sk_bn<CT, 32, 5, 2>(g, P, slices, slice_stride, dev_err, st);
-      if (g.M <= 64) return launch_sk_bn<CT, 64, 4, 2>(g, P, slices, slice_stride, dev_err, st);
-      if (g.M <= 128) return launch_sk_bn<CT, 128, 3, 2>(g, P, slices, slice_stride, dev_err, st);
-      return launch_sk_bn<CT, 256, 2, 2>(g, P, slices, slice_stride, dev_err, st);
+      if (g.M <= 16) HE_SK(16, 5, 2);
+      if (g.M <= 32) HE_SK(32, 5, 2);
+      if (g.M <= 64) HE_SK(64, 4, 2);
+      if (g.M <= 128) HE_SK(128, 3, 2);
+      HE_SK(256, 2, 2);
     }
-    if (g.M <= 16) return launch_sk_bn<CT, 16, 10, 1>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 32) return launch_sk_bn<CT, 32, 9, 1>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 64) return launch_sk_bn<CT, 64, 8, 1>(g, P, slices, slice_stride, dev_err, st);
-    if (g.M <= 128) return launch_sk_bn<CT, 128, 6, 1>(g, P, slices, slice_stride, dev_err, st);
-    return launch_sk_bn<CT, 256, 4, 1>(g, P, slices, slice_stride, dev_err, st);
+    if (g.M <= 16) HE_SK(16, 10, 1);
+    if (g.M <= 32) HE_SK(32, 9, 1);
+    if (g.M <= 64) HE_SK(64, 8, 1);
+    if (g.M <= 128) HE_SK(128, 6, 1);
+    HE_SK(256, 4, 1);
+#undef HE_SK
   };
   if (g.act == ACT_BF16) return pick(bf16{});
   return pick(f16{});

@@ -175,9 +175,17 @@ cudaError_t launch_gemm(const GemmArgs &a, int *dev_err, cudaStream_t st);
 // units per tile.
 int sk_kps(const GemmArgs &a);
 long long sk_units(const GemmArgs &a);
-int sk_ctas(const GemmArgs &a, int num_sms);
+int sk_ctas(const GemmArgs &a, int num_sms, bool fixup);
+// Whether a.epi can be completed inside the kernel (tile_cnt != null): an
+// element-wise kind, N % 4 == 0 and vector-aligned outputs.
+bool sk_fixup_ok(const GemmArgs &a);
+// tile_cnt: null, or ceil(N / 128) ints that are zero at the launch (and are left
+// zero): the other runs of a split tile count their finished slices there and the
+// tile's owner applies a.epi to the sum, so no reduction kernel follows; the
+// slices are then tile-contiguous, [slot][tile][M][128], slice_stride >= M *
+// 128 * ceil(N / 128).
 cudaError_t launch_gemm_sk(const GemmArgs &a, int P, float *slices, long long slice_stride,
-                           int *dev_err, cudaStream_t st);
+                           int *tile_cnt, int *dev_err, cudaStream_t st);
 int gemm_pick_split(const GemmArgs &a, int num_sms);  // heuristic for decode shapes
 
 cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int split,

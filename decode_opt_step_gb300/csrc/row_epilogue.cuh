@@ -123,4 +123,276 @@ __device__ __forceinline__ void row_epi_store(const RowEpi<CT> &r, int tok0, int
   }
 }
 
+template <typename CT>
+__device__ __forceinline__ void store4(CT *p, float a, float b, float c, float d) {
+  union {
+    uint2 u;
+    CT e[4];
+  } pk;
+  pk.e[0] = from_f<CT>(a);
+  pk.e[1] = from_f<CT>(b);
+  pk.e[2] = from_f<CT>(c);
+  pk.e[3] = from_f<CT>(d);
+  *reinterpret_cast<uint2 *>(p) = pk.u;
+}
+
+// Final epilogue of one 128-feature output tile from its S fp32 slices
+// (tile-contiguous: tslices + s * sstride + tok * 128 + feature in the tile,
+// s = 0 .. S-1), summed in slot order.  Called by the 128
+// threads et = 0..127 of one CTA: thread et owns features n0 .. n0 + 3 with
+// n0 = 128 t + 4 (et % 32) and tokens et / 32, et / 32 + 4, ...; a warp thus
+// reads and writes 128 consecutive features of one token (coalesced).
+// Needs N % 4 == 0 and, per kind, 16-byte aligned fp32 rows (STORE_F32) or
+// 8-byte aligned groups of four 16-bit outputs (QKV, RELU).
+template <typename CT>
+__device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, long long sstride,
+                                           int N, int M, int t, int S, int et) {
+  const int n0 = t * 128 + 4 * (et & 31);
+  if (n0 >= N) return;
+  float b4[4] = {0.f, 0.f, 0.f, 0.f};
+  float scale = 1.f;
+  int mode = 0;
+  float *f32 = nullptr;
+  CT *dst = nullptr;
+  long long tok_stride = 0, pos_stride = 0;
+  int tps = 1;
+  auto bias4 = [&](const void *bp, int c) {
+    const bf16 *bb = static_cast<const bf16 *>(bp) + c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b4[i] = __bfloat162float(bb[i]);
+  };
+  switch (e.kind) {
+    case EPI_STORE_F32:
+    case EPI_PARTIAL:
+      mode = 0;
+      f32 = e.partial + n0;
+      tok_stride = e.ldp;
+      break;
+    case EPI_RELU:
+      mode = 3;
+      bias4(e.bias[0], n0);
+      dst = static_cast<CT *>(e.out);
+      break;
+    case EPI_QKV: {
+      const int which = n0 / e.d_model;
+      const int c = n0 - which * e.d_model;
+      bias4(e.bias[which], c);
+      if (which == 0) {
+        mode = 1;
+        scale = e.q_scale;
+        dst = static_cast<CT *>(e.out) + c;
+        tok_stride = e.ldo;
+      } else {
+        mode = 2;
+        const int hh = c / e.head_dim, dd = c - hh * e.head_dim;
+        dst = static_cast<CT *>(which == 1 ? e.kc : e.vc) +
+              ((long long)hh * e.max_seq + e.pos0) * e.head_dim + dd;
+        tok_stride = (long long)e.n_heads * e.max_seq * e.head_dim;
+        pos_stride = e.head_dim;
+        tps = e.tok_per_seq;
+      }
+      break;
+    }
+  }
+  const float *src = tslices + 4 * (et & 31);
+  constexpr int TU = 8;  // tokens per thread per round: 8 x 2 slices of loads in flight
+  for (int tb = et >> 5; tb < M; tb += 4 * TU) {
+    float4 acc[TU];
+#pragma unroll
+    for (int i = 0; i < TU; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; s += 2) {
+      float4 v0[TU], v1[TU];
+#pragma unroll
+      for (int i = 0; i < TU; ++i) {
+        const int tok = tb + 4 * i;
+        const float *p = src + (long long)s * sstride + (long long)tok * 128;
+        v0[i] = tok < M ? __ldcg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[i] = tok < M && s + 1 < S ? __ldcg(reinterpret_cast<const float4 *>(p + sstride))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < TU; ++i) {
+        acc[i].x += v0[i].x;
+        acc[i].y += v0[i].y;
+        acc[i].z += v0[i].z;
+        acc[i].w += v0[i].w;
+        if (s + 1 < S) {
+          acc[i].x += v1[i].x;
+          acc[i].y += v1[i].y;
+          acc[i].z += v1[i].z;
+          acc[i].w += v1[i].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < TU; ++i) {
+      const int tok = tb + 4 * i;
+      if (tok >= M) break;
+      const float4 a = acc[i];
+      switch (mode) {
+        case 0:
+          *reinterpret_cast<float4 *>(f32 + (long long)tok * tok_stride) = a;
+          break;
+        case 1:
+          store4<CT>(dst + (long long)tok * tok_stride, (a.x + b4[0]) * scale,
+                     (a.y + b4[1]) * scale, (a.z + b4[2]) * scale, (a.w + b4[3]) * scale);
+          break;
+        case 2: {
+          const int b = tok / tps, p = tok - b * tps;
+          store4<CT>(dst + (long long)b * tok_stride + (long long)p * pos_stride, a.x + b4[0],
+                     a.y + b4[1], a.z + b4[2], a.w + b4[3]);
+          break;
+        }
+        case 3:
+          store4<CT>(dst + act_index(tok, n0, e.ldo, e.out_rows), fmaxf(a.x + b4[0], 0.f),
+                     fmaxf(a.y + b4[1], 0.f), fmaxf(a.z + b4[2], 0.f), fmaxf(a.w + b4[3], 0.f));
+          break;
+      }
+    }
+  }
+}
+
+// Output element type of a stream-K tile's final epilogue: fp32 logits / partial
+// sums, else the activation type.
+__host__ __device__ inline int tile_out_bytes(int kind, int ct_bytes) {
+  return kind == EPI_STORE_F32 || kind == EPI_PARTIAL ? 4 : ct_bytes;
+}
+
+// Tokens of a tile that the staged reduction of the tile's owner handles at a
+// time in `avail` bytes of shared memory (a multiple of W; 0 if not even W fit):
+// per token, the S - 1 other slices' 128 fp32 values and the 128 outputs.
+__host__ __device__ inline int tile_stage_tokens(int S, int M, int W, int out_bytes, int avail) {
+  const int per_tok = (S - 1) * 512 + 128 * out_bytes;
+  int ch = avail / per_tok / W * W;
+  const int m = (M + W - 1) / W * W;
+  return ch < m ? ch : m;
+}
+
+// Address of the 16-byte group of outputs of token `tok` that starts at feature
+// n (a multiple of 16 / out_bytes) of the GEMM output, for an element-wise kind.
+template <typename CT>
+__device__ __forceinline__ void *tile_out_ptr(const Epi &e, int tok, int n) {
+  switch (e.kind) {
+    case EPI_QKV: {
+      const int which = n / e.d_model, c = n - which * e.d_model;
+      if (which == 0) return static_cast<CT *>(e.out) + (long long)tok * e.ldo + c;
+      const int hh = c / e.head_dim, dd = c - hh * e.head_dim;
+      const int b = tok / e.tok_per_seq, p = tok - b * e.tok_per_seq;
+      return static_cast<CT *>(which == 1 ? e.kc : e.vc) +
+             (((long long)b * e.n_heads + hh) * e.max_seq + e.pos0 + p) * e.head_dim + dd;
+    }
+    case EPI_RELU:
+      return static_cast<CT *>(e.out) + act_index(tok, n, e.ldo, e.out_rows);
+    default:
+      return e.partial + (long long)tok * e.ldp + n;
+  }
+}
+
+// Final epilogue of stream-K tile t by its owner (the run holding the tile's first
+// k-blocks, whose accumulator is in TMEM at `tl` for this thread's row), with the
+// other S - 1 runs' fp32 slices in global memory (tile-contiguous: tslices +
+// s * sstride + tok * 128 + feature), once they have all counted themselves in
+// *cnt.  Runs on the four epilogue warps (et = threadIdx.x < 128) after the CTA's
+// last MMA, so the pipeline's shared memory `stage` (avail bytes) is free: per
+// chunk of ch tokens the other slices come in as one bulk copy each (completing
+// on the mbarrier `bar`), each thread adds its row's values in slot order (its own
+// slice is slot 0) and applies the epilogue into a [token][128] staging tile,
+// which then leaves as 16-byte stores.  `flag` is a shared int; returns with
+// every epilogue thread past the same barriers.
+template <typename CT, int W>
+__device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *tslices,
+                                                    long long sstride, int N, int M, int t, int S,
+                                                    uint32_t tl, bool live, int *cnt,
+                                                    uint8_t *stage, int avail, uint64_t *bar,
+                                                    int *flag, int *dev_err) {
+  const int et = threadIdx.x, r = et;  // r: this thread's row (feature) of the tile
+  const int n_row = t * 128 + r;
+  // per-row epilogue constants (parameters: read while the other runs finish)
+  float bias = 0.f, scale = 1.f;
+  if (n_row < N) {
+    if (e.kind == EPI_RELU) {
+      bias = __bfloat162float(static_cast<const bf16 *>(e.bias[0])[n_row]);
+    } else if (e.kind == EPI_QKV) {
+      const int which = n_row / e.d_model;
+      bias = __bfloat162float(static_cast<const bf16 *>(e.bias[which])[n_row - which * e.d_model]);
+      if (which == 0) scale = e.q_scale;
+    }
+  }
+  epi_bar_sync();  // *flag may still be read from an earlier segment
+  if (et == 0) {
+    // acquire: the other runs' slices (written, fenced, then counted) are visible
+    // to this thread and, through the barrier below, to the whole group
+    bool ok = live;
+    if (ok && S > 1 && !wait_count_at_least(cnt, S - 1)) {
+      set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+      ok = false;
+    }
+    *flag = ok;
+  }
+  epi_bar_sync();
+  const bool go = *flag != 0;
+  const int ob = tile_out_bytes(e.kind, (int)sizeof(CT));
+  const int ch = tile_stage_tokens(S, M, W, ob, avail);
+  float *ps = reinterpret_cast<float *>(stage);                 // [S-1][ch][128]
+  uint8_t *os = stage + (size_t)(S - 1) * ch * 512;             // [ch][128] outputs
+  uint32_t phase = 0;
+  for (int c0 = 0; c0 < M; c0 += ch) {
+    const int cn = min(ch, M - c0);
+    if (go && S > 1) {
+      if (et == 0) {
+        // earlier generic reads of the staging area come before these async writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(bar, (uint32_t)((S - 1) * cn * 512));
+        for (int s = 1; s < S; ++s)
+          bulk_load(ps + (size_t)(s - 1) * ch * 128, tslices + s * sstride + (size_t)c0 * 128,
+                    (uint32_t)(cn * 512), bar);
+      }
+      if (!mbar_wait_bounded(bar, phase)) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+      phase ^= 1;
+    }
+    epi_bar_sync();
+    const uint32_t ps_s = smem_u32(ps), os_s = smem_u32(os);
+#pragma unroll 1
+    for (int j0 = 0; j0 < cn; j0 += W) {
+      // own accumulator (slot 0), then the other slots in order; rows j0 .. j0+W-1
+      // stay inside the chunk's staging (ch is a multiple of W)
+      float v[W];
+      tmem_load_cols<W>(tl + (uint32_t)(c0 + j0), v);
+      for (int s = 0; s < S - 1; ++s) {
+        const uint32_t src = ps_s + (uint32_t)((((size_t)s * ch + j0) * 128 + r) * 4);
+        float p[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) p[j] = lds_f32(src + j * 512);
+#pragma unroll
+        for (int j = 0; j < W; ++j) v[j] += p[j];
+      }
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const uint32_t o = (uint32_t)((j0 + j) * 128 + r);
+        if (ob == 4) {
+          sts_f32(os_s + o * 4, v[j]);
+        } else {
+          float y = (v[j] + bias) * scale;
+          if (e.kind == EPI_RELU) y = fmaxf(y, 0.f);
+          const CT yc = from_f<CT>(y);
+          sts_u16(os_s + o * 2, *reinterpret_cast<const uint16_t *>(&yc));
+        }
+      }
+    }
+    epi_bar_sync();
+    if (go) {
+      const int cpr = 128 * ob / 16, per = 16 / ob;  // 16-byte groups per row, outputs per group
+      for (int q = et; q < cn * cpr; q += 128) {
+        const int jj = q / cpr, k = q - jj * cpr;
+        const int n = t * 128 + k * per;
+        if (n < N)
+          *reinterpret_cast<uint4 *>(tile_out_ptr<CT>(e, c0 + jj, n)) =
+              lds_u128(os_s + (uint32_t)((jj * 128 + k * per) * ob));
+      }
+    }
+    epi_bar_sync();  // the next chunk reuses the staging memory
+  }
+  if (go && S > 1 && et == 0) *cnt = 0;  // every other run of t has counted itself
+}
+
 }  // namespace he

@@ -4,6 +4,7 @@
 // restore copy.
 #include <type_traits>
 
+#include "../../include/he.h"
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -114,6 +115,88 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
   }
   __syncthreads();
   ln_store<PT, OT>(row, d, g, b, eps, h, (int)r, h_rows, red);
+}
+
+// Eight consecutive parameters (16-bit: one 16-byte load; fp32: two).
+template <typename PT>
+__device__ __forceinline__ void load8(const PT *p, float (&v)[8]) {
+  if constexpr (std::is_same<PT, float>::value) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const PT *e = reinterpret_cast<const PT *>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = to_f<PT>(e[i]);
+  }
+}
+
+template <typename OT>
+__device__ __forceinline__ void store8(OT *p, const float (&v)[8]) {
+  if constexpr (std::is_same<OT, float>::value) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    uint4 u;
+    OT *e = reinterpret_cast<OT *>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = from_f<OT>(v[i]);
+    *reinterpret_cast<uint4 *>(p) = u;
+  }
+}
+
+// k_resid_ln with the row held in registers: d / 8 threads (a multiple of 32),
+// thread t owns elements 8t .. 8t + 7, so the LN output leaves as one 16-byte
+// store into either layout of act_index (eight consecutive elements of a row stay
+// contiguous there).  Same arithmetic as k_resid_ln: slices summed in slot order,
+// then bias; mean, then the biased variance of the centred values.
+template <typename PT, typename OT>
+__global__ void k_resid_ln8(const float *partial, const SliceInfo si, long long split_stride,
+                            int ldp, const PT *bias, float *x, const PT *g, const PT *b, float eps,
+                            OT *h, int h_rows, int d) {
+  __shared__ float red[33];
+  const int c = 8 * threadIdx.x;
+  float bs[8], gs[8], bt[8];
+  load8<PT>(bias + c, bs);  // parameters do not depend on the kernel before this one
+  load8<PT>(g + c, gs);
+  load8<PT>(b + c, bt);
+  pdl_wait();
+  pdl_trigger();
+  const long long r = blockIdx.x;
+  float4 *xr = reinterpret_cast<float4 *>(x + r * d + c);
+  const float *pr = partial + r * ldp + c;
+  const int S = si.slices(c);
+  const float4 a0 = sum_slices(pr, S, split_stride);
+  const float4 a1 = sum_slices(pr + 4, S, split_stride);
+  float4 x0 = xr[0], x1 = xr[1];
+  x0.x += a0.x + bs[0];
+  x0.y += a0.y + bs[1];
+  x0.z += a0.z + bs[2];
+  x0.w += a0.w + bs[3];
+  x1.x += a1.x + bs[4];
+  x1.y += a1.y + bs[5];
+  x1.z += a1.z + bs[6];
+  x1.w += a1.w + bs[7];
+  xr[0] = x0;
+  xr[1] = x1;
+  float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s += v[i];
+  const float mean = block_sum(s, red) / (float)d;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] -= mean;
+    q += v[i] * v[i];
+  }
+  const float var = block_sum(q, red) / (float)d;
+  const float rstd = 1.0f / sqrtf(var + eps);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = v[i] * rstd * gs[i] + bt[i];
+  store8<OT>(h + act_index((int)r, c, d, h_rows), v);
 }
 
 // Element-wise epilogue after a split-K GEMM: four consecutive outputs per thread.
@@ -380,7 +463,15 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
   if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
     return cudaErrorInvalidValue;
   const size_t sm = (size_t)d * sizeof(float);
+  // 16-bit parameters: the register-resident variant (row of d / 8 threads).
+  const bool reg8 = dtype == HE_DTYPE_BF16 && d % 256 == 0 && d / 8 <= 1024 &&
+                    (uintptr_t)bias % 16 == 0 && (uintptr_t)g % 16 == 0 &&
+                    (uintptr_t)b % 16 == 0 && (uintptr_t)h % 16 == 0;
   HE_DISPATCH_PT_CT(dtype, out_act, {
+    if (reg8)
+      return launch_k(k_resid_ln8<PT, CT>, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si,
+                      split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
+                      (CT *)h, h_rows, d);
     return launch_k(k_resid_ln<PT, CT>, dim3(rows), dim3(row_threads(d)), sm, st, g_pdl, partial,
                     si, split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
                     (CT *)h, h_rows, d);

@@ -26,8 +26,14 @@ extern "C" {
  * (bf16, M <= 256, K % 64 == 0, N % 128 == 0 with tiled weights): the
  * (128-row tile, k-block) units are cut into P equal runs, P = -split if
  * split < 0 (at most min(units, 15 * tiles)), else the engine's choice (one per
- * SM); scratch needs 16 * M * N floats followed by R * K bf16 (R = M rounded up
- * to 16, 32, 64, 128 or 256) for the row-tiled copy of x that kernel reads.
+ * SM).  A tile split over several runs is finished inside the kernel by the run
+ * holding its first k-blocks, which adds the others' fp32 slices in slot order
+ * and stores y (N % 4 == 0 and y 16-byte aligned; otherwise a second kernel adds
+ * the slices).  scratch needs 16 * M * Np floats (Np = N rounded up to a
+ * multiple of 128) for the slices, then R * K bf16 (R = M rounded up to 16, 32,
+ * 64, 128 or 256) for the row-tiled copy of x that the kernel reads, then, from
+ * the next 16-byte boundary, Np / 128 ints of per-tile counters that the op
+ * clears itself before the kernel.
  * All pointers are device memory; asynchronous on `stream`. */
 he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
                        int M, int N, int K, int split, float *scratch, void *stream);
