@@ -279,24 +279,23 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[W]) {
   }
 }
 
-// Shared-memory accesses through a 32-bit shared-window address.
+// Shared-memory accesses through a 32-bit shared-window address.  No "memory"
+// clobber: callers order them against other threads and the async proxy with
+// barriers, and a clobber would make the compiler reload every kernel parameter
+// read by reference after each access.
 __device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
 __device__ __forceinline__ void sts_f32(uint32_t a, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-__device__ __forceinline__ void sts_u16(uint32_t a, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
 }
 __device__ __forceinline__ uint4 lds_u128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a)
-               : "memory");
+               : "r"(a));
   return v;
 }
 

@@ -262,8 +262,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
       // (all conditions below are uniform over the four epilogue warps)
       const bool staged = fix && slot == 0 && u + n == u_end &&
-                          tile_stage_tokens(S, a.M, W, tile_out_bytes(epi.kind, (int)sizeof(CT)),
-                                            kStageAvail) >= W;
+                          tile_stage_tokens(S, a.M, W, kStageAvail) >= W;
       if (staged) {
         tile_owner_epilogue<CT, W>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N,
                                    a.M, t, S, tl, live, &a.tile_cnt[t], base, kStageAvail,

@@ -260,31 +260,73 @@ __host__ __device__ inline int tile_out_bytes(int kind, int ct_bytes) {
 
 // Tokens of a tile that the staged reduction of the tile's owner handles at a
 // time in `avail` bytes of shared memory (a multiple of W; 0 if not even W fit):
-// per token, the S - 1 other slices' 128 fp32 values and the 128 outputs.
-__host__ __device__ inline int tile_stage_tokens(int S, int M, int W, int out_bytes, int avail) {
-  const int per_tok = (S - 1) * 512 + 128 * out_bytes;
+// per token, the S - 1 other slices' 128 fp32 values and the 128 fp32 outputs.
+__host__ __device__ inline int tile_stage_tokens(int S, int M, int W, int avail) {
+  const int per_tok = S * 512;
   int ch = avail / per_tok / W * W;
   const int m = (M + W - 1) / W * W;
   return ch < m ? ch : m;
 }
 
-// Address of the 16-byte group of outputs of token `tok` that starts at feature
-// n (a multiple of 16 / out_bytes) of the GEMM output, for an element-wise kind.
+// Where the outputs of feature n (and the following ones of its 16-byte group)
+// go, for any token: the part that depends on n only, computed once.
+struct TileOutRow {
+  char *base;                       // element of token 0 (kind 0 / 1) or the buffer (kind 2)
+  long long tok_stride, pos_stride;  // bytes
+  int kind;                         // 0 base + tok * tok_stride; 1 KV cache; 2 act_index layout
+  int tps, n, ldo, rows, esize;
+};
+
 template <typename CT>
-__device__ __forceinline__ void *tile_out_ptr(const Epi &e, int tok, int n) {
+__device__ __forceinline__ TileOutRow tile_out_row(const Epi &e, int n) {
+  TileOutRow o{};
+  o.n = n;
   switch (e.kind) {
     case EPI_QKV: {
       const int which = n / e.d_model, c = n - which * e.d_model;
-      if (which == 0) return static_cast<CT *>(e.out) + (long long)tok * e.ldo + c;
-      const int hh = c / e.head_dim, dd = c - hh * e.head_dim;
-      const int b = tok / e.tok_per_seq, p = tok - b * e.tok_per_seq;
-      return static_cast<CT *>(which == 1 ? e.kc : e.vc) +
-             (((long long)b * e.n_heads + hh) * e.max_seq + e.pos0 + p) * e.head_dim + dd;
+      o.esize = (int)sizeof(CT);
+      if (which == 0) {
+        o.kind = 0;
+        o.base = reinterpret_cast<char *>(static_cast<CT *>(e.out) + c);
+        o.tok_stride = (long long)e.ldo * sizeof(CT);
+      } else {
+        const int hh = c / e.head_dim, dd = c - hh * e.head_dim;
+        o.kind = 1;
+        o.base = reinterpret_cast<char *>(static_cast<CT *>(which == 1 ? e.kc : e.vc) +
+                                          ((long long)hh * e.max_seq + e.pos0) * e.head_dim + dd);
+        o.tok_stride = (long long)e.n_heads * e.max_seq * e.head_dim * sizeof(CT);
+        o.pos_stride = (long long)e.head_dim * sizeof(CT);
+        o.tps = e.tok_per_seq;
+      }
+      break;
     }
     case EPI_RELU:
-      return static_cast<CT *>(e.out) + act_index(tok, n, e.ldo, e.out_rows);
+      o.kind = 2;
+      o.esize = (int)sizeof(CT);
+      o.base = static_cast<char *>(e.out);
+      o.ldo = e.ldo;
+      o.rows = e.out_rows;
+      break;
     default:
-      return e.partial + (long long)tok * e.ldp + n;
+      o.kind = 0;
+      o.esize = 4;
+      o.base = reinterpret_cast<char *>(e.partial + n);
+      o.tok_stride = (long long)e.ldp * 4;
+      break;
+  }
+  return o;
+}
+
+__device__ __forceinline__ void *tile_out_ptr(const TileOutRow &o, int tok) {
+  switch (o.kind) {
+    case 0:
+      return o.base + tok * o.tok_stride;
+    case 1: {
+      const int b = tok / o.tps, p = tok - b * o.tps;
+      return o.base + b * o.tok_stride + p * o.pos_stride;
+    }
+    default:
+      return o.base + act_index(tok, o.n, o.ldo, o.rows) * o.esize;
   }
 }
 
@@ -296,8 +338,8 @@ __device__ __forceinline__ void *tile_out_ptr(const Epi &e, int tok, int n) {
 // last MMA, so the pipeline's shared memory `stage` (avail bytes) is free: per
 // chunk of ch tokens the other slices come in as one bulk copy each (completing
 // on the mbarrier `bar`), each thread adds its row's values in slot order (its own
-// slice is slot 0) and applies the epilogue into a [token][128] staging tile,
-// which then leaves as 16-byte stores.  `flag` is a shared int; returns with
+// slice is slot 0) and applies the epilogue into a [token][128] fp32 staging
+// tile, which then leaves (rounded to the output type) as 16-byte stores.  `flag` is a shared int; returns with
 // every epilogue thread past the same barriers.
 template <typename CT, int W>
 __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *tslices,
@@ -332,9 +374,10 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
   epi_bar_sync();
   const bool go = *flag != 0;
   const int ob = tile_out_bytes(e.kind, (int)sizeof(CT));
-  const int ch = tile_stage_tokens(S, M, W, ob, avail);
-  float *ps = reinterpret_cast<float *>(stage);                 // [S-1][ch][128]
-  uint8_t *os = stage + (size_t)(S - 1) * ch * 512;             // [ch][128] outputs
+  const bool relu = e.kind == EPI_RELU;
+  const int ch = tile_stage_tokens(S, M, W, avail);
+  float *ps = reinterpret_cast<float *>(stage);      // [S-1][ch][128] other slices
+  uint8_t *os = stage + (size_t)(S - 1) * ch * 512;  // [ch][128] fp32 outputs
   uint32_t phase = 0;
   for (int c0 = 0; c0 < M; c0 += ch) {
     const int cn = min(ch, M - c0);
@@ -368,26 +411,41 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
       }
 #pragma unroll
       for (int j = 0; j < W; ++j) {
-        const uint32_t o = (uint32_t)((j0 + j) * 128 + r);
-        if (ob == 4) {
-          sts_f32(os_s + o * 4, v[j]);
-        } else {
-          float y = (v[j] + bias) * scale;
-          if (e.kind == EPI_RELU) y = fmaxf(y, 0.f);
-          const CT yc = from_f<CT>(y);
-          sts_u16(os_s + o * 2, *reinterpret_cast<const uint16_t *>(&yc));
+        float y = v[j];
+        if (ob != 4) {
+          y = (y + bias) * scale;
+          if (relu) y = fmaxf(y, 0.f);
         }
+        sts_f32(os_s + (uint32_t)(((j0 + j) * 128 + r) * 4), y);
       }
     }
     epi_bar_sync();
     if (go) {
-      const int cpr = 128 * ob / 16, per = 16 / ob;  // 16-byte groups per row, outputs per group
-      for (int q = et; q < cn * cpr; q += 128) {
-        const int jj = q / cpr, k = q - jj * cpr;
-        const int n = t * 128 + k * per;
-        if (n < N)
-          *reinterpret_cast<uint4 *>(tile_out_ptr<CT>(e, c0 + jj, n)) =
-              lds_u128(os_s + (uint32_t)((jj * 128 + k * per) * ob));
+      // 16-byte output groups (4 fp32 values, or 8 values rounded to CT): thread et
+      // always takes group et % cpr of rows et / cpr, et / cpr + 128 / cpr, ...
+      const int per = 16 / ob, cpr = 128 / per;
+      const int k = et % cpr, n = t * 128 + k * per;
+      if (n < N) {
+        const TileOutRow orow = tile_out_row<CT>(e, n);
+        for (int jj = et / cpr; jj < cn; jj += 128 / cpr) {
+          const uint32_t src = os_s + (uint32_t)((jj * 128 + k * per) * 4);
+          uint4 o = lds_u128(src);
+          if (ob != 4) {
+            const uint4 hi = lds_u128(src + 16);
+            const float f[8] = {__uint_as_float(o.x),  __uint_as_float(o.y),
+                                __uint_as_float(o.z),  __uint_as_float(o.w),
+                                __uint_as_float(hi.x), __uint_as_float(hi.y),
+                                __uint_as_float(hi.z), __uint_as_float(hi.w)};
+            union {
+              uint4 u;
+              CT c[8];
+            } pk;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk.c[i] = from_f<CT>(f[i]);
+            o = pk.u;
+          }
+          *reinterpret_cast<uint4 *>(tile_out_ptr(orow, c0 + jj)) = o;
+        }
       }
     }
     epi_bar_sync();  // the next chunk reuses the staging memory
