@@ -192,6 +192,194 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Persistent variant for many tiles (prefill: every prompt token at once).  One
+// CTA per SM walks the (128-feature, 256-token) tiles c, c + P, c + 2P, ... in an
+// order that groups kTokGroup token tiles, so the tiles in flight at one time
+// share operands in L2 (about 19 weight tiles x 8 token tiles per wave).  Two
+// TMEM accumulators (2 x 256 columns): the epilogue of one tile runs while the
+// MMAs of the next one accumulate, and the load ring never drains between tiles.
+// ---------------------------------------------------------------------------
+constexpr int PBN = 256, PSTAGES = 4, kTokGroup = 8;
+
+__host__ __device__ inline void tcp_tile(long long L, int MT, int NT, int *mt, int *nt) {
+  const long long gsz = (long long)kTokGroup * MT;
+  const long long g = L / gsz, rem = L - g * gsz;
+  const int gnt = min(kTokGroup, NT - (int)g * kTokGroup);  // the last group may be narrower
+  *mt = (int)(rem / gnt);
+  *nt = (int)g * kTokGroup + (int)(rem % gnt);
+}
+
+template <typename CT, bool ABULK>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_tcp(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
+               int tiles_per_group, int M, int N, int kb_total, int MT, int NT,
+               const __grid_constant__ Epi epi, WTiles wt, int *dev_err) {
+  using C = Cfg<PBN, PSTAGES>;
+  constexpr uint32_t kCols = 2 * PBN;  // two accumulators
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t *smA = base;
+  uint8_t *smB = base + PSTAGES * A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + PSTAGES * C::STAGE_BYTES);
+  uint64_t *empty = full + PSTAGES;
+  uint64_t *acc_full = empty + PSTAGES;  // [2]
+  uint64_t *acc_empty = acc_full + 2;    // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = gridDim.x, c = blockIdx.x;
+  const long long T = (long long)MT * NT;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 4 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    if (!ABULK) {
+      prefetch_tmap(&tm_w0);
+      prefetch_tmap(&tm_w1);
+      prefetch_tmap(&tm_w2);
+    }
+    prefetch_tmap(&tm_x);
+    pdl_wait();  // the activations come from the kernel before this one
+    long long it = 0, issued = 0;
+    bool stop = false;
+    for (long long L = c; L < T && !stop; L += P) {
+      int mt, nt;
+      tcp_tile(L, MT, NT, &mt, &nt);
+      const int group = mt / tiles_per_group;
+      const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
+      const int m_row = (mt - group * tiles_per_group) * BM;
+      const uint16_t *wtile =
+          ABULK ? wt.p[group] + (long long)(m_row / BM) * wt.kt * (BM * BK) : nullptr;
+      for (int kb = 0; kb < kb_total; ++kb, ++it) {
+        const int s = (int)(it % PSTAGES);
+        if (it >= PSTAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((it / PSTAGES - 1) & 1))) {
+          *(volatile int *)abort_flag = 1;
+          set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+          stop = true;
+          break;
+        }
+        if (*(volatile int *)abort_flag) {
+          stop = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        if (ABULK)
+          bulk_load(smA + s * A_BYTES, wtile + (long long)kb * (BM * BK), A_BYTES, &full[s]);
+        else
+          tma_load_2d(smA + s * A_BYTES, tw, &full[s], kb * BK, m_row);
+        tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kb * BK, nt * PBN);
+        issued = it + 1;
+      }
+    }
+    // the last load issued into each stage must have landed before exit
+    for (long long i = issued > PSTAGES ? issued - PSTAGES : 0; i < issued; ++i)
+      if (!mbar_wait_bounded(&full[i % PSTAGES], (uint32_t)((i / PSTAGES) & 1)))
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+  } else if (warp == 5 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_f16kind<CT>(PBN);
+    long long it = 0;
+    int tcount = 0;
+    bool ok = true;
+    for (long long L = c; L < T && ok; L += P, ++tcount) {
+      const int buf = tcount & 1;
+      if (tcount >= 2 &&
+          !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((tcount >> 1) - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc = tmem_base + (uint32_t)(buf * PBN);
+      for (int kb = 0; kb < kb_total; ++kb, ++it) {
+        const int s = (int)(it % PSTAGES);
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((it / PSTAGES) & 1)) ||
+            *(volatile int *)abort_flag) {
+          *(volatile int *)abort_flag = 1;
+          set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smA + s * A_BYTES);
+        const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+          tc_mma_f16(acc, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
+                     idesc, (kb | kk) != 0);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
+    }
+  } else if (warp < 4) {
+    // ---------------- epilogue ----------------
+    pdl_wait();  // outputs may still be read by the kernel before this one
+    constexpr int W = 32;
+    const bool part = epi.kind == EPI_PARTIAL;
+    int tcount = 0;
+    for (long long L = c; L < T; L += P, ++tcount) {
+      if (*(volatile int *)abort_flag) break;
+      int mt, nt;
+      tcp_tile(L, MT, NT, &mt, &nt);
+      const int buf = tcount & 1;
+      const bool ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)((tcount >> 1) & 1));
+      if (!ok) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+      }
+      tc_fence_after();
+      const bool live = ok && !*(volatile int *)abort_flag;
+      const int row = mt * BM + warp * 32 + lane;  // output feature n
+      const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * PBN);
+      const RowEpi<CT> re = row_epi_prepare<CT>(epi, row < N ? row : 0,
+                                                part ? epi.partial : nullptr, epi.split_stride,
+                                                0, epi.ldp);
+      const int tok_base = nt * PBN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < PBN; c0 += W) {
+        float v[W];
+        tmem_load_cols<W>(tl + c0, v);
+        if (live && row < N && tok_base + c0 < M)
+          row_epi_store<CT, W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side: tensor maps and launch.
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -261,6 +449,45 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
                   dev_err);
 }
 
+template <typename CT, bool ABULK>
+cudaError_t launch_tcp(const GemmArgs &a, int num_sms, int *dev_err, cudaStream_t st) {
+  using C = Cfg<PBN, PSTAGES>;
+  CUtensorMap tw[3], tx;
+  WTiles wt{};
+  memset(tw, 0, sizeof tw);
+  for (int g = 0; g < 3; ++g) {
+    const void *p = a.w[g < a.n_groups ? g : 0];
+    if (ABULK)
+      wt.p[g] = static_cast<const uint16_t *>(p);
+    else if (!make_tmap(&tw[g], p, a.group_rows, a.K, a.K, BM, tmap_type<CT>()))
+      return cudaErrorInvalidValue;
+  }
+  wt.kt = a.K / BK;
+  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, PBN, tmap_type<CT>())) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<CT, ABULK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int kb_total = (a.K + BK - 1) / BK;
+  const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
+  const int MT = a.N / BM + (a.N % BM != 0), NT = (a.M + PBN - 1) / PBN;
+  const long long T = (long long)MT * NT;
+  const int P = (int)(T < num_sms ? T : num_sms);
+  return launch_k(k_gemm_tcp<CT, ABULK>, dim3(P), dim3(192), C::SMEM, st, g_pdl, tw[0], tw[1],
+                  tw[2], tx, tiles_per_group, a.M, a.N, kb_total, MT, NT, a.epi, wt, dev_err);
+}
+
+int device_sms() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev];
+}
+
 }  // namespace
 
 bool make_tmap_16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_rows,
@@ -285,8 +512,14 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
     for (int g = 0; g < a.n_groups; ++g)
       if ((uintptr_t)a.w[g] % 16) return cudaErrorInvalidValue;
   }
+  // many token tiles and no split: the persistent kernel
+  const int sms = device_sms();
+  const bool persist = a.split == 1 && a.M > PBN && sms > 0;
   auto pick = [&](auto ct) -> cudaError_t {
     using CT = decltype(ct);
+    if (persist)
+      return a.w_tiled ? launch_tcp<CT, true>(a, sms, dev_err, st)
+                       : launch_tcp<CT, false>(a, sms, dev_err, st);
     if (a.w_tiled) {
       if (a.M <= 16) return launch_bn<CT, 16, 10, true>(a, dev_err, st);
       if (a.M <= 32) return launch_bn<CT, 32, 9, true>(a, dev_err, st);

@@ -8,9 +8,13 @@ generation path the way a decode step does, for profiling one kernel at a time:
 * attn_decode: one decode-attention launch, B=128, 40 heads of 128, 384 cached
   keys (1.0 GB of K and V, above the 126 MB L2);
 * gemm_sk: the fc1 projection, 128 tokens x 5120 -> 20480, tiled weights,
-  stream-K over one CTA per SM (210 MB of weights, two copies alternated).
+  stream-K over one CTA per SM (210 MB of weights, two copies alternated);
+* gemm_prefill: the fc1 projection of a prefill, 32768 tokens (128 prompts of
+  256) x 5120 -> 20480, tiled weights, the persistent tensor-core kernel
+  (fp32 output, 3.3 GB in all).
 
-Prints the CUDA-event time per launch and the algorithmic GB/s.
+Prints the CUDA-event time per launch and the algorithmic GB/s (TFLOP/s for
+the prefill GEMM).
 """
 from __future__ import annotations
 
@@ -55,9 +59,20 @@ def gemm_sk(iters):
           f"{ms * 1e3:.1f} us/call, {N * K * 2 / (ms / 1e3) / 1e9:.0f} GB/s of weights")
 
 
+def gemm_prefill(iters):
+    M, N, K = 32768, 20480, 5120
+    w = torch.randn(N, K, device="cuda").to(torch.bfloat16)
+    wt = he.tile_weight(w)
+    x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    ms = _time(lambda i: he.linear(x, w, split=1, w_tiled=wt), iters)
+    print(f"gemm_prefill M={M} N={N} K={K}: {ms * 1e3:.1f} us/call, "
+          f"{2 * M * N * K / (ms / 1e3) / 1e12:.0f} TFLOP/s")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", nargs="?", default="all", choices=["attn_decode", "gemm_sk", "all"])
+    ap.add_argument("case", nargs="?", default="all",
+                    choices=["attn_decode", "gemm_sk", "gemm_prefill", "all"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
@@ -65,6 +80,8 @@ def main():
         attn_decode(args.iters)
     if args.case in ("gemm_sk", "all"):
         gemm_sk(args.iters)
+    if args.case in ("gemm_prefill", "all"):
+        gemm_prefill(args.iters)
 
 
 if __name__ == "__main__":

@@ -21,7 +21,7 @@ def _bound(x, w, K):
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (3, 256, 8), (16, 384, 768), (17, 200, 136),
                                    (100, 640, 1024), (129, 128, 520), (300, 1000, 256),
-                                   (513, 384, 64)])
+                                   (513, 384, 64), (4133, 2560, 320)])
 def test_linear_16bit_tcgen05_matches_exact(cuda_device, M, N, K, dt):
     g = torch.Generator().manual_seed(M * 7919 + N * 31 + K)
     x = torch.randn(M, K, generator=g).to(dt).cuda()
@@ -101,7 +101,8 @@ def test_tile_weight_layout(cuda_device, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,split", [(1, 128, 64, 1), (17, 384, 512, 1), (128, 1280, 1024, 1),
-                                         (128, 256, 2048, 4), (300, 256, 640, 1), (64, 640, 1280, 5)])
+                                         (128, 256, 2048, 4), (300, 256, 640, 1), (64, 640, 1280, 5),
+                                         (4133, 2560, 192, 1)])
 def test_linear_bf16_tiled_weights(cuda_device, M, N, K, split):
     g = torch.Generator().manual_seed(M + 3 * N + 7 * K)
     x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
