@@ -348,7 +348,14 @@ def main():
                             "bytes_per_launch": byts / n if n else None, "gbs": ach}
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
     pk = per_kernel[dom]
-    traffic = None
+    # DRAM bytes (read + write) per launch, scaled from one ncu capture of the kernel
+    # (summaries under profiles/) by the ratio of measured to algorithmic bytes of the
+    # captured launch: k_attn_decode at B=128, 40 heads, 384 keys (the average decode
+    # launch here) and k_gemm_sk on the fc1 shape.  Set to None when the kernel changes.
+    traffic_ratio = {"attn_decode": (1.007986e9 + 4.340736e6) / 1.00663296e9,
+                     "gemm": (211.114496e6 + 6.177024e6) / 209.7152e6}
+    traffic = (pk["bytes_per_launch"] * traffic_ratio[dom]
+               if pk["bytes_per_launch"] and dom in traffic_ratio else None)
     roofline = {"bound": "hbm",
                 "kernel": "k_attn_decode" if dom == "attn_decode" else "k_gemm_sk (decode projections)",
                 "achieved": pk["gbs"], "peak": hbm_peak, "unit": "GB/s",
