@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(128)
   const T *vb = vc + row0 * HD + li * VEC;
 
   pdl_wait();
+  // The next kernel (the out projection) may launch once every CTA of this grid has
+  // started, i.e. during the last wave: its CTAs take SMs as these finish, set up and
+  // prefetch weights, and wait for this grid to complete before reading its output.
+  pdl_trigger();
   float qv[VEC];
   Vec16<T>::load(q + ((long long)b * H + h) * HD + li * VEC, qv);
   float m = -INFINITY, l = 0.f, o[VEC];
@@ -153,7 +157,6 @@ __global__ void __launch_bounds__(128)
       }
     }
   }
-  pdl_trigger();  // many waves: the next kernel starts launching as the last ones finish
 }
 
 template <typename T, int HD>
