@@ -21,6 +21,7 @@ _LIB_PATH = Path(__file__).resolve().parent / "libhe.so"
 HE_OK, HE_ERR_ARG, HE_ERR_STATE, HE_ERR_OOM = 0, -1, -2, -3
 HE_ERR_CUDA, HE_ERR_UNSUPPORTED, HE_ERR_DEVICE_CHECK = -4, -5, -6
 HE_DTYPE_F32, HE_DTYPE_BF16, HE_DTYPE_F16 = 0, 1, 2
+HE_PROJ_Q, HE_PROJ_K, HE_PROJ_V, HE_PROJ_O, HE_PROJ_FC1, HE_PROJ_FC2 = range(6)
 PROJ = ("wq", "wk", "wv", "wo", "w1", "w2")
 BIAS = ("bq", "bk", "bv", "bo", "b1", "b2")
 KCLASS = ("gemm", "attn_decode", "norm", "head", "prefill_gemm", "prefill_attn", "other", "spare")
@@ -75,6 +76,7 @@ _SIGNATURES = {
     "he_destroy": (c_int, [c_void_p]),
     "he_fuse_lora": (c_int, [c_void_p, c_void_p]),
     "he_unfuse_lora": (c_int, [c_void_p, c_void_p]),
+    "he_read_fused_weight": (c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "he_generate": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "he_generate_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
@@ -229,6 +231,22 @@ class Engine:
 
     def unfuse_lora(self, stream=None):
         _check(self._lib.he_unfuse_lora(self._h, self._s(stream)))
+
+    def read_fused_weight(self, layer: int, proj: int, stream=None):
+        """Projection `proj` (HE_PROJ_*) of `layer` as generation reads it while fused:
+        the merged fp32 weight [out][in] (fp32 engines) or the flat fp16 tiled copy
+        (bf16 engines, he_op_tile_weight's element order)."""
+        import torch
+        c = self.cfg
+        rows = c.ffn if proj == HE_PROJ_FC1 else c.d_model
+        cols = c.ffn if proj == HE_PROJ_FC2 else c.d_model
+        if c.dtype == "f32":
+            out = torch.empty((rows, cols), dtype=torch.float32, device=self.device)
+        else:
+            out = torch.empty(rows * cols, dtype=torch.float16, device=self.device)
+        _check(self._lib.he_read_fused_weight(self._h, layer, proj, out.data_ptr(),
+                                              out.numel() * out.element_size(), self._s(stream)))
+        return out
 
     def release_workspace(self, stream=None):
         _check(self._lib.he_release_workspace(self._h, self._s(stream)))

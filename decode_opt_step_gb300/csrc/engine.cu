@@ -67,6 +67,9 @@ struct he_engine {
   size_t elem = 4;
   const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_g = nullptr, *lnf_b = nullptr;
   std::vector<he_layer_weights> layers;
+  // BF16 while fused: the merged fp16 projections in the tiled layout, one per
+  // (layer, projection), inside `restore`; generation reads these instead of w[]
+  std::vector<const void *> fused_w;
   he_allocator alloc{};
 
   bool taken = false, fused = false;
@@ -333,7 +336,9 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   // embedding table: that output is written in the parameter type
   const int out_act = l == cf.n_layers - 1 ? cf.dtype : act;
   // LN1 + QKV (+ KV append at the tokens' positions)
-  const void *wqkv[3] = {lw.w[HE_PROJ_Q], lw.w[HE_PROJ_K], lw.w[HE_PROJ_V]};
+  // projections as generation reads them: the fused copies while fused on BF16
+  auto W = [&](int p) { return tw ? h->fused_w[(size_t)l * HE_N_PROJ + p] : lw.w[p]; };
+  const void *wqkv[3] = {W(HE_PROJ_Q), W(HE_PROJ_K), W(HE_PROJ_V)};
   gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw, act);
   Epi ep{};
   ep.kind = EPI_PARTIAL;
@@ -355,7 +360,7 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
             split > 1 ? 2 : 1);
   }
   // out projection -> partials; + bo + residual; LN2
-  const void *wo[1] = {lw.w[HE_PROJ_O]};
+  const void *wo[1] = {W(HE_PROJ_O)};
   SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw, act);
   {
     Timed t(h, HE_KCLASS_NORM, c.st);
@@ -371,10 +376,10 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   er.out = h->mid.p;
   er.ldo = cf.ffn;
   er.out_rows = R;
-  const void *w1[1] = {lw.w[HE_PROJ_FC1]};
+  const void *w1[1] = {W(HE_PROJ_FC1)};
   gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw, act);
   // fc2 -> partials; + b2 + residual; next LN
-  const void *w2[1] = {lw.w[HE_PROJ_FC2]};
+  const void *w2[1] = {W(HE_PROJ_FC2)};
   si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw, act);
   const bool last = l == cf.n_layers - 1;
   const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
@@ -662,11 +667,12 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
     for (int p = 0; p < HE_N_PROJ; ++p)
       if (fuse_touches(h, p)) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
   if (!get(h, h->restore, total, st))
-    return fail(HE_ERR_OOM, "LoRA restore copy of %zu bytes failed", total);
+    return fail(HE_ERR_OOM, "LoRA fuse buffer of %zu bytes failed", total);
   ensure_phase_events(h);
   cudaEventRecord(h->ph[3], st);
   const float scale = c.lora_targets ? c.lora_alpha / (float)c.lora_r : 0.f;
   const bool bf = c.dtype == HE_DTYPE_BF16;
+  h->fused_w.assign((size_t)c.n_layers * HE_N_PROJ, nullptr);
   size_t off = 0;
   cudaError_t err = cudaSuccess;
   auto chk = [&](cudaError_t e, int n) {
@@ -681,12 +687,12 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
       void *save = at(h->restore.p, off);
       const bool lora = (c.lora_targets >> p) & 1u;
       if (bf) {
-        // save the original bits, then write the merged weight tiled from the copy
-        chk(launch_copy(save, lw.w[p], bytes, st), bytes % 16 ? 2 : 1);
-        chk(launch_fuse_tiled(lw.w[p], ACT_F16, save, lora ? lw.lora_a[p] : nullptr,
+        // the merged weight, tiled, into the engine's buffer; w[] stays as it is
+        chk(launch_fuse_tiled(save, ACT_F16, lw.w[p], lora ? lw.lora_a[p] : nullptr,
                               lora ? lw.lora_b[p] : nullptr, rows_of(p), cols_of(p), c.lora_r,
                               scale, st),
             1);
+        h->fused_w[(size_t)l * HE_N_PROJ + p] = save;
       } else {
         chk(launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p], save, rows_of(p),
                              cols_of(p), c.lora_r, scale, st),
@@ -704,6 +710,25 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
   return HE_OK;
 }
 
+he_status he_read_fused_weight(he_engine *h, int layer, int proj, void *dst, size_t bytes,
+                               void *stream) {
+  g_err.clear();
+  if (!h || !dst) return fail(HE_ERR_ARG, "NULL argument");
+  if (!h->fused) return fail(HE_ERR_STATE, "LoRA is not fused");
+  const he_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || proj < 0 || proj >= HE_N_PROJ)
+    return fail(HE_ERR_ARG, "bad layer or projection");
+  const size_t rows = proj == HE_PROJ_FC1 ? c.ffn : c.d_model;
+  const size_t cols = proj == HE_PROJ_FC2 ? c.ffn : c.d_model;
+  if (bytes != rows * cols * h->elem) return fail(HE_ERR_ARG, "bytes must be %zu", rows * cols * h->elem);
+  cudaSetDevice(h->device);
+  const void *src = h->tiled ? h->fused_w[(size_t)layer * HE_N_PROJ + proj] : h->layers[layer].w[proj];
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "he_read_fused_weight");
+  return HE_OK;
+}
+
 he_status he_unfuse_lora(he_engine *h, void *stream) {
   g_err.clear();
   if (!h) return fail(HE_ERR_ARG, "engine is NULL");
@@ -717,18 +742,21 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
   cudaEventRecord(h->ph[5], st);
   size_t off = 0;
   cudaError_t err = cudaSuccess;
-  for (int l = 0; l < c.n_layers; ++l)
-    for (int p = 0; p < HE_N_PROJ; ++p) {
-      if (!fuse_touches(h, p)) continue;
-      const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
-      cudaError_t e = launch_copy(h->layers[l].w[p], at(h->restore.p, off), bytes, st);
-      if (e != cudaSuccess && err == cudaSuccess) err = e;
-      h->stats.launches += (bytes % 16 ? 2 : 1);
-      off += bytes;
-    }
+  if (c.dtype != HE_DTYPE_BF16) {  // BF16 never wrote w[]: releasing the buffer is all
+    for (int l = 0; l < c.n_layers; ++l)
+      for (int p = 0; p < HE_N_PROJ; ++p) {
+        if (!fuse_touches(h, p)) continue;
+        const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
+        cudaError_t e = launch_copy(h->layers[l].w[p], at(h->restore.p, off), bytes, st);
+        if (e != cudaSuccess && err == cudaSuccess) err = e;
+        h->stats.launches += (bytes % 16 ? 2 : 1);
+        off += bytes;
+      }
+  }
   cudaEventRecord(h->ph[6], st);
   h->unfuse_pending = true;
   put(h, h->restore, st);
+  h->fused_w.clear();
   h->fused = false;
   h->tiled = false;
   h->stats.restore_bytes = 0;

@@ -241,10 +241,18 @@ __global__ void __launch_bounds__(192, 1)
     // pipeline's shared memory, free after the CTA's last MMA.  Without
     // a.tile_cnt, tiles of one run are stored directly and the others are left as
     // slices for a second kernel.
-    pdl_wait();  // outputs may still be read by the kernel before this one
     const bool fix = a.tile_cnt != nullptr && epi.kind != EPI_PARTIAL;
     constexpr int W = BN >= 32 ? 32 : 16;
     constexpr int kStageAvail = STAGES * C::STAGE_BYTES;
+    // The bias of this thread's row in the tile of the last segment (the one an
+    // owner finishes at the end of the run), read before waiting on the kernel
+    // before this one: parameters do not depend on it.
+    float last_bias = 0.f;
+    if (fix && u_end > u_begin) {
+      const int t_last = (int)((u_end - 1) / a.KB);
+      last_bias = tile_row_bias(epi, t_last * BM + warp * 32 + lane, a.N);
+    }
+    pdl_wait();  // outputs may still be read by the kernel before this one
     int seg = 0;
     for (long long u = u_begin; u < u_end;) {
       const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
       if (staged) {
         tile_owner_epilogue<CT, W>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N,
                                    a.M, t, S, tl, live, &a.tile_cnt[t], base, kStageAvail,
-                                   fix_bar, last_flag, dev_err);
+                                   fix_bar, last_flag, dev_err, last_bias);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);

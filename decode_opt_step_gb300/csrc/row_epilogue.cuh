@@ -330,6 +330,17 @@ __device__ __forceinline__ void *tile_out_ptr(const TileOutRow &o, int tok) {
   }
 }
 
+// Bias of output feature n for an element-wise epilogue (0 past N or without one).
+__device__ __forceinline__ float tile_row_bias(const Epi &e, int n, int N) {
+  if (n >= N) return 0.f;
+  if (e.kind == EPI_RELU) return __bfloat162float(static_cast<const bf16 *>(e.bias[0])[n]);
+  if (e.kind == EPI_QKV) {
+    const int which = n / e.d_model;
+    return __bfloat162float(static_cast<const bf16 *>(e.bias[which])[n - which * e.d_model]);
+  }
+  return 0.f;
+}
+
 // Final epilogue of stream-K tile t by its owner (the run holding the tile's first
 // k-blocks, whose accumulator is in TMEM at `tl` for this thread's row), with the
 // other S - 1 runs' fp32 slices in global memory (tile-contiguous: tslices +
@@ -339,27 +350,20 @@ __device__ __forceinline__ void *tile_out_ptr(const TileOutRow &o, int tok) {
 // chunk of ch tokens the other slices come in as one bulk copy each (completing
 // on the mbarrier `bar`), each thread adds its row's values in slot order (its own
 // slice is slot 0) and applies the epilogue into a [token][128] fp32 staging
-// tile, which then leaves (rounded to the output type) as 16-byte stores.  `flag` is a shared int; returns with
+// tile, which then leaves (rounded to the output type) as 16-byte stores.  `bias`
+// is this thread's row's (tile_row_bias).  `flag` is a shared int; returns with
 // every epilogue thread past the same barriers.
 template <typename CT, int W>
 __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *tslices,
                                                     long long sstride, int N, int M, int t, int S,
                                                     uint32_t tl, bool live, int *cnt,
                                                     uint8_t *stage, int avail, uint64_t *bar,
-                                                    int *flag, int *dev_err) {
+                                                    int *flag, int *dev_err, float bias) {
   const int et = threadIdx.x, r = et;  // r: this thread's row (feature) of the tile
   const int n_row = t * 128 + r;
-  // per-row epilogue constants (parameters: read while the other runs finish)
-  float bias = 0.f, scale = 1.f;
-  if (n_row < N) {
-    if (e.kind == EPI_RELU) {
-      bias = __bfloat162float(static_cast<const bf16 *>(e.bias[0])[n_row]);
-    } else if (e.kind == EPI_QKV) {
-      const int which = n_row / e.d_model;
-      bias = __bfloat162float(static_cast<const bf16 *>(e.bias[which])[n_row - which * e.d_model]);
-      if (which == 0) scale = e.q_scale;
-    }
-  }
+  // per-row epilogue constants (`bias`, this row's, was read by the caller)
+  float scale = 1.f;
+  if (n_row < N && e.kind == EPI_QKV && n_row < e.d_model) scale = e.q_scale;
   epi_bar_sync();  // *flag may still be read from an earlier segment
   if (et == 0) {
     // acquire: the other runs' slices (written, fenced, then counted) are visible

@@ -97,7 +97,8 @@ typedef struct {
 /* One decoder layer.  Projections are [out][in] row-major (y = x W^T + b):
  * Wq, Wk, Wv, Wo: [d][d]; W1: [ffn][d]; W2: [d][ffn].  All tensors have the
  * config's dtype and are caller-owned device memory that must stay valid until
- * he_destroy.  w[] is written in place by he_fuse_lora / he_unfuse_lora. */
+ * he_destroy.  F32 engines write w[] in place in he_fuse_lora / he_unfuse_lora;
+ * BF16 engines never write it. */
 typedef struct {
   void *w[HE_N_PROJ];            /* indexed by HE_PROJ_* */
   const void *b[HE_N_PROJ];      /* biases [out] */
@@ -130,7 +131,7 @@ typedef struct {
   long long generate_calls;
   size_t workspace_bytes;        /* KV cache + scratch currently held */
   size_t kv_bytes;               /* KV cache part of it */
-  size_t restore_bytes;          /* LoRA restore copy currently held */
+  size_t restore_bytes;          /* held by he_fuse_lora (restore copy or fused buffer) */
   /* Per-kernel-class device time of the last he_generate, filled only while
    * profiling is on (he_set_profiling); index by HE_KCLASS_*. */
   double kclass_ms[8];
@@ -158,23 +159,34 @@ he_status he_create(const he_config *cfg, const he_weights *w, const he_allocato
                     int device, he_engine **out);
 
 /* Frees everything the engine holds (restoring fused weights first is the
- * caller's job: destroying a fused engine leaves the weights fused).  NULL is a no-op. */
+ * caller's job: destroying a fused F32 engine leaves its weights fused).  NULL is
+ * a no-op. */
 he_status he_destroy(he_engine *h);
 
-/* [DSC-lora], [HE-guide]: saves the bits of the projections, then writes the
- * merged weight W + (alpha/r) * B A (fp32 arithmetic) in place.  F32: the
- * targeted projections, round to nearest.  BF16: all six projections of every
- * layer are rewritten as fp16 (round to nearest even; OPT's native precision and
- * the pages' hybrid-engine test config, fp16.enabled) in the tiled streaming
- * layout of he_ops.h, merged where LoRA-targeted.  While fused the weight
- * tensors hold that representation; he_unfuse_lora restores the original bits.
- * HE_ERR_STATE if already fused; the restore copy is taken through the
- * allocator (HE_ERR_OOM leaves the engine unfused and the weights untouched). */
+/* [DSC-lora], [HE-guide]: the merged weight W + (alpha/r) * B A (fp32
+ * arithmetic) for generation.  F32: saves the bits of the targeted projections,
+ * then writes the merged weight in place (round to nearest).  BF16: all six
+ * projections of every layer, merged where LoRA-targeted, are written as fp16
+ * (round to nearest even; the pages' hybrid-engine test config runs with
+ * fp16.enabled) in the tiled streaming layout of he_ops.h into a buffer of the
+ * same size as those projections, taken through the allocator; w[] is not
+ * written, and generation reads that buffer while fused.  HE_ERR_STATE if
+ * already fused; HE_ERR_OOM (from the allocator) leaves the engine unfused and
+ * the weights untouched. */
 he_status he_fuse_lora(he_engine *h, void *stream);
 
-/* Restores the saved bits of every targeted projection (bit-exact) and frees
- * the restore copy.  HE_ERR_STATE if not fused. */
+/* F32: restores the saved bits of every targeted projection (bit-exact).  Both
+ * dtypes: frees the buffer he_fuse_lora took.  HE_ERR_STATE if not fused. */
 he_status he_unfuse_lora(he_engine *h, void *stream);
+
+/* Copies projection `proj` of `layer` as generation reads it while fused into
+ * dst (device, `bytes` = rows * cols * element size of the config's dtype): the
+ * merged weight in place for F32, the fp16 tiled copy for BF16 (element layout
+ * of he_op_tile_weight, 2-byte elements).  For tests and inspection.
+ * HE_ERR_STATE if not fused, HE_ERR_ARG for a bad layer, projection or size.
+ * Asynchronous on `stream`. */
+he_status he_read_fused_weight(he_engine *h, int layer, int proj, void *dst, size_t bytes,
+                               void *stream);
 
 /* [DSC-gen], [DSC-kv], [RLHF-ch11]: greedy generation of Lgen tokens for B
  * prompts of Lp tokens.  prompt_ids: device int32 [B][Lp], every id in
