@@ -44,9 +44,12 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // Sum over the block; every thread gets the result.  `red` holds >= 33 floats.
-// Barrier 1 over the four epilogue warps (threads 0..127) of a warp-specialised
+// Barrier 1 over the NT epilogue threads (threads 0..NT-1) of a warp-specialised
 // tcgen05 kernel; the other warps never use it.
-__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
 __device__ __forceinline__ float block_sum(float v, float *red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;

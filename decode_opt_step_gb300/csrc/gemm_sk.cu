@@ -18,10 +18,10 @@
 // partial[slot][tile][tok][128], so each arrives as one bulk copy.  A tile
 // covered by a single segment gets the element-wise epilogue directly.
 //
-// Warp roles (192 threads): warps 0-3 epilogue (warp w reads TMEM lanes
-// 32w..32w+31), warp 4 loads (per stage one bulk copy of KPS tiled 128 x 64
+// Warp roles (320 threads): warps 0-7 epilogue (warp w reads TMEM lanes
+// 32 (w % 4) .. +31, warps w and w + 4 splitting the token columns), warp 8 loads (per stage one bulk copy of KPS tiled 128 x 64
 // weight tiles, or KPS TMA boxes of row-major weights, plus one bulk copy of the
-// KPS row-tiled activation k-blocks), warp 5 owns TMEM and issues the MMAs.
+// KPS row-tiled activation k-blocks), warp 9 owns TMEM and issues the MMAs.
 // The SM's copy engine spends a roughly fixed time per request (about 0.3 us for
 // a bulk copy, 0.55 us for a tensor-tiled box, nearly independent of size up to
 // 32 KB), so a stage is two large bulk requests.  All waits are bounded.
@@ -82,8 +82,13 @@ struct SkArgs {
   int *tile_cnt;         // per-tile arrival counters (zero between launches); null: no fix-up
 };
 
+constexpr int EPW = 8;              // epilogue warps
+constexpr int EPT = 32 * EPW;        // epilogue threads
+constexpr int SK_THREADS = EPT + 64; // + producer warp + MMA warp
+constexpr int PRODUCER = EPW, MMA = EPW + 1;
+
 template <typename CT, int BN, int STAGES, int KPS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(SK_THREADS, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const uint16_t *x,
@@ -107,20 +112,20 @@ __global__ void __launch_bounds__(192, 1)
   const int P = gridDim.x, c = blockIdx.x;
   const long long u_begin = (long long)c * a.U / P, u_end = (long long)(c + 1) * a.U / P;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == PRODUCER && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], EPW);  // one arrival per epilogue warp
     }
     mbar_init(fix_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == MMA) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();  // one CTA per SM: the next kernel may start its set-up
 
-  if (warp == 4 && lane == 0) {
+  if (warp == PRODUCER && lane == 0) {
     // ---------------- loads ----------------
     if (!a.tiled) {
       prefetch_tmap(&tm_w0);
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(192, 1)
     for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
       if (!mbar_wait_bounded(&full[i % STAGES], (uint32_t)((i / STAGES) & 1)))
         set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
-  } else if (warp == 5 && lane == 0) {
+  } else if (warp == MMA && lane == 0) {
     // ---------------- MMA ----------------
     constexpr uint32_t idesc = idesc_f16kind<CT>(BN);
     int seg = 0;
@@ -229,7 +234,7 @@ __global__ void __launch_bounds__(192, 1)
       u += n;
       ++seg;
     }
-  } else if (warp < 4) {
+  } else if (warp < EPW) {
     // ---------------- epilogue ----------------
     // With a.tile_cnt (element-wise epilogues) a tile split over S runs is finished
     // inside the kernel by its owner, the run holding its first k-blocks (slot 0;
@@ -247,10 +252,11 @@ __global__ void __launch_bounds__(192, 1)
     // The bias of this thread's row in the tile of the last segment (the one an
     // owner finishes at the end of the run), read before waiting on the kernel
     // before this one: parameters do not depend on it.
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32 quarter.., column half
     float last_bias = 0.f;
     if (fix && u_end > u_begin) {
       const int t_last = (int)((u_end - 1) / a.KB);
-      last_bias = tile_row_bias(epi, t_last * BM + warp * 32 + lane, a.N);
+      last_bias = tile_row_bias(epi, t_last * BM + quarter * 32 + lane, a.N);
     }
     pdl_wait();  // outputs may still be read by the kernel before this one
     int seg = 0;
@@ -266,15 +272,15 @@ __global__ void __launch_bounds__(192, 1)
       int cf, S;
       sk_segments(t, a.KB, P, a.U, &cf, &S);
       const int slot = c - cf;
-      const int row = t * BM + warp * 32 + lane;
-      const uint32_t tl = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      const int row = t * BM + quarter * 32 + lane;
+      const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
       // (all conditions below are uniform over the four epilogue warps)
       const bool staged = fix && slot == 0 && u + n == u_end &&
                           tile_stage_tokens(S, a.M, W, kStageAvail) >= W;
       if (staged) {
-        tile_owner_epilogue<CT, W>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N,
-                                   a.M, t, S, tl, live, &a.tile_cnt[t], base, kStageAvail,
-                                   fix_bar, last_flag, dev_err, last_bias);
+        tile_owner_epilogue<CT, W, EPT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride,
+                                        a.N, a.M, t, S, tl, live, &a.tile_cnt[t], base,
+                                        kStageAvail, fix_bar, last_flag, dev_err, last_bias);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -287,11 +293,16 @@ __global__ void __launch_bounds__(192, 1)
           re.f32 = a.slices + slot * a.slice_stride + (size_t)t * a.M * BM + (row - t * BM);
           re.f32_stride = BM;
         }
+        // the two warps of a lane quarter take one half of the columns each (BN 16:
+        // the first one all 16)
+        constexpr int WH = BN >= 64 ? 32 : 16;
+        const int c_begin = BN >= 32 ? half * (BN / 2) : 0;
+        const int c_end = BN >= 32 ? c_begin + BN / 2 : (half == 0 ? BN : 0);
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += W) {
-          float v[W];
-          tmem_load_cols<W>(tl + c0, v);
-          if (live && row < a.N && c0 < a.M) row_epi_store<CT, W>(re, c0, min(W, a.M - c0), v);
+        for (int c0 = c_begin; c0 < c_end; c0 += WH) {
+          float v[WH];
+          tmem_load_cols<WH>(tl + c0, v);
+          if (live && row < a.N && c0 < a.M) row_epi_store<CT, WH>(re, c0, min(WH, a.M - c0), v);
         }
         tc_fence_before();
         __syncwarp();
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(192, 1)
           // this run's slice is complete: count it (release), every run of the
           // tile including an owner without room for the staged reduction
           __threadfence();
-          epi_bar_sync();
+          epi_bar_sync<EPT>();
           if (threadIdx.x == 0 && live) atomicAdd(&a.tile_cnt[t], 1);
           if (slot == 0) {
             // owner: wait for all S slices, then reduce them through registers
@@ -309,11 +320,11 @@ __global__ void __launch_bounds__(192, 1)
               if (live && !ok2) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
               *last_flag = ok2;
             }
-            epi_bar_sync();
+            epi_bar_sync<EPT>();
             if (*last_flag) {
               __threadfence();
-              tile_fixup<CT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N, a.M, t,
-                             S, threadIdx.x);
+              tile_fixup<CT, EPT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride, a.N,
+                                  a.M, t, S, threadIdx.x);
               if (threadIdx.x == 0) a.tile_cnt[t] = 0;
             }
           }
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
@@ -365,7 +376,7 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_k(k_gemm_sk<CT, BN, STAGES, KPS>, dim3(P), dim3(192), C::SMEM, st, g_pdl, tw[0],
+  return launch_k(k_gemm_sk<CT, BN, STAGES, KPS>, dim3(P), dim3(SK_THREADS), C::SMEM, st, g_pdl, tw[0],
                   tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
 }
 

@@ -138,13 +138,13 @@ __device__ __forceinline__ void store4(CT *p, float a, float b, float c, float d
 
 // Final epilogue of one 128-feature output tile from its S fp32 slices
 // (tile-contiguous: tslices + s * sstride + tok * 128 + feature in the tile,
-// s = 0 .. S-1), summed in slot order.  Called by the 128
-// threads et = 0..127 of one CTA: thread et owns features n0 .. n0 + 3 with
-// n0 = 128 t + 4 (et % 32) and tokens et / 32, et / 32 + 4, ...; a warp thus
-// reads and writes 128 consecutive features of one token (coalesced).
+// s = 0 .. S-1), summed in slot order.  Called by the NT threads et = 0..NT-1
+// of one CTA: thread et owns features n0 .. n0 + 3 with n0 = 128 t + 4 (et % 32)
+// and tokens et / 32, et / 32 + NT / 32, ...; a warp thus reads and writes 128
+// consecutive features of one token (coalesced).
 // Needs N % 4 == 0 and, per kind, 16-byte aligned fp32 rows (STORE_F32) or
 // 8-byte aligned groups of four 16-bit outputs (QKV, RELU).
-template <typename CT>
+template <typename CT, int NT>
 __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, long long sstride,
                                            int N, int M, int t, int S, int et) {
   const int n0 = t * 128 + 4 * (et & 31);
@@ -196,7 +196,8 @@ __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, l
   }
   const float *src = tslices + 4 * (et & 31);
   constexpr int TU = 8;  // tokens per thread per round: 8 x 2 slices of loads in flight
-  for (int tb = et >> 5; tb < M; tb += 4 * TU) {
+  constexpr int TS = NT / 32;  // token step between a thread's tokens
+  for (int tb = et >> 5; tb < M; tb += TS * TU) {
     float4 acc[TU];
 #pragma unroll
     for (int i = 0; i < TU; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -204,7 +205,7 @@ __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, l
       float4 v0[TU], v1[TU];
 #pragma unroll
       for (int i = 0; i < TU; ++i) {
-        const int tok = tb + 4 * i;
+        const int tok = tb + TS * i;
         const float *p = src + (long long)s * sstride + (long long)tok * 128;
         v0[i] = tok < M ? __ldcg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
         v1[i] = tok < M && s + 1 < S ? __ldcg(reinterpret_cast<const float4 *>(p + sstride))
@@ -226,7 +227,7 @@ __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, l
     }
 #pragma unroll
     for (int i = 0; i < TU; ++i) {
-      const int tok = tb + 4 * i;
+      const int tok = tb + TS * i;
       if (tok >= M) break;
       const float4 a = acc[i];
       switch (mode) {
@@ -345,7 +346,8 @@ __device__ __forceinline__ float tile_row_bias(const Epi &e, int n, int N) {
 // k-blocks, whose accumulator is in TMEM at `tl` for this thread's row), with the
 // other S - 1 runs' fp32 slices in global memory (tile-contiguous: tslices +
 // s * sstride + tok * 128 + feature), once they have all counted themselves in
-// *cnt.  Runs on the four epilogue warps (et = threadIdx.x < 128) after the CTA's
+// *cnt.  Runs on the NT (256) epilogue threads, two per TMEM lane (et and et +
+// 128 take alternate W-column chunks), after the CTA's
 // last MMA, so the pipeline's shared memory `stage` (avail bytes) is free: per
 // chunk of ch tokens the other slices come in as one bulk copy each (completing
 // on the mbarrier `bar`), each thread adds its row's values in slot order (its own
@@ -353,18 +355,19 @@ __device__ __forceinline__ float tile_row_bias(const Epi &e, int n, int N) {
 // tile, which then leaves (rounded to the output type) as 16-byte stores.  `bias`
 // is this thread's row's (tile_row_bias).  `flag` is a shared int; returns with
 // every epilogue thread past the same barriers.
-template <typename CT, int W>
+template <typename CT, int W, int NT>
 __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *tslices,
                                                     long long sstride, int N, int M, int t, int S,
                                                     uint32_t tl, bool live, int *cnt,
                                                     uint8_t *stage, int avail, uint64_t *bar,
                                                     int *flag, int *dev_err, float bias) {
-  const int et = threadIdx.x, r = et;  // r: this thread's row (feature) of the tile
+  static_assert(NT == 256, "two threads per TMEM lane");
+  const int et = threadIdx.x, r = et & 127, hf = et >> 7;  // row (feature) of the tile, half
   const int n_row = t * 128 + r;
   // per-row epilogue constants (`bias`, this row's, was read by the caller)
   float scale = 1.f;
   if (n_row < N && e.kind == EPI_QKV && n_row < e.d_model) scale = e.q_scale;
-  epi_bar_sync();  // *flag may still be read from an earlier segment
+  epi_bar_sync<NT>();  // *flag may still be read from an earlier segment
   if (et == 0) {
     // acquire: the other runs' slices (written, fenced, then counted) are visible
     // to this thread and, through the barrier below, to the whole group
@@ -375,7 +378,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
     }
     *flag = ok;
   }
-  epi_bar_sync();
+  epi_bar_sync<NT>();
   const bool go = *flag != 0;
   const int ob = tile_out_bytes(e.kind, (int)sizeof(CT));
   const bool relu = e.kind == EPI_RELU;
@@ -397,10 +400,10 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
       if (!mbar_wait_bounded(bar, phase)) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
       phase ^= 1;
     }
-    epi_bar_sync();
+    epi_bar_sync<NT>();
     const uint32_t ps_s = smem_u32(ps), os_s = smem_u32(os);
 #pragma unroll 1
-    for (int j0 = 0; j0 < cn; j0 += W) {
+    for (int j0 = hf * W; j0 < cn; j0 += 2 * W) {
       // own accumulator (slot 0), then the other slots in order; rows j0 .. j0+W-1
       // stay inside the chunk's staging (ch is a multiple of W)
       float v[W];
@@ -423,7 +426,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
         sts_f32(os_s + (uint32_t)(((j0 + j) * 128 + r) * 4), y);
       }
     }
-    epi_bar_sync();
+    epi_bar_sync<NT>();
     if (go) {
       // 16-byte output groups (4 fp32 values, or 8 values rounded to CT): thread et
       // always takes group et % cpr of rows et / cpr, et / cpr + 128 / cpr, ...
@@ -431,7 +434,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
       const int k = et % cpr, n = t * 128 + k * per;
       if (n < N) {
         const TileOutRow orow = tile_out_row<CT>(e, n);
-        for (int jj = et / cpr; jj < cn; jj += 128 / cpr) {
+        for (int jj = et / cpr; jj < cn; jj += NT / cpr) {
           const uint32_t src = os_s + (uint32_t)((jj * 128 + k * per) * 4);
           uint4 o = lds_u128(src);
           if (ob != 4) {
@@ -452,7 +455,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
         }
       }
     }
-    epi_bar_sync();  // the next chunk reuses the staging memory
+    epi_bar_sync<NT>();  // the next chunk reuses the staging memory
   }
   if (go && S > 1 && et == 0) *cnt = 0;  // every other run of t has counted itself
 }
