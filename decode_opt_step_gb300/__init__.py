@@ -86,6 +86,7 @@ _SIGNATURES = {
     "he_release_workspace": (c_int, [c_void_p, c_void_p]),
     "he_retake_workspace": (c_int, [c_void_p, c_void_p]),
     "he_set_profiling": (c_int, [c_void_p, c_uint]),
+    "he_set_cuda_graph": (c_int, [c_void_p, c_int]),
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
     "he_last_error": (c_char_p, []),
     "he_version": (c_char_p, []),
@@ -256,6 +257,10 @@ class Engine:
 
     def check(self, stream=None):
         _check(self._lib.he_check(self._h, self._s(stream)))
+
+    def set_cuda_graph(self, enable: bool = True):
+        """Run he_generate / he_generate_host as a captured, cached CUDA graph."""
+        _check(self._lib.he_set_cuda_graph(self._h, 1 if enable else 0))
 
     def set_profiling(self, classes=()):
         """Time the given kernel classes (names from KCLASS, or "all"); () turns it off."""

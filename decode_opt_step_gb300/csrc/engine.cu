@@ -8,6 +8,7 @@
 // embedded on the device by the head kernel for step k + 1.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -86,6 +87,13 @@ struct he_engine {
 
   he_stats stats{};
   cudaEvent_t ph[7] = {};  // generate begin/prefill end/end, fuse begin/end, unfuse begin/end
+  // CUDA-graph generation (he_set_cuda_graph): one captured generation per shape and
+  // buffer set, replayed on the caller's stream
+  bool graph_on = false, capturing = false;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  std::vector<const void *> gkey;  // shape, activation type and every buffer address
+  unsigned long long glaunches = 0;  // kernel launches in the captured generation
   struct Pair { cudaEvent_t a, b; };
   std::vector<Pair> prof_pool[kClasses];
   size_t prof_used[kClasses] = {};
@@ -462,6 +470,14 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   c.check(launch_head_select(cf.dtype, h->act, ha, c.st), 1);
 }
 
+// Phase events: recorded as graph nodes while a generation is being captured.
+void record_phase(he_engine *h, int i, cudaStream_t st) {
+  if (h->capturing)
+    cudaEventRecordWithFlags(h->ph[i], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(h->ph[i], st);
+}
+
 he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int Lgen,
                         int32_t *out_ids, float *out_lp, const int32_t *force,
                         const int32_t *log_map, float *logits_out, cudaStream_t st) {
@@ -473,7 +489,7 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   h->act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
   for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
   ensure_phase_events(h);
-  cudaEventRecord(h->ph[0], st);
+  record_phase(h, 0, st);
   // the GEMMs leave the tile counters at zero; clearing them here also recovers
   // from a call whose GEMM gave up on a wait part-way
   c.check(cudaMemsetAsync(h->tilecnt.p, 0, tilecnt_bytes(cf), st), 0);
@@ -491,14 +507,14 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   // head on the last prompt position of every sequence (rows b*Lp + Lp-1)
   head(c, at(h->h.p, (size_t)(Lp - 1) * d * h->elem), Lp * d, B, 0, Lp, Lgen, force, out_ids,
        out_lp, log_map, logits_out);
-  cudaEventRecord(h->ph[1], st);
+  record_phase(h, 1, st);
   // ---- decode: token k is fed at position Lp + k - 1 ----
   for (int k = 1; k < Lgen; ++k) {
     const int t = Lp + k - 1;
     for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, B, 1, t, false);
     head(c, h->h.p, d, B, k, Lp, Lgen, force, out_ids, out_lp, log_map, logits_out);
   }
-  cudaEventRecord(h->ph[2], st);
+  record_phase(h, 2, st);
   h->stats.generate_calls++;
   h->stats_pending = true;
   if (c.e != cudaSuccess) return cuda_fail(c.e, "he_generate launch");
@@ -518,6 +534,80 @@ he_status check_generate_args(he_engine *h, const void *prompt, int B, int Lp, i
     return fail(HE_ERR_ARG, "positions up to %lld exceed max_pos=%d", (long long)Lp + Lgen - 2,
                 c.max_pos);
   if (!h->taken) return fail(HE_ERR_STATE, "workspace is released; call he_retake_workspace");
+  return HE_OK;
+}
+
+void drop_graph(he_engine *h) {
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  h->gexec = nullptr;
+  h->gkey.clear();
+}
+
+// A generation from h->ids_in into h->ids_out / h->lp_out: launched directly, or,
+// with he_set_cuda_graph on and profiling off, as the replay of a captured graph
+// of the whole generation (re-captured when the shape, the activation type or any
+// buffer address differs from the captured one).
+he_status generate_internal(he_engine *h, int B, int Lp, int Lgen, cudaStream_t st) {
+  int32_t *ids_in = static_cast<int32_t *>(h->ids_in.p);
+  int32_t *ids_out = static_cast<int32_t *>(h->ids_out.p);
+  float *lp_out = static_cast<float *>(h->lp_out.p);
+  if (!h->graph_on || h->prof_mask)
+    return generate_impl(h, ids_in, B, Lp, Lgen, ids_out, lp_out, nullptr, nullptr, nullptr, st);
+  const he_config &cf = h->cfg;
+  const int act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
+  std::vector<const void *> key = {
+      reinterpret_cast<const void *>((uintptr_t)B), reinterpret_cast<const void *>((uintptr_t)Lp),
+      reinterpret_cast<const void *>((uintptr_t)Lgen), reinterpret_cast<const void *>((uintptr_t)act),
+      h->kc.p, h->vc.p, h->x.p, h->h.p, h->q.p, h->ctx.p, h->mid.p, h->partial.p, h->logits.p,
+      h->attn_part.p, h->ids_in.p, h->ids_out.p, h->lp_out.p, h->err.p, h->tilecnt.p,
+      h->restore.p};
+  if (!h->gexec || key != h->gkey) {
+    if (!h->cap_stream &&
+        cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(HE_ERR_CUDA, "capture stream creation failed");
+    ensure_phase_events(h);
+    const unsigned long long l0 = h->stats.launches;
+    const unsigned long long calls0 = h->stats.generate_calls;
+    cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) return cuda_fail(e, "graph capture begin");
+    h->capturing = true;
+    he_status s = generate_impl(h, ids_in, B, Lp, Lgen, ids_out, lp_out, nullptr, nullptr,
+                                nullptr, h->cap_stream);
+    h->capturing = false;
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(h->cap_stream, &g);
+    h->stats.generate_calls = calls0;  // counted at each replay below
+    if (s != HE_OK || e != cudaSuccess || !g) {
+      if (g) cudaGraphDestroy(g);
+      drop_graph(h);
+      return s != HE_OK ? s : cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown, "graph capture");
+    }
+    h->glaunches = h->stats.launches - l0;
+    h->stats.launches = l0;
+    bool updated = false;
+    if (h->gexec && h->gkey.size() >= 4 &&
+        std::equal(key.begin(), key.begin() + 4, h->gkey.begin())) {
+      cudaGraphExecUpdateResultInfo info;
+      updated = cudaGraphExecUpdate(h->gexec, g, &info) == cudaSuccess;
+      if (!updated) cudaGetLastError();
+    }
+    if (!updated) {
+      drop_graph(h);
+      e = cudaGraphInstantiate(&h->gexec, g, 0);
+      if (e != cudaSuccess) {
+        h->gexec = nullptr;
+        cudaGraphDestroy(g);
+        return cuda_fail(e, "graph instantiation");
+      }
+    }
+    cudaGraphDestroy(g);
+    h->gkey = key;
+  }
+  cudaError_t e = cudaGraphLaunch(h->gexec, st);
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  h->stats.launches += h->glaunches;
+  h->stats.generate_calls++;
+  h->stats_pending = true;
   return HE_OK;
 }
 
@@ -635,6 +725,8 @@ he_status he_destroy(he_engine *h) {
   put(h, h->restore, nullptr);
   put(h, h->tilecnt, nullptr);
   put(h, h->err, nullptr);
+  drop_graph(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   for (auto &e : h->ph)
     if (e) cudaEventDestroy(e);
   for (auto &pool : h->prof_pool)
@@ -766,8 +858,35 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
 
 he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
                       int32_t *out_ids, float *out_logprob, void *stream) {
-  return he_generate_ex(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob, nullptr, nullptr, 0,
-                        nullptr, stream);
+  if (!h || !h->graph_on)
+    return he_generate_ex(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob, nullptr, nullptr, 0,
+                          nullptr, stream);
+  // graph mode: the captured generation reads and writes the engine's own buffers
+  g_err.clear();
+  he_status s = check_generate_args(h, prompt_ids, B, Lp, Lgen, out_ids, out_logprob);
+  if (s != HE_OK) return s;
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->ids_in.p, prompt_ids, (size_t)B * Lp * 4,
+                                  cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prompt copy");
+  s = generate_internal(h, B, Lp, Lgen, st);
+  if (s != HE_OK) return s;
+  e = cudaMemcpyAsync(out_ids, h->ids_out.p, (size_t)B * Lgen * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(out_logprob, h->lp_out.p, (size_t)B * Lgen * 4, cudaMemcpyDeviceToDevice,
+                        st);
+  if (e != cudaSuccess) return cuda_fail(e, "result copy");
+  return HE_OK;
+}
+
+he_status he_set_cuda_graph(he_engine *h, int enable) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  cudaSetDevice(h->device);
+  h->graph_on = enable != 0;
+  if (!h->graph_on) drop_graph(h);
+  return HE_OK;
 }
 
 he_status he_generate_ex(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
@@ -830,9 +949,7 @@ he_status he_generate_host(he_engine *h, const int32_t *prompt_ids, int B, int L
   cudaError_t e = cudaMemcpyAsync(h->ids_in.p, prompt_ids, (size_t)B * Lp * 4,
                                   cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "prompt upload");
-  s = generate_impl(h, static_cast<int32_t *>(h->ids_in.p), B, Lp, Lgen,
-                    static_cast<int32_t *>(h->ids_out.p), static_cast<float *>(h->lp_out.p),
-                    nullptr, nullptr, nullptr, st);
+  s = generate_internal(h, B, Lp, Lgen, st);
   if (s != HE_OK) return s;
   e = cudaMemcpyAsync(out_ids, h->ids_out.p, (size_t)B * Lgen * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess)

@@ -25,7 +25,7 @@
  *             model before generation and restores it after; the KV cache and
  *             intermediate results live in a workspace that is released after
  *             generation and retaken before the next; §四 (config fields):
- *             max_out_tokens, release_inference_cache.
+ *             max_out_tokens, release_inference_cache, enable_cuda_graph.
  *  [RLHF-ch11] "Chapter 11 System Architecture & Infrastructure at Scale",
  *             "The Generation Bottleneck: Quantitative Analysis": generation
  *             returns the log-probabilities of the generated tokens.
@@ -229,6 +229,17 @@ he_status he_release_workspace(he_engine *h, void *stream);
 /* Takes the workspace again before the next generation.  HE_ERR_STATE if held;
  * HE_ERR_OOM leaves the engine released and usable (retry later). */
 he_status he_retake_workspace(he_engine *h, void *stream);
+
+/* [HE-guide] enable_cuda_graph (§三 and the §四 field table: a CUDA-graph cache
+ * for generation to cut launch overhead; off by default there and here).  With
+ * enable != 0, he_generate and he_generate_host run the generation as one CUDA
+ * graph, captured on first use and replayed afterwards; it is re-captured when
+ * B, Lp, Lgen, fused / unfused, or the address of a workspace buffer changes
+ * (e.g. after he_release_workspace / he_retake_workspace).  The kernels and their
+ * order are those of the direct launch, so the results are identical.
+ * he_generate_ex with teacher forcing or logit capture, and any generation with
+ * profiling on, launch directly.  enable == 0 frees the cached graph. */
+he_status he_set_cuda_graph(he_engine *h, int enable);
 
 /* Per-kernel-class event timing of he_generate: class_mask has bit c set for
  * every HE_KCLASS_c to time (0 = off, the default).  Costs two events per
