@@ -231,6 +231,7 @@ def main():
     ap.add_argument("--workload", default="opt-13b", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-score", action="store_true")
     ap.add_argument("--no-cuda-graph", dest="cuda_graph", action="store_false",
                     help="launch every kernel directly instead of replaying the captured "
                          "CUDA graph of the generation (enable_cuda_graph)")
@@ -323,6 +324,31 @@ def main():
             kln[k] += st["kclass_launches"][k]
     eng.set_profiling(())
 
+    # ---- scoring: log-probs of the generated answers in one pass (he_score) ----
+    score = None
+    if not args.no_score:
+        eng.fuse_lora()
+        eng.generate(prompts, Lgen, out=(ids, lps))
+        full = torch.cat([prompts, ids], dim=1).contiguous()
+        sc = torch.empty((B, Lgen), dtype=torch.float32, device=dev)
+        eng.score(full, Lp, out=sc)  # warm-up
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 2
+        s0.record()
+        for _ in range(reps):
+            eng.score(full, Lp, out=sc)
+        s1.record()
+        torch.cuda.synchronize()
+        sc_ms = s0.elapsed_time(s1) / reps
+        lp_gap = (sc - lps).abs().max().item()
+        eng.unfuse_lora()
+        f_tok = B * (Lp + Lgen - 1)
+        score = {"ms": sc_ms, "tokens_per_s": B * Lgen / (sc_ms / 1000.0),
+                 "tflops": (prefill_flops(cfg, B, Lp + Lgen - 1)[0]
+                            + 2 * B * (Lgen - 1) * cfg.d_model * cfg.vocab) / (sc_ms / 1000.0) / 1e12,
+                 "tokens_in_pass": f_tok, "max_abs_vs_decode_logprobs": lp_gap}
+
     # ---- end to end through the host-buffer entry point ----
     e2e = None
     if not args.no_e2e:
@@ -389,6 +415,7 @@ def main():
                        "tokens_per_s": B * (Lgen - 1) / (dec_ms / 1000.0)},
             "prefill": {"ms": pf_ms, "tflops": pf_flops / (pf_ms / 1000.0) / 1e12},
             "fuse_ms": phase["fuse_ms"] / steps, "unfuse_ms": phase["unfuse_ms"] / steps,
+            "score": score,
             "kernels": per_kernel}
     if rank == 0:
         if cpu is not None:

@@ -87,6 +87,7 @@ _SIGNATURES = {
     "he_retake_workspace": (c_int, [c_void_p, c_void_p]),
     "he_set_profiling": (c_int, [c_void_p, c_uint]),
     "he_set_cuda_graph": (c_int, [c_void_p, c_int]),
+    "he_score": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
     "he_last_error": (c_char_p, []),
     "he_version": (c_char_p, []),
@@ -313,6 +314,18 @@ class Engine:
                                         rows_c.ctypes.data if n else None, n,
                                         logits.data_ptr() if n else None, self._s(stream)))
         return ids, lps, logits[:n]
+
+    def score(self, ids, prompt_len: int, out=None, stream=None):
+        """Log-probs of ids[:, prompt_len:] given their prefixes, one forward pass over
+        prompt + answer (he_score): fp32 [B][L - prompt_len]."""
+        torch = self._torch
+        p = self._prompts(ids)
+        B, L = p.shape
+        if out is None:
+            out = torch.empty((B, L - prompt_len), dtype=torch.float32, device=self.device)
+        _check(self._lib.he_score(self._h, p.data_ptr(), B, L, prompt_len, out.data_ptr(),
+                                  self._s(stream)))
+        return out
 
     def generate_host(self, prompts: np.ndarray, gen_len: int, stream=None):
         """Host buffers in and out (copies inside the call); synchronises the stream."""

@@ -399,6 +399,32 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
           1);
 }
 
+// Logits [B][vocab] (fp32, h->logits) of B row-major rows of the last LayerNorm's
+// output (row stride ldh, the parameter type) against the tied embedding table.
+void head_rows_gemm(Ctx &c, const void *hrows, int ldh, int B) {
+  he_engine *h = c.h;
+  const he_config &cf = h->cfg;
+  Timed t(h, HE_KCLASS_HEAD, c.st);
+  Epi el{};
+  el.kind = EPI_STORE_F32;
+  el.partial = static_cast<float *>(h->logits.p);
+  el.ldp = cf.vocab;
+  GemmArgs a{};
+  a.dtype = cf.dtype;
+  a.act = cf.dtype;  // the head reads the caller's embedding table
+  a.x = hrows;
+  a.ldx = ldh;
+  a.w[0] = h->tok_emb;
+  a.n_groups = 1;
+  a.group_rows = cf.vocab;
+  a.M = B;
+  a.N = cf.vocab;
+  a.K = cf.d_model;
+  a.split = 1;
+  a.epi = el;
+  c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+}
+
 // LM head over B rows of h + greedy select for step k.  Step 0 (after the prefill)
 // reads row-major h rows b*Lp + Lp-1 (row stride ldh); decode steps read the
 // row-tiled h through the stream-K kernel.  The chosen token is embedded and
@@ -418,21 +444,7 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
     const void *we[1] = {h->tok_emb};
     gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false, cf.dtype);
   } else {
-    Timed t(h, HE_KCLASS_HEAD, c.st);
-    GemmArgs a{};
-    a.dtype = cf.dtype;
-    a.act = cf.dtype;  // the head reads the caller's embedding table
-    a.x = hrows;
-    a.ldx = ldh;
-    a.w[0] = h->tok_emb;
-    a.n_groups = 1;
-    a.group_rows = cf.vocab;
-    a.M = B;
-    a.N = cf.vocab;
-    a.K = cf.d_model;
-    a.split = 1;
-    a.epi = el;
-    c.check(launch_gemm(a, static_cast<int *>(h->err.p), c.st), 1);
+    head_rows_gemm(c, hrows, ldh, B);
   }
   if (!dec && R > 0) {
     // from here on h, ctx and mid hold row-tiled decode tiles whose padding rows
@@ -936,6 +948,65 @@ he_status he_check(he_engine *h, void *stream) {
       return fail(HE_ERR_DEVICE_CHECK, "a GEMM pipeline wait timed out (flags 0x%x)", flags);
     return fail(HE_ERR_DEVICE_CHECK, "token id outside [0, vocab) replaced by 0 (flags 0x%x)", flags);
   }
+  return HE_OK;
+}
+
+he_status he_score(he_engine *h, const int32_t *ids, int B, int L, int Lp, float *out_logprob,
+                   void *stream) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (!ids || !out_logprob) return fail(HE_ERR_ARG, "NULL buffer");
+  const he_config &cf = h->cfg;
+  if (B < 1 || B > cf.max_batch) return fail(HE_ERR_ARG, "B=%d outside [1, max_batch=%d]", B, cf.max_batch);
+  if (Lp < 1 || L <= Lp) return fail(HE_ERR_ARG, "need 1 <= Lp < L (Lp=%d, L=%d)", Lp, L);
+  if (L > cf.max_seq) return fail(HE_ERR_ARG, "L=%d exceeds max_seq=%d", L, cf.max_seq);
+  if (L - 1 > cf.max_pos) return fail(HE_ERR_ARG, "positions up to %d exceed max_pos=%d", L - 2, cf.max_pos);
+  if (!h->taken) return fail(HE_ERR_STATE, "workspace is released; call he_retake_workspace");
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Lgen = L - Lp, T = L - 1, M = B * T, d = cf.d_model;
+  int32_t *toks = static_cast<int32_t *>(h->ids_in.p);      // [B][T]: the tokens fed
+  int32_t *targets = static_cast<int32_t *>(h->ids_out.p);  // [B][Lgen]: the tokens scored
+  int32_t *echo = static_cast<int32_t *>(h->logmap.p);      // [B][Lgen]: ids the head emits
+  cudaError_t e = cudaMemcpy2DAsync(toks, (size_t)T * 4, ids, (size_t)L * 4, (size_t)T * 4, B,
+                                    cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(targets, (size_t)Lgen * 4, ids + Lp, (size_t)L * 4, (size_t)Lgen * 4, B,
+                          cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "token copy");
+  Ctx c{h, st};
+  h->act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
+  for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
+  c.check(cudaMemsetAsync(h->tilecnt.p, 0, tilecnt_bytes(cf), st), 0);
+  // one pass over tokens 0 .. L-2 of every sequence (the prefill kernels)
+  {
+    Timed t(h, HE_KCLASS_OTHER, st);
+    c.check(launch_embed_ln(cf.dtype, h->act, toks, M, T, 0, h->tok_emb, h->pos_emb, cf.pos_offset,
+                            cf.vocab, h->layers[0].ln1_g, h->layers[0].ln1_b, cf.ln_eps,
+                            static_cast<float *>(h->x.p), h->h.p, d,
+                            static_cast<int *>(h->err.p), st),
+            1);
+  }
+  for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, M, T, 0, true);
+  // the distribution at position Lp-1+k scores token Lp+k
+  for (int k = 0; k < Lgen; ++k) {
+    head_rows_gemm(c, at(h->h.p, (size_t)(Lp - 1 + k) * d * h->elem), T * d, B);
+    Timed t(h, HE_KCLASS_HEAD, st);
+    HeadArgs ha{};
+    ha.logits = static_cast<float *>(h->logits.p);
+    ha.ldl = cf.vocab;
+    ha.vocab = cf.vocab;
+    ha.B = B;
+    ha.step = k;
+    ha.gen_len = Lgen;
+    ha.force_ids = targets;
+    ha.out_ids = echo;
+    ha.out_lp = out_logprob;
+    ha.embed_next = 0;
+    c.check(launch_head_select(cf.dtype, h->act, ha, st), 1);
+  }
+  h->stats_pending = false;
+  if (c.e != cudaSuccess) return cuda_fail(c.e, "he_score launch");
   return HE_OK;
 }
 

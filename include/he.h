@@ -230,6 +230,22 @@ he_status he_release_workspace(he_engine *h, void *stream);
  * HE_ERR_OOM leaves the engine released and usable (retry later). */
 he_status he_retake_workspace(he_engine *h, void *stream);
 
+/* [DSC-gen] item 2 (the training phase consumes the log-probabilities of the
+ * generated responses under the reference model) and [RLHF-ch11] (log-probs of
+ * every generated token are needed for PPO): the log-probability of each answer
+ * token under this model, computed in one forward pass over prompt + answer
+ * rather than token by token.  ids: device
+ * int32 [B][L], a prompt of Lp tokens followed by L - Lp answer tokens, every id
+ * in [0, vocab).  out_logprob: device fp32 [B][L - Lp]; element (b, k) is the
+ * natural-log softmax at position Lp - 1 + k of token ids[b][Lp + k], i.e. what
+ * he_generate_ex reports when teacher-forced on the same answer.  One pass of the
+ * prefill kernels over tokens 0 .. L-2 (filling the KV cache), then the head on
+ * rows Lp - 1 .. L - 2.  Requires 1 <= B <= max_batch, 1 <= Lp < L <= max_seq,
+ * L - 1 <= max_pos and a taken workspace.  Runs fused or unfused; an id out of
+ * range is replaced by 0 on the device and reported by he_check. */
+he_status he_score(he_engine *h, const int32_t *ids, int B, int L, int Lp, float *out_logprob,
+                   void *stream);
+
 /* [HE-guide] enable_cuda_graph (§三 and the §四 field table: a CUDA-graph cache
  * for generation to cut launch overhead; off by default there and here).  With
  * enable != 0, he_generate and he_generate_host run the generation as one CUDA
