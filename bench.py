@@ -232,6 +232,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-score", action="store_true")
+    ap.add_argument("--sampling", default=None, metavar="T,TOP_P,SEED",
+                    help="sampled instead of greedy generation, e.g. 0.7,0.9,1234")
     ap.add_argument("--no-cuda-graph", dest="cuda_graph", action="store_false",
                     help="launch every kernel directly instead of replaying the captured "
                          "CUDA graph of the generation (enable_cuda_graph)")
@@ -273,6 +275,9 @@ def main():
     eng = he.Engine(cfg, w, max_batch=B, max_seq=Lp + Lgen)
     if args.cuda_graph:
         eng.set_cuda_graph(True)
+    if args.sampling:
+        t_s, p_s, seed_s = args.sampling.split(",")
+        eng.set_sampling(float(t_s), float(p_s), int(seed_s))
     prompts = torch.from_numpy(prompts_np).to(dev)
     ids = torch.empty((B, Lgen), dtype=torch.int32, device=dev)
     lps = torch.empty((B, Lgen), dtype=torch.float32, device=dev)
@@ -406,7 +411,9 @@ def main():
             "data": "synthetic (N(0,0.02) weights and LoRA factors, uniform prompt ids)",
             "config": {**workload_config(cfg),
                        "launch": ("one CUDA graph per generation" if args.cuda_graph
-                                  else "direct launches, programmatic dependent launch")},
+                                  else "direct launches, programmatic dependent launch"),
+                       "decoding": (f"sampled (temperature, top_p, seed = {args.sampling})"
+                                    if args.sampling else "greedy")},
             "clocks": clk, "gpu_launches": launches,
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
             "decode": {"ms": dec_ms, "bytes_per_step_avg": dec_total / (Lgen - 1),

@@ -87,6 +87,7 @@ _SIGNATURES = {
     "he_retake_workspace": (c_int, [c_void_p, c_void_p]),
     "he_set_profiling": (c_int, [c_void_p, c_uint]),
     "he_set_cuda_graph": (c_int, [c_void_p, c_int]),
+    "he_set_sampling": (c_int, [c_void_p, ctypes.c_float, ctypes.c_float, ctypes.c_uint64]),
     "he_score": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
     "he_last_error": (c_char_p, []),
@@ -258,6 +259,11 @@ class Engine:
 
     def check(self, stream=None):
         _check(self._lib.he_check(self._h, self._s(stream)))
+
+    def set_sampling(self, temperature: float = 0.0, top_p: float = 1.0, seed: int = 0):
+        """Sampled generation (temperature > 0, nucleus top_p, counter-based seed); 0 = greedy."""
+        _check(self._lib.he_set_sampling(self._h, float(temperature), float(top_p),
+                                         int(seed) & ((1 << 64) - 1)))
 
     def set_cuda_graph(self, enable: bool = True):
         """Run he_generate / he_generate_host as a captured, cached CUDA graph."""

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -87,6 +88,9 @@ struct he_engine {
 
   he_stats stats{};
   cudaEvent_t ph[7] = {};  // generate begin/prefill end/end, fuse begin/end, unfuse begin/end
+  // sampling (he_set_sampling): temperature 0 = greedy
+  float temperature = 0.f, top_p = 1.f;
+  unsigned long long seed = 0;
   // CUDA-graph generation (he_set_cuda_graph): one captured generation per shape and
   // buffer set, replayed on the caller's stream
   bool graph_on = false, capturing = false;
@@ -479,6 +483,9 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   ha.h = h->h.p;
   ha.d = cf.d_model;
   ha.h_rows = R;
+  ha.temperature = h->temperature;
+  ha.top_p = h->top_p;
+  ha.seed = h->seed;
   c.check(launch_head_select(cf.dtype, h->act, ha, c.st), 1);
 }
 
@@ -549,6 +556,12 @@ he_status check_generate_args(he_engine *h, const void *prompt, int B, int Lp, i
   return HE_OK;
 }
 
+uint32_t float_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return u;
+}
+
 void drop_graph(he_engine *h) {
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
   h->gexec = nullptr;
@@ -572,7 +585,9 @@ he_status generate_internal(he_engine *h, int B, int Lp, int Lgen, cudaStream_t 
       reinterpret_cast<const void *>((uintptr_t)Lgen), reinterpret_cast<const void *>((uintptr_t)act),
       h->kc.p, h->vc.p, h->x.p, h->h.p, h->q.p, h->ctx.p, h->mid.p, h->partial.p, h->logits.p,
       h->attn_part.p, h->ids_in.p, h->ids_out.p, h->lp_out.p, h->err.p, h->tilecnt.p,
-      h->restore.p};
+      h->restore.p, reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
+      reinterpret_cast<const void *>((uintptr_t)float_bits(h->top_p)),
+      reinterpret_cast<const void *>((uintptr_t)h->seed)};
   if (!h->gexec || key != h->gkey) {
     if (!h->cap_stream &&
         cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -892,6 +907,19 @@ he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, in
   return HE_OK;
 }
 
+he_status he_set_sampling(he_engine *h, float temperature, float top_p,
+                          unsigned long long seed) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (!(temperature >= 0.f) || !std::isfinite(temperature))
+    return fail(HE_ERR_ARG, "temperature must be finite and >= 0");
+  if (!(top_p > 0.f && top_p <= 1.f)) return fail(HE_ERR_ARG, "top_p must be in (0, 1]");
+  h->temperature = temperature;
+  h->top_p = top_p;
+  h->seed = seed;
+  return HE_OK;
+}
+
 he_status he_set_cuda_graph(he_engine *h, int enable) {
   g_err.clear();
   if (!h) return fail(HE_ERR_ARG, "engine is NULL");
@@ -1003,6 +1031,8 @@ he_status he_score(he_engine *h, const int32_t *ids, int B, int L, int Lp, float
     ha.out_ids = echo;
     ha.out_lp = out_logprob;
     ha.embed_next = 0;
+    ha.temperature = h->temperature;  // log-probs under the sampling temperature
+    ha.top_p = 1.f;
     c.check(launch_head_select(cf.dtype, h->act, ha, st), 1);
   }
   h->stats_pending = false;

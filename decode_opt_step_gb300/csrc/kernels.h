@@ -227,6 +227,10 @@ struct HeadArgs {
   const void *g, *b; float eps;      // first layer's LN1
   float *x; void *h; int d;
   int h_rows;                        // h row-tiled with this R (0 = row-major)
+  // sampling (temperature > 0): softmax(logits / T) cut to its top_p nucleus, drawn by
+  // Gumbel-max with SplitMix64 uniforms keyed by (seed, b, step, token); 0 = greedy
+  float temperature, top_p;
+  unsigned long long seed;
 };
 // h is written in `act`.
 cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st);

@@ -248,6 +248,61 @@ __global__ void k_reduce_epi(const float *partial, int split, long long split_st
   epi_store<PT, CT>(epi, 0, tok, n, acc);
 }
 
+// Uniform in (0, 1) for (sequence b, step, token i): output number c + 1 of SplitMix64
+// (Steele, Lea and Flood 2014: state += 0x9E3779B97F4A7C15, then the two
+// xor-shift-multiply rounds) started from `seed`, c = (b * 2^20 + step) * 2^20 + i,
+// as (2 (z >> 41) + 1) / 2^24, exactly representable in fp32.
+__device__ __forceinline__ float sample_uniform(unsigned long long seed, int b, int step, int i) {
+  const unsigned long long c = ((((unsigned long long)b << 20) + (unsigned long long)step) << 20) +
+                               (unsigned long long)i;
+  unsigned long long z = seed + (c + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (float)(2ull * (z >> 41) + 1ull) * (1.0f / 16777216.0f);
+}
+
+// Block-wide (value, index) maximum, lowest index on equal values; every thread
+// gets the result.
+__device__ __forceinline__ void block_argmax(float &best, int &bidx, float *s_val, int *s_idx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ov > best || (ov == best && oi < bidx)) {
+      best = ov;
+      bidx = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) {
+    s_val[wid] = best;
+    s_idx[wid] = bidx;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    best = lane < nw ? s_val[lane] : -INFINITY;
+    bidx = lane < nw ? s_idx[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      if (ov > best || (ov == best && oi < bidx)) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if (lane == 0) {
+      s_val[0] = best;
+      s_idx[0] = bidx;
+    }
+  }
+  __syncthreads();
+  best = s_val[0];
+  bidx = s_idx[0];
+}
+
 // One block per sequence: greedy choice (lowest index among equal maxima),
 // log-prob of the emitted token, optional logit capture, then the embedding of
 // the emitted token at the next position followed by the first layer's LN1.
@@ -306,18 +361,68 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   __syncthreads();
   const float m = s_val[0];
   const int amax = s_idx[0] == 0x7fffffff ? 0 : s_idx[0];
-  float se = 0.f;
-  for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) se += expf(lg[i] - m);
-  se = block_sum(se, red);
-  if (threadIdx.x == 0) {
-    int tok = amax;
-    if (a.force_ids) {
-      const int f = a.force_ids[(long long)b * a.gen_len + a.step];
-      if (f >= 0 && f < a.vocab) tok = f;
+  if (a.temperature > 0.f) {
+    // ---- sampling: q_i = exp((l_i - m) / T), nucleus {q_i >= tau}, Gumbel-max ----
+    const float inv_t = 1.f / a.temperature;
+    float zs = 0.f;
+    for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) zs += expf((lg[i] - m) * inv_t);
+    const float Z = block_sum(zs, red);
+    // tau: the largest q whose "q_j >= tau" mass still reaches top_p * Z, built bit by
+    // bit (q <= 1 = the maximum's, so bits 30 and 31 stay clear); every decision is
+    // on a block sum, the same in all threads
+    uint32_t tau_bits = 0;
+    if (a.top_p < 1.f) {
+      const float target = a.top_p * Z;
+      for (int bit = 29; bit >= 0; --bit) {
+        const uint32_t cand = tau_bits | (1u << bit);
+        const float x = __uint_as_float(cand);
+        float ms = 0.f;
+        for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) {
+          const float q = expf((lg[i] - m) * inv_t);
+          if (q >= x) ms += q;
+        }
+        if (block_sum(ms, red) >= target) tau_bits = cand;
+      }
     }
-    a.out_ids[(long long)b * a.gen_len + a.step] = tok;
-    a.out_lp[(long long)b * a.gen_len + a.step] = lg[tok] - (m + logf(se));
-    s_tok = tok;
+    const float tau = __uint_as_float(tau_bits);
+    float sb = -INFINITY;
+    int si = 0x7fffffff;
+    for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) {
+      const float zi = (lg[i] - m) * inv_t;
+      if (expf(zi) >= tau) {
+        const float g = -logf(-logf(sample_uniform(a.seed, b, a.step, i)));
+        const float sc = zi + g;
+        if (sc > sb) {  // ascending scan: the first of equal scores keeps the lowest index
+          sb = sc;
+          si = i;
+        }
+      }
+    }
+    block_argmax(sb, si, s_val, s_idx);
+    if (threadIdx.x == 0) {
+      int tok = si == 0x7fffffff ? amax : si;
+      if (a.force_ids) {
+        const int f = a.force_ids[(long long)b * a.gen_len + a.step];
+        if (f >= 0 && f < a.vocab) tok = f;
+      }
+      a.out_ids[(long long)b * a.gen_len + a.step] = tok;
+      a.out_lp[(long long)b * a.gen_len + a.step] = (lg[tok] - m) * inv_t - logf(Z);
+      s_tok = tok;
+    }
+  } else {
+    float se = 0.f;
+    for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) se += expf(lg[i] - m);
+    se = block_sum(se, red);
+    if (threadIdx.x == 0) {
+      int tok = amax;
+      if (a.force_ids) {
+        const int f = a.force_ids[(long long)b * a.gen_len + a.step];
+        if (f >= 0 && f < a.vocab) tok = f;
+      }
+      a.out_ids[(long long)b * a.gen_len + a.step] = tok;
+      a.out_lp[(long long)b * a.gen_len + a.step] = lg[tok] - (m + logf(se));
+      s_tok = tok;
+    }
   }
   if (a.log_map) {
     const int r = a.log_map[(long long)a.step * a.B + b];

@@ -246,6 +246,21 @@ he_status he_retake_workspace(he_engine *h, void *stream);
 he_status he_score(he_engine *h, const int32_t *ids, int B, int L, int Lp, float *out_logprob,
                    void *stream);
 
+/* [RLHF-ch11] (the production generation setup there samples with a temperature
+ * and a nucleus cut-off and returns the log-probs PPO needs): sampled instead of
+ * greedy generation for the following he_generate* calls.  temperature 0 (the
+ * default) is greedy.  Otherwise, per sequence b and step k, with q_i =
+ * exp((l_i - max l) / temperature): the nucleus is every token with q_i >= tau,
+ * tau the largest value for which those tokens hold at least top_p of the sum of
+ * q (so ties at the boundary are in); the token is the argmax over the nucleus of
+ * (l_i - max l) / temperature - log(-log u_i), lowest index on ties, u_i in (0, 1)
+ * from SplitMix64 output number c + 1 started at `seed`, c = (b * 2^20 + k) * 2^20
+ * + i, u = (2 (z >> 41) + 1) / 2^24.  The reported log-prob (and he_score's) is
+ * log softmax(l / temperature) of the emitted token over the whole vocabulary.
+ * temperature >= 0 and finite, 0 < top_p <= 1, else HE_ERR_ARG. */
+he_status he_set_sampling(he_engine *h, float temperature, float top_p,
+                          unsigned long long seed);
+
 /* [HE-guide] enable_cuda_graph (§三 and the §四 field table: a CUDA-graph cache
  * for generation to cut launch overhead; off by default there and here).  With
  * enable != 0, he_generate and he_generate_host run the generation as one CUDA

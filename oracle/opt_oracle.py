@@ -24,7 +24,21 @@ What it computes, and from where:
   embedding layer.
 * "Chapter 11 System Architecture & Infrastructure at Scale", "The Generation
   Bottleneck: Quantitative Analysis": the generation step must hand back the
-  log-probabilities of the generated tokens (needed for the PPO ratio).
+  log-probabilities of the generated tokens (needed for the PPO ratio); the
+  production setup there samples with a temperature and a nucleus (top-p)
+  cut-off instead of taking the argmax.
+
+Sampling (``sample_token``; greedy when the temperature is 0).  Readings, where
+the page only names the two parameters: the sampling distribution is
+softmax(logits / T); the nucleus is the smallest set of most probable tokens whose
+probability reaches top_p, every token tied with the least probable member
+included; the token is drawn from the nucleus renormalised, as the argmax of
+log q_i + G_i over the nucleus (the Gumbel-max form of that draw, lowest index on
+ties), G_i = -log(-log u_i) with u_i from SplitMix64 (Steele, Lea and Flood,
+2014) used as a counter: u for (sequence b, step k, token i) comes from output
+number c + 1 of the generator seeded with the sampling seed, c = (b * 2^20 + k)
+* 2^20 + i, as (2 * (z >> 41) + 1) / 2^24 (never 0 or 1).  The reported log-prob
+is log softmax(logits / T) of the chosen token over the full vocabulary.
 
 Readings where the pages are silent (the plainest OPT reading):
 pre-LN decoder layers; LayerNorm with biased variance and eps 1e-5; learned
@@ -54,6 +68,48 @@ def to_f32(a: np.ndarray) -> np.ndarray:
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << 16).view(np.float32)
     return np.asarray(a, dtype=np.float32)
+
+
+_MASK64 = (1 << 64) - 1
+_GAMMA = 0x9E3779B97F4A7C15
+
+
+def splitmix64_output(seed: int, n: int) -> int:
+    """Output number n (n >= 1) of SplitMix64 started from state `seed`: the state
+    advances by the golden-ratio increment and each state is mixed."""
+    z = (seed + n * _GAMMA) & _MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK64
+    return z ^ (z >> 31)
+
+
+def sample_uniforms(seed: int, b: int, step: int, n_tokens: int) -> np.ndarray:
+    """u_i in (0, 1) for tokens 0 .. n_tokens-1 of (sequence b, step), fp64."""
+    base = ((b << 20) + step) << 20
+    return np.array([(2 * (splitmix64_output(seed, base + i + 1) >> 41) + 1) / float(1 << 24)
+                     for i in range(n_tokens)], dtype=np.float64)
+
+
+def sample_token(logits: np.ndarray, temperature: float, top_p: float, seed: int, b: int,
+                 step: int) -> tuple:
+    """One draw from softmax(logits / T) restricted to its top_p nucleus (see the
+    module notes); returns (token, log-prob of the token under softmax(logits / T))."""
+    lg = np.asarray(logits, dtype=np.float64)
+    z = (lg - lg.max()) / temperature
+    q = np.exp(z)
+    total = q.sum()
+    if top_p < 1.0:
+        order = np.argsort(-q, kind="stable")
+        mass = np.cumsum(q[order])
+        k = int(np.searchsorted(mass, top_p * total))  # first prefix reaching top_p
+        tau = q[order[min(k, len(order) - 1)]]
+        member = q >= tau
+    else:
+        member = np.ones_like(q, dtype=bool)
+    g = -np.log(-np.log(sample_uniforms(seed, b, step, len(q))))
+    score = np.where(member, z + g, -np.inf)
+    tok = int(np.argmax(score))  # first index of the maximum
+    return tok, float(z[tok] - np.log(total))
 
 
 def lora_delta(a: np.ndarray, b: np.ndarray, alpha: float, r: int) -> np.ndarray:
@@ -181,8 +237,9 @@ class OracleModel:
         return y @ self.tok_emb.T
 
     def generate(self, prompts: np.ndarray, gen_len: int, force_ids: np.ndarray | None = None,
-                 log_steps=()) -> tuple:
-        """Greedy generation of ``gen_len`` tokens per prompt.
+                 log_steps=(), sampling=None) -> tuple:
+        """Generation of ``gen_len`` tokens per prompt: greedy, or with ``sampling`` =
+        (temperature, top_p, seed) and temperature > 0 drawn by ``sample_token``.
 
         Step 0 is the head of the prefill pass (last prompt position); step k >= 1
         feeds token k-1's id at position Lp + k - 1.  With ``force_ids`` [B][gen_len]
@@ -202,12 +259,26 @@ class OracleModel:
             if k > 0:
                 x = self.forward(ids[:, k - 1:k].astype(np.int64), cache, lp + k - 1)
             lg = self.logits(x[:, 0])
-            tok = greedy(lg)
+            if sampling is not None and sampling[0] > 0:
+                drawn = [sample_token(lg[b], sampling[0], sampling[1], sampling[2], b, k)
+                         for b in range(bsz)]
+                tok = np.array([t for t, _ in drawn], dtype=np.int32)
+                lpk = np.array([v for _, v in drawn], dtype=np.float32)
+            else:
+                tok = greedy(lg)
+                lpk = None
             if force_ids is not None:
                 f = np.asarray(force_ids)[:, k]
-                tok = np.where(f >= 0, f, tok).astype(np.int32)
+                forced = f >= 0
+                tok = np.where(forced, f, tok).astype(np.int32)
+                if lpk is not None and forced.any():
+                    lpk = lpk.copy()
+                    t_inv = 1.0 / sampling[0]
+                    for b in np.nonzero(forced)[0]:
+                        zb = (lg[b].astype(np.float64) - lg[b].max()) * t_inv
+                        lpk[b] = zb[tok[b]] - np.log(np.exp(zb).sum())
             ids[:, k] = tok
-            lps[:, k] = log_softmax_pick(lg, tok)
+            lps[:, k] = log_softmax_pick(lg, tok) if lpk is None else lpk
             if k in log_steps:
                 logged[k] = lg.copy()
         return ids, lps, logged

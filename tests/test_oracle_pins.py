@@ -302,3 +302,58 @@ def test_logprob_identities():
     assert log_softmax_pick(lg, np.array([0]))[0] < log_softmax_pick(lg, np.array([2]))[0]
     assert math.isclose(float(log_softmax_pick(lg, np.array([2]))[0]),
                         2.0 - math.log(1 + math.e + math.e ** 2), abs_tol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Sampling (temperature + nucleus, counter-based SplitMix64 uniforms)
+# ---------------------------------------------------------------------------
+def test_sampler_rng_is_published_splitmix64():
+    from oracle import splitmix64_output
+    # Published SplitMix64 outputs for the initial state 1234567 (outputs 1..5).
+    assert [splitmix64_output(1234567, n) for n in range(1, 6)] == [
+        6457827717110365317, 3203168211198807973, 9817491932198370423,
+        4593380528125082431, 16408922859458223821]
+
+
+def _draws(logits, t, top_p, n_seq=40, n_step=100, seed=99):
+    from oracle import sample_token
+    counts = np.zeros(len(logits))
+    for b in range(n_seq):
+        for k in range(n_step):
+            tok, _ = sample_token(np.asarray(logits, np.float32), t, top_p, seed, b, k)
+            counts[tok] += 1
+    return counts / counts.sum()
+
+
+def test_sampler_frequencies_follow_tempered_softmax():
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    freq = _draws(np.log(p), 1.0, 1.0)
+    assert np.abs(freq - p).max() < 0.03, freq
+    # temperature 2: probabilities proportional to p^(1/2)
+    q = np.sqrt(p) / np.sqrt(p).sum()
+    freq = _draws(np.log(p), 2.0, 1.0)
+    assert np.abs(freq - q).max() < 0.03, freq
+    # a tiny temperature is the argmax
+    assert _draws(np.log(p), 1e-4, 1.0, n_seq=3, n_step=10)[0] == 1.0
+
+
+def test_sampler_nucleus():
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    # top_p 0.7: {0, 1} (0.5 < 0.7 <= 0.8), renormalised 0.625 / 0.375
+    freq = _draws(np.log(p), 1.0, 0.7)
+    assert freq[2] == 0 and freq[3] == 0 and abs(freq[0] - 0.625) < 0.03, freq
+    # a tie at the boundary joins the nucleus whole: 0.4 < 0.5 <= 0.7 cuts inside the tie
+    freq = _draws(np.log(np.array([0.4, 0.3, 0.3])), 1.0, 0.5)
+    assert (freq > 0.2).all(), freq
+    # top_p at or below the largest probability keeps the argmax alone
+    assert _draws(np.log(p), 1.0, 0.5, n_seq=5, n_step=20)[0] == 1.0
+
+
+def test_sampler_logprob_is_tempered_log_softmax():
+    from oracle import sample_token
+    rng = np.random.default_rng(3)
+    lg = rng.normal(size=64).astype(np.float32) * 3
+    for t in (0.5, 1.0, 1.7):
+        tok, lp = sample_token(lg, t, 0.9, 7, 1, 2)
+        ref = torch.log_softmax(torch.from_numpy(lg).double() / t, 0)[tok].item()
+        assert abs(lp - ref) < 1e-12
