@@ -388,8 +388,8 @@ def main():
     # (summaries under profiles/) by the ratio of measured to algorithmic bytes of the
     # captured launch: k_attn_decode at B=128, 40 heads, 384 keys (the average decode
     # launch here) and k_gemm_sk on the fc1 shape.  Set to None when the kernel changes.
-    traffic_ratio = {"attn_decode": (1.007986e9 + 4.340736e6) / 1.00663296e9,
-                     "gemm": (211.114496e6 + 6.177024e6) / 209.7152e6}
+    traffic_ratio = {"attn_decode": (1.007987e9 + 4.402432e6) / 1.00663296e9,
+                     "gemm": (211.110656e6 + 6.247168e6) / 209.7152e6}
     traffic = (pk["bytes_per_launch"] * traffic_ratio[dom]
                if pk["bytes_per_launch"] and dom in traffic_ratio else None)
     roofline = {"bound": "hbm",
