@@ -61,13 +61,14 @@ template <typename T, int HD, int UNROLL>
 __global__ void __launch_bounds__(128)
     k_attn_decode(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
                   T *__restrict__ ctx, int ctx_rows, int H, int max_seq, int n_keys, int per_split,
-                  float *__restrict__ part) {
+                  float *__restrict__ part, int *__restrict__ cnt) {
   constexpr int VEC = Vec16<T>::N;
   constexpr int LPK = HD / VEC;       // lanes per key row
   constexpr int GROUPS = 128 / LPK;   // key groups per CTA
   static_assert(LPK <= 32 && (32 % LPK) == 0, "a key row must fit in a warp");
   __shared__ float s_m[GROUPS], s_l[GROUPS];
   __shared__ float s_o[GROUPS][HD];
+  __shared__ int s_last;
 
   const int bh = blockIdx.x, sidx = blockIdx.y, nsplit = gridDim.y;
   const int b = bh / H, h = bh - b * H;
@@ -155,6 +156,33 @@ __global__ void __launch_bounds__(128)
         pp[HD] = M;
         pp[HD + 1] = L;
       }
+    }
+  }
+  if (nsplit > 1 && cnt) {
+    // The key slices of (b, h) are merged by whichever CTA finishes its slice last
+    // (a counter per (b, h), no waiting), in slice order, so the result does not
+    // depend on which one it is.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&cnt[bh], 1) == nsplit - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      if (threadIdx.x < HD) {
+        const int dd = threadIdx.x;
+        const float *pp = part + (long long)bh * nsplit * (HD + 2);
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(pp + s2 * (HD + 2) + HD));
+        float L = 0.f, O = 0.f;
+        for (int s2 = 0; s2 < nsplit; ++s2) {
+          const float ms = __ldcg(pp + s2 * (HD + 2) + HD);
+          const float w = ms == -INFINITY ? 0.f : expf(ms - M);
+          L = fmaf(__ldcg(pp + s2 * (HD + 2) + HD + 1), w, L);
+          O = fmaf(__ldcg(pp + s2 * (HD + 2) + dd), w, O);
+        }
+        ctx[act_index(b, h * HD + dd, H * HD, ctx_rows)] = from_f<T>(O / L);
+      }
+      if (threadIdx.x == 0) cnt[bh] = 0;  // every slice of (b, h) has arrived
     }
   }
 }
@@ -264,15 +292,16 @@ __global__ void __launch_bounds__(256)
 
 template <typename T, int HD>
 cudaError_t decode_t(const void *q, const void *kc, const void *vc, void *ctx, int ctx_rows, int B,
-                     int H, int max_seq, int n_keys, int split, float *part, cudaStream_t st) {
+                     int H, int max_seq, int n_keys, int split, float *part, int *cnt,
+                     cudaStream_t st) {
   const int per = (n_keys + split - 1) / split;
   const int ns = (n_keys + per - 1) / per;
   if (ns > 1 && !part) return cudaErrorInvalidValue;
   dim3 grid(B * H, ns);
   cudaError_t e = launch_k(k_attn_decode<T, HD, 4>, grid, dim3(128), 0, st, g_pdl, (const T *)q,
                            (const T *)kc, (const T *)vc, (T *)ctx, ctx_rows, H, max_seq, n_keys,
-                           per, part);
-  if (e == cudaSuccess && ns > 1)
+                           per, part, cnt);
+  if (e == cudaSuccess && ns > 1 && !cnt)
     e = launch_k(k_attn_combine<T, HD>, dim3(B * H), dim3(HD), 0, st, g_pdl, (const float *)part,
                  (T *)ctx, ctx_rows, H, ns);
   return e;
@@ -309,13 +338,16 @@ int attn_decode_pick_split(int B, int H, int n_keys, int num_sms) {
 
 cudaError_t launch_attn_decode(int act, const void *q, const void *kc, const void *vc,
                                void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
-                               int n_keys, int split, float *part, cudaStream_t st) {
+                               int n_keys, int split, float *part, cudaStream_t st, int *cnt) {
   if (n_keys <= 0 || split < 1) return cudaErrorInvalidValue;
   auto run = [&](auto tag) -> cudaError_t {
     using T = decltype(tag);
-    if (hd == 128) return decode_t<T, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 64) return decode_t<T, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
-    if (hd == 32) return decode_t<T, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, st);
+    if (hd == 128)
+      return decode_t<T, 128>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, cnt, st);
+    if (hd == 64)
+      return decode_t<T, 64>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, cnt, st);
+    if (hd == 32)
+      return decode_t<T, 32>(q, kc, vc, ctx, ctx_rows, B, H, max_seq, n_keys, split, part, cnt, st);
     return cudaErrorInvalidValue;
   };
   if (act == ACT_BF16) return run(bf16{});

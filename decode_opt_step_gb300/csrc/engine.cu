@@ -83,6 +83,7 @@ struct he_engine {
   // held for the engine's lifetime
   Buf err;
   Buf tilecnt;  // per-tile arrival counters of the stream-K fix-up (zero between GEMMs)
+  Buf attncnt;  // per-(sequence, head) counters of the decode attention's slice merge
   // LoRA restore copy (held while fused)
   Buf restore;
 
@@ -136,6 +137,9 @@ size_t tilecnt_bytes(const he_config &c) {
   if ((size_t)c.vocab > wide) wide = c.vocab;
   return (wide + 127) / 128 * sizeof(int);
 }
+
+// Attention slice-merge counters: one int per (sequence, head) pair.
+size_t attncnt_bytes(const he_config &c) { return (size_t)c.max_batch * c.n_heads * sizeof(int); }
 
 void free_workspace(he_engine *h, cudaStream_t st) {
   Buf *all[] = {&h->kc, &h->vc, &h->x, &h->h, &h->q, &h->ctx, &h->mid, &h->partial,
@@ -363,13 +367,15 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
             1);
   } else {
     const int n_keys = pos0 + 1;
+    // few (b, h) pairs: several key slices each, merged in-kernel by the last to finish
     int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
     if (split > kMaxAttnSplit) split = kMaxAttnSplit;
     Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
     c.check(launch_attn_decode(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, R,
                                B, cf.n_heads, hd, cf.max_seq, n_keys, split,
-                               static_cast<float *>(h->attn_part.p), c.st),
-            split > 1 ? 2 : 1);
+                               static_cast<float *>(h->attn_part.p), c.st,
+                               static_cast<int *>(h->attncnt.p)),
+            1);
   }
   // out projection -> partials; + bo + residual; LN2
   const void *wo[1] = {W(HE_PROJ_O)};
@@ -512,6 +518,7 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   // the GEMMs leave the tile counters at zero; clearing them here also recovers
   // from a call whose GEMM gave up on a wait part-way
   c.check(cudaMemsetAsync(h->tilecnt.p, 0, tilecnt_bytes(cf), st), 0);
+  c.check(cudaMemsetAsync(h->attncnt.p, 0, attncnt_bytes(cf), st), 0);
   // ---- prefill: all prompt tokens of all sequences in one pass ----
   const int M = B * Lp;
   {
@@ -720,14 +727,18 @@ he_status he_create(const he_config *cfg, const he_weights *w, const he_allocato
     delete h;
     return fail(HE_ERR_OOM, "error-flag allocation failed");
   }
-  if (!get(h, h->tilecnt, tilecnt_bytes(c), nullptr)) {
+  if (!get(h, h->tilecnt, tilecnt_bytes(c), nullptr) ||
+      !get(h, h->attncnt, attncnt_bytes(c), nullptr)) {
+    put(h, h->tilecnt, nullptr);
     put(h, h->err, nullptr);
     delete h;
-    return fail(HE_ERR_OOM, "tile-counter allocation failed");
+    return fail(HE_ERR_OOM, "counter allocation failed");
   }
   ce = cudaMemset(h->err.p, 0, 256);
   if (ce == cudaSuccess) ce = cudaMemset(h->tilecnt.p, 0, tilecnt_bytes(c));
+  if (ce == cudaSuccess) ce = cudaMemset(h->attncnt.p, 0, attncnt_bytes(c));
   if (ce != cudaSuccess) {
+    put(h, h->attncnt, nullptr);
     put(h, h->tilecnt, nullptr);
     put(h, h->err, nullptr);
     delete h;
@@ -735,6 +746,7 @@ he_status he_create(const he_config *cfg, const he_weights *w, const he_allocato
   }
   he_status s = take_workspace(h, nullptr);
   if (s != HE_OK) {
+    put(h, h->attncnt, nullptr);
     put(h, h->tilecnt, nullptr);
     put(h, h->err, nullptr);
     delete h;
@@ -751,6 +763,7 @@ he_status he_destroy(he_engine *h) {
   free_workspace(h, nullptr);
   put(h, h->restore, nullptr);
   put(h, h->tilecnt, nullptr);
+  put(h, h->attncnt, nullptr);
   put(h, h->err, nullptr);
   drop_graph(h);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);

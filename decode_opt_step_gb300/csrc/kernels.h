@@ -236,11 +236,14 @@ struct HeadArgs {
 cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st);
 
 // Decode attention: one query per (b, h) over keys 0..n_keys-1 of the cache.
-// part: scratch of B*H*split*(hd+2) floats when split > 1.
+// part: scratch of B*H*split*(hd+2) floats when split > 1; the slices are merged by a
+// second kernel, or, with cnt (B*H ints, zero at the launch and left zero), by the
+// last CTA of each (b, h) to finish.
 // act: type of q, K/V and ctx.  ctx is row-tiled with ctx_rows rows when ctx_rows > 0.
 cudaError_t launch_attn_decode(int act, const void *q, const void *kc, const void *vc,
                                void *ctx, int ctx_rows, int B, int H, int hd, int max_seq,
-                               int n_keys, int split, float *part, cudaStream_t st);
+                               int n_keys, int split, float *part, cudaStream_t st,
+                               int *cnt = nullptr);
 int attn_decode_pick_split(int B, int H, int n_keys, int num_sms);
 
 // Prefill attention: causal within each prompt of Lp tokens (positions 0..Lp-1).
