@@ -199,6 +199,68 @@ __global__ void k_resid_ln8(const float *partial, const SliceInfo si, long long 
   store8<OT>(h + act_index((int)r, c, d, h_rows), v);
 }
 
+// k_resid_ln8 for many rows (prefill): 128 threads per row, so that 16 rows are in
+// flight per SM; thread t owns the 8-element groups 8t + 1024 j (d % 1024 == 0).
+template <typename PT, typename OT, int NG>
+__global__ void __launch_bounds__(128)
+    k_resid_ln_rows(const float *partial, const SliceInfo si, long long split_stride, int ldp,
+                    const PT *bias, float *x, const PT *g, const PT *b, float eps, OT *h,
+                    int h_rows, int d) {
+  __shared__ float red[33];
+  pdl_wait();
+  pdl_trigger();
+  const long long r = blockIdx.x;
+  float v[NG][8];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    const int c = 8 * threadIdx.x + 1024 * j;
+    float bs[8];
+    load8<PT>(bias + c, bs);
+    float4 *xr = reinterpret_cast<float4 *>(x + r * d + c);
+    const float *pr = partial + r * ldp + c;
+    const int S = si.slices(c);
+    const float4 a0 = sum_slices(pr, S, split_stride);
+    const float4 a1 = sum_slices(pr + 4, S, split_stride);
+    float4 x0 = xr[0], x1 = xr[1];
+    x0.x += a0.x + bs[0];
+    x0.y += a0.y + bs[1];
+    x0.z += a0.z + bs[2];
+    x0.w += a0.w + bs[3];
+    x1.x += a1.x + bs[4];
+    x1.y += a1.y + bs[5];
+    x1.z += a1.z + bs[6];
+    x1.w += a1.w + bs[7];
+    xr[0] = x0;
+    xr[1] = x1;
+    v[j][0] = x0.x; v[j][1] = x0.y; v[j][2] = x0.z; v[j][3] = x0.w;
+    v[j][4] = x1.x; v[j][5] = x1.y; v[j][6] = x1.z; v[j][7] = x1.w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += v[j][i];
+  }
+  const float mean = block_sum(s, red) / (float)d;
+  float q = 0.f;
+#pragma unroll
+  for (int j = 0; j < NG; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[j][i] -= mean;
+      q += v[j][i] * v[j][i];
+    }
+  const float var = block_sum(q, red) / (float)d;
+  const float rstd = 1.0f / sqrtf(var + eps);
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    const int c = 8 * threadIdx.x + 1024 * j;
+    float gs[8], bt[8];
+    load8<PT>(g + c, gs);
+    load8<PT>(b + c, bt);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[j][i] = v[j][i] * rstd * gs[i] + bt[i];
+    store8<OT>(h + act_index((int)r, c, d, h_rows), v[j]);
+  }
+}
+
 // Element-wise epilogue after a split-K GEMM: four consecutive outputs per thread.
 template <typename PT, typename CT>
 __global__ void k_reduce_epi4(const float *partial, int split, long long split_stride, int ldp,
@@ -528,6 +590,28 @@ __global__ void k_copy1(uint8_t *dst, const uint8_t *src, long long n) {
   if (i < n) dst[i] = src[i];
 }
 
+template <typename PT, typename OT, int N>
+cudaError_t launch_resid_rows_n(const float *partial, const SliceInfo &si, long long split_stride,
+                                int ldp, const PT *bias, float *x, const PT *g, const PT *b,
+                                float eps, OT *h, int h_rows, int rows, int d, cudaStream_t st) {
+  return launch_k(k_resid_ln_rows<PT, OT, N>, dim3(rows), dim3(128), 0, st, g_pdl, partial, si,
+                  split_stride, ldp, bias, x, g, b, eps, h, h_rows, d);
+}
+
+template <typename PT, typename OT>
+cudaError_t launch_resid_rows(int ng, const float *partial, const SliceInfo &si,
+                              long long split_stride, int ldp, const PT *bias, float *x,
+                              const PT *g, const PT *b, float eps, OT *h, int h_rows, int rows,
+                              int d, cudaStream_t st) {
+#define HE_RL(N)                                                                          \
+  case N:                                                                                 \
+    return launch_resid_rows_n<PT, OT, N>(partial, si, split_stride, ldp, bias, x, g, b, eps, \
+                                          h, h_rows, rows, d, st);
+  switch (ng) { HE_RL(1) HE_RL(2) HE_RL(3) HE_RL(4) HE_RL(5) HE_RL(6) HE_RL(7) HE_RL(8) }
+#undef HE_RL
+  return cudaErrorInvalidValue;
+}
+
 int row_threads(int d) { return d >= 2048 ? 512 : (d >= 512 ? 256 : 128); }
 
 }  // namespace
@@ -572,7 +656,14 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
   const bool reg8 = dtype == HE_DTYPE_BF16 && d % 256 == 0 && d / 8 <= 1024 &&
                     (uintptr_t)bias % 16 == 0 && (uintptr_t)g % 16 == 0 &&
                     (uintptr_t)b % 16 == 0 && (uintptr_t)h % 16 == 0;
+  // many rows (prefill): four warps per row, up to 8 groups of 1024 elements
+  const int ng = d / 1024;
+  const bool rows4 = reg8 && rows >= 2048 && d % 1024 == 0 && ng >= 1 && ng <= 8;
   HE_DISPATCH_PT_CT(dtype, out_act, {
+    if (rows4)
+      return launch_resid_rows<PT, CT>(ng, partial, si, split_stride, ldp, (const PT *)bias, x,
+                                       (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows, rows,
+                                       d, st);
     if (reg8)
       return launch_k(k_resid_ln8<PT, CT>, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si,
                       split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
