@@ -29,3 +29,38 @@ def test_large_models_sampled_sequences(cuda_device, name):
     cfg = WORKLOADS[name]
     logit_err, lp_err = teacher_forced_check(cfg, torch, steps=STEPS, oracle_seqs=[0, 1])
     assert logit_err < BF16_LOGIT_TOL and lp_err < BF16_LP_TOL, (name, logit_err, lp_err)
+
+
+def test_opt125m_graph_replay_and_score(cuda_device):
+    """At the full OPT-125M size: the captured graph gives the direct launch's exact
+    ids and log-probs, and one he_score pass over prompt + answer reproduces the
+    decode path's log-probs within the log-prob bar (sequences 0 and 1 also against
+    the oracle, teacher-forced on the GPU's answers)."""
+    import numpy as np
+
+    from oracle import OracleModel
+    from synth.workloads import make_model, make_prompts
+    from tests.gpu_helpers import engine_for
+
+    cfg = WORKLOADS["opt-125m"]
+    inputs = make_model(cfg)
+    prompts_np = make_prompts(cfg)
+    prompts = torch.from_numpy(prompts_np).cuda()
+    L = cfg.gen_len
+    eng, _w = engine_for(cfg, inputs, torch)
+    eng.fuse_lora()
+    ids, lps = [t.clone() for t in eng.generate(prompts, L)]
+    eng.set_cuda_graph(True)
+    for _ in range(2):
+        ids_g, lps_g = eng.generate(prompts, L)
+        assert torch.equal(ids_g, ids) and torch.equal(lps_g.view(torch.int32), lps.view(torch.int32))
+    full = torch.cat([prompts, ids], dim=1).contiguous()
+    sc = eng.score(full, cfg.prompt_len)
+    torch.cuda.synchronize()
+    assert (sc - lps).abs().max().item() < BF16_LP_TOL
+    eng.unfuse_lora()
+    eng.close()
+    oracle = OracleModel(inputs, "merged")
+    answers = ids.cpu().numpy()[:2]
+    _, lps_o, _ = oracle.generate(prompts_np[:2], L, force_ids=answers)
+    assert np.abs(sc.cpu().numpy()[:2] - lps_o).max() < BF16_LP_TOL
