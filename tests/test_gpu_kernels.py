@@ -116,7 +116,10 @@ def test_linear_bf16_tiled_weights(cuda_device, M, N, K, split):
 @pytest.mark.parametrize("M,N,K,ctas", [(1, 128, 64, 0), (17, 384, 320, 0), (128, 1280, 1024, 0),
                                         (128, 640, 5120, 0), (200, 256, 512, 0), (64, 384, 640, -1),
                                         (5, 128, 640, -5), (33, 256, 192, -6), (128, 1280, 128, -7),
-                                        (9, 512, 1152, -13), (16, 15360, 256, 0)])
+                                        (9, 512, 1152, -13), (16, 15360, 256, 0),
+                                        # 15 runs on one tile: the owner's staged reduction
+                                        # does not fit, the register fallback finishes it
+                                        (128, 128, 2048, -15), (200, 128, 4096, -15)])
 @pytest.mark.parametrize("tiled", [False, True])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 def test_linear_16bit_stream_k(cuda_device, M, N, K, ctas, tiled, dt):
