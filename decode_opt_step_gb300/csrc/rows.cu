@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "rowops.cuh"
 
 namespace he {
 
@@ -64,32 +65,6 @@ __global__ void k_embed_ln(const int32_t *ids, int tok_per_seq, int pos0, const 
   ln_store<PT, CT>(row, d, g, b, eps, h, tok, 0, red);
 }
 
-// Sum of the split slices of one float4 of a row, in slice order (loads of four
-// slices are issued together; the additions keep the order 0, 1, 2, ...).
-__device__ __forceinline__ float4 sum_slices(const float *p, int split, long long stride) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = 0;
-  for (; s + 4 <= split; s += 4) {
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4 *>(p + (s + u) * stride));
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x += v[u].x;
-      acc.y += v[u].y;
-      acc.z += v[u].z;
-      acc.w += v[u].w;
-    }
-  }
-  for (; s < split; ++s) {
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(p + s * stride));
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  return acc;
-}
 
 // One block per row (d % 4 == 0, ldp % 4 == 0): x += sum of slices + bias, then LN.
 template <typename PT, typename OT>
@@ -117,60 +92,34 @@ __global__ void k_resid_ln(const float *partial, const SliceInfo si, long long s
   ln_store<PT, OT>(row, d, g, b, eps, h, (int)r, h_rows, red);
 }
 
-// Eight consecutive parameters (16-bit: one 16-byte load; fp32: two).
-template <typename PT>
-__device__ __forceinline__ void load8(const PT *p, float (&v)[8]) {
-  if constexpr (std::is_same<PT, float>::value) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
-    const PT *e = reinterpret_cast<const PT *>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = to_f<PT>(e[i]);
-  }
-}
-
-template <typename OT>
-__device__ __forceinline__ void store8(OT *p, const float (&v)[8]) {
-  if constexpr (std::is_same<OT, float>::value) {
-    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else {
-    uint4 u;
-    OT *e = reinterpret_cast<OT *>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) e[i] = from_f<OT>(v[i]);
-    *reinterpret_cast<uint4 *>(p) = u;
-  }
-}
 
 // k_resid_ln with the row held in registers: d / 8 threads (a multiple of 32),
 // thread t owns elements 8t .. 8t + 7, so the LN output leaves as one 16-byte
 // store into either layout of act_index (eight consecutive elements of a row stay
 // contiguous there).  Same arithmetic as k_resid_ln: slices summed in slot order,
 // then bias; mean, then the biased variance of the centred values.
-template <typename PT, typename OT>
-__global__ void k_resid_ln8(const float *partial, const SliceInfo si, long long split_stride,
+template <typename PT, typename OT, int MAXT>
+__global__ void __launch_bounds__(MAXT)
+    k_resid_ln8(const float *partial, const SliceInfo si, long long split_stride,
                             int ldp, const PT *bias, float *x, const PT *g, const PT *b, float eps,
                             OT *h, int h_rows, int d) {
   __shared__ float red[33];
   const int c = 8 * threadIdx.x;
-  float bs[8], gs[8], bt[8];
+  static_assert(sizeof(PT) == 2, "16-bit parameters");
+  float bs[8];
   load8<PT>(bias + c, bs);  // parameters do not depend on the kernel before this one
-  load8<PT>(g + c, gs);
-  load8<PT>(b + c, bt);
+  // gamma and beta stay packed (4 registers each) until the end
+  const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(g + c));
+  const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(b + c));
   pdl_wait();
   pdl_trigger();
   const long long r = blockIdx.x;
   float4 *xr = reinterpret_cast<float4 *>(x + r * d + c);
   const float *pr = partial + r * ldp + c;
   const int S = si.slices(c);
-  const float4 a0 = sum_slices(pr, S, split_stride);
-  const float4 a1 = sum_slices(pr + 4, S, split_stride);
   float4 x0 = xr[0], x1 = xr[1];
+  float4 a0, a1;
+  sum_slices8<4>(pr, S, split_stride, a0, a1);
   x0.x += a0.x + bs[0];
   x0.y += a0.y + bs[1];
   x0.z += a0.z + bs[2];
@@ -194,8 +143,9 @@ __global__ void k_resid_ln8(const float *partial, const SliceInfo si, long long 
   }
   const float var = block_sum(q, red) / (float)d;
   const float rstd = 1.0f / sqrtf(var + eps);
+  const PT *gp = reinterpret_cast<const PT *>(&graw), *bp = reinterpret_cast<const PT *>(&braw);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = v[i] * rstd * gs[i] + bt[i];
+  for (int i = 0; i < 8; ++i) v[i] = v[i] * rstd * to_f<PT>(gp[i]) + to_f<PT>(bp[i]);
   store8<OT>(h + act_index((int)r, c, d, h_rows), v);
 }
 
@@ -664,10 +614,16 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
       return launch_resid_rows<PT, CT>(ng, partial, si, split_stride, ldp, (const PT *)bias, x,
                                        (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows, rows,
                                        d, st);
-    if (reg8)
-      return launch_k(k_resid_ln8<PT, CT>, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si,
-                      split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
-                      (CT *)h, h_rows, d);
+    if constexpr (sizeof(PT) == 2) {
+      if (reg8) {
+        // register budget by row width (d / 8 threads)
+        auto k = d / 8 <= 512 ? k_resid_ln8<PT, CT, 512>
+                              : d / 8 <= 768 ? k_resid_ln8<PT, CT, 768> : k_resid_ln8<PT, CT, 1024>;
+        return launch_k(k, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si, split_stride, ldp,
+                        (const PT *)bias, x, (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows,
+                        d);
+      }
+    }
     return launch_k(k_resid_ln<PT, CT>, dim3(rows), dim3(row_threads(d)), sm, st, g_pdl, partial,
                     si, split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
                     (CT *)h, h_rows, d);
