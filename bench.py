@@ -237,9 +237,6 @@ def main():
     ap.add_argument("--no-cuda-graph", dest="cuda_graph", action="store_false",
                     help="launch every kernel directly instead of replaying the captured "
                          "CUDA graph of the generation (enable_cuda_graph)")
-    ap.add_argument("--decode-launch", default="separate", choices=["separate", "chained"],
-                    help="decode layers as separate launches (default) or as attention + one "
-                         "chained stream-K launch per layer (he_set_chained_decode)")
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -278,7 +275,6 @@ def main():
     eng = he.Engine(cfg, w, max_batch=B, max_seq=Lp + Lgen)
     if args.cuda_graph:
         eng.set_cuda_graph(True)
-    eng.set_chained_decode(args.decode_launch == "chained")
     if args.sampling:
         t_s, p_s, seed_s = args.sampling.split(",")
         eng.set_sampling(float(t_s), float(p_s), int(seed_s))
@@ -417,8 +413,7 @@ def main():
                        "launch": ("one CUDA graph per generation" if args.cuda_graph
                                   else "direct launches, programmatic dependent launch"),
                        "decoding": (f"sampled (temperature, top_p, seed = {args.sampling})"
-                                    if args.sampling else "greedy"),
-                       "decode_launch": args.decode_launch},
+                                    if args.sampling else "greedy")},
             "clocks": clk, "gpu_launches": launches,
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
             "decode": {"ms": dec_ms, "bytes_per_step_avg": dec_total / (Lgen - 1),

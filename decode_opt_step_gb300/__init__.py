@@ -87,7 +87,6 @@ _SIGNATURES = {
     "he_retake_workspace": (c_int, [c_void_p, c_void_p]),
     "he_set_profiling": (c_int, [c_void_p, c_uint]),
     "he_set_cuda_graph": (c_int, [c_void_p, c_int]),
-    "he_set_chained_decode": (c_int, [c_void_p, c_int]),
     "he_set_sampling": (c_int, [c_void_p, ctypes.c_float, ctypes.c_float, ctypes.c_uint64]),
     "he_score": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_get_stats": (c_int, [c_void_p, POINTER(HeStats)]),
@@ -269,10 +268,6 @@ class Engine:
     def set_cuda_graph(self, enable: bool = True):
         """Run he_generate / he_generate_host as a captured, cached CUDA graph."""
         _check(self._lib.he_set_cuda_graph(self._h, 1 if enable else 0))
-
-    def set_chained_decode(self, enable: bool = True):
-        """Decode layers as attention + one chained stream-K launch (on by default)."""
-        _check(self._lib.he_set_chained_decode(self._h, 1 if enable else 0))
 
     def set_profiling(self, classes=()):
         """Time the given kernel classes (names from KCLASS, or "all"); () turns it off."""

@@ -76,7 +76,6 @@ struct he_engine {
 
   bool taken = false, fused = false;
   bool tiled = false;  // projections hold the tiled layout (bf16 path while fused)
-  bool chain_on = true;  // he_set_chained_decode
   int act = 0;         // activation type of the generation in flight (ActType)
   unsigned prof_mask = 0;
   // workspace (released / retaken together)
@@ -132,15 +131,12 @@ void put(he_engine *h, Buf &b, cudaStream_t st) {
   b.bytes = 0;
 }
 
-// Stream-K tile counters: one int per 128-row tile of the widest projection (a
-// multiple of four), then the grid-barrier arrival counter of the chained decode
-// launches; all zero at the start of a generation.
-size_t tile_counters(const he_config &c) {
+// Stream-K tile counters: one int per 128-row tile of the widest projection.
+size_t tilecnt_bytes(const he_config &c) {
   size_t wide = (size_t)(3 * c.d_model > c.ffn ? 3 * c.d_model : c.ffn);
   if ((size_t)c.vocab > wide) wide = c.vocab;
-  return ((wide + 127) / 128 + 3) / 4 * 4;
+  return (wide + 127) / 128 * sizeof(int);
 }
-size_t tilecnt_bytes(const he_config &c) { return (tile_counters(c) + 4) * sizeof(int); }
 
 // Attention slice-merge counters: one int per (sequence, head) pair.
 size_t attncnt_bytes(const he_config &c) { return (size_t)c.max_batch * c.n_heads * sizeof(int); }
@@ -233,7 +229,6 @@ struct Ctx {
   he_engine *h;
   cudaStream_t st;
   cudaError_t e = cudaSuccess;
-  unsigned bar_arrivals = 0;  // grid-barrier arrivals of the chained launches so far
   void check(cudaError_t r, int launches) {
     if (e == cudaSuccess && r != cudaSuccess) e = r;
     h->stats.launches += launches;
@@ -343,31 +338,6 @@ Epi qkv_epi(he_engine *h, int layer, int tok_per_seq, int pos0) {
 // One decoder layer over M tokens (prefill: M = B*Lp, tok_per_seq = Lp, pos0 = 0;
 // decode: M = B, tok_per_seq = 1, pos0 = t).  Input h = LN1(x); output h = LN1 of
 // the next layer (or the final LN after the last layer).
-// Attention of layer l over the q / K / V cache its QKV projection wrote.
-void attention(Ctx &c, int l, int B, int tok_per_seq, int pos0, bool prefill) {
-  he_engine *h = c.h;
-  const he_config &cf = h->cfg;
-  const int hd = cf.d_model / cf.n_heads;
-  const size_t lay = (size_t)l * h->kv_layer_elems() * h->elem;
-  if (prefill) {
-    Timed t(h, HE_KCLASS_PREFILL_ATTN, c.st);
-    c.check(launch_attn_prefill(h->act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
-                                tok_per_seq, cf.n_heads, hd, cf.max_seq, c.st),
-            1);
-  } else {
-    const int n_keys = pos0 + 1;
-    // few (b, h) pairs: several key slices each, merged in-kernel by the last to finish
-    int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
-    if (split > kMaxAttnSplit) split = kMaxAttnSplit;
-    Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
-    c.check(launch_attn_decode(h->act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p,
-                               act_rows(h, B, true), B, cf.n_heads, hd, cf.max_seq, n_keys, split,
-                               static_cast<float *>(h->attn_part.p), c.st,
-                               static_cast<int *>(h->attncnt.p)),
-            1);
-  }
-}
-
 void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool prefill) {
   he_engine *h = c.h;
   const he_config &cf = h->cfg;
@@ -388,7 +358,25 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw, act);
   Epi ep{};
   ep.kind = EPI_PARTIAL;
-  attention(c, l, B, tok_per_seq, pos0, prefill);
+  // attention
+  const size_t lay = (size_t)l * h->kv_layer_elems() * h->elem;
+  if (prefill) {
+    Timed t(h, HE_KCLASS_PREFILL_ATTN, c.st);
+    c.check(launch_attn_prefill(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
+                                tok_per_seq, cf.n_heads, hd, cf.max_seq, c.st),
+            1);
+  } else {
+    const int n_keys = pos0 + 1;
+    // few (b, h) pairs: several key slices each, merged in-kernel by the last to finish
+    int split = attn_decode_pick_split(B, cf.n_heads, n_keys, h->num_sms);
+    if (split > kMaxAttnSplit) split = kMaxAttnSplit;
+    Timed t(h, HE_KCLASS_ATTN_DECODE, c.st);
+    c.check(launch_attn_decode(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, R,
+                               B, cf.n_heads, hd, cf.max_seq, n_keys, split,
+                               static_cast<float *>(h->attn_part.p), c.st,
+                               static_cast<int *>(h->attncnt.p)),
+            1);
+  }
   // out projection -> partials; + bo + residual; LN2
   const void *wo[1] = {W(HE_PROJ_O)};
   SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw, act);
@@ -419,142 +407,6 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
                           lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
                           h->h.p, R, M, d, c.st),
           1);
-}
-
-// A decode projection as one phase of a chained stream-K launch (the stream-K
-// branch of gemm(): element-wise epilogues finish inside the kernel); *si tells the
-// rows phase after an EPI_PARTIAL projection how its slices are organised.
-ChainPhase chain_gemm(he_engine *h, const void *x, const void *const *w, int n_groups,
-                      int group_rows, int B, int K, const Epi &epi, SliceInfo *si) {
-  ChainPhase p{};
-  p.kind = PH_GEMM;
-  GemmArgs &a = p.g;
-  a.dtype = h->cfg.dtype;
-  a.act = h->act;
-  a.x = x;
-  a.ldx = K;
-  for (int g = 0; g < n_groups; ++g) a.w[g] = w[g];
-  a.n_groups = n_groups;
-  a.group_rows = group_rows;
-  a.M = B;
-  a.N = n_groups * group_rows;
-  a.K = K;
-  a.split = 1;
-  a.w_tiled = h->tiled;
-  a.epi = epi;
-  const bool fix = sk_fixup_ok(a);
-  p.P = sk_ctas(a, h->num_sms, fix);
-  const long long U = sk_units(a), T = (a.N + 127) / 128;
-  p.slices = static_cast<float *>(h->partial.p);
-  p.slice_stride = fix ? (long long)B * T * 128 : (long long)B * a.N;
-  p.tile_cnt = fix ? static_cast<int *>(h->tilecnt.p) : nullptr;
-  if (si) *si = SliceInfo{0, U, (int)(U / T), p.P};
-  return p;
-}
-
-// The residual + LayerNorm after an EPI_PARTIAL projection as a rows phase.
-ChainPhase chain_rows(he_engine *h, int B, const SliceInfo &si, const void *bias, const void *g,
-                      const void *b, int out_act) {
-  const he_config &cf = h->cfg;
-  ChainPhase p{};
-  p.kind = PH_ROWS;
-  p.partial = static_cast<const float *>(h->partial.p);
-  p.si = si;
-  p.split_stride = (long long)B * cf.d_model;
-  p.ldp = cf.d_model;
-  p.bias = bias;
-  p.gamma = g;
-  p.beta = b;
-  p.x = static_cast<float *>(h->x.p);
-  p.eps = cf.ln_eps;
-  p.h = h->h.p;
-  p.h_rows = act_rows(h, B, true);
-  p.d = cf.d_model;
-  p.out_act = out_act;
-  return p;
-}
-
-const void *proj_w(const he_engine *h, int l, int p) {
-  return h->tiled ? h->fused_w[(size_t)l * HE_N_PROJ + p] : h->layers[l].w[p];
-}
-
-// Whether decode runs chained: per layer the attention, then one stream-K launch of
-// out projection, residual + LayerNorm, fc1, fc2, residual + LayerNorm and the next
-// layer's QKV projection (bf16 workloads whose projections all take the in-kernel
-// completion).
-bool use_chain(he_engine *h, int B) {
-  const he_config &cf = h->cfg;
-  const int d = cf.d_model;
-  if (!h->chain_on || cf.dtype != HE_DTYPE_BF16 || B > 256 || d % 256 || d > 8192 ||
-      cf.ffn % 128 || cf.n_layers < 1)
-    return false;
-  if (!use_stream_k(h, B, 3 * d, d, true, h->tiled) || !use_stream_k(h, B, cf.ffn, d, true, h->tiled) ||
-      !use_stream_k(h, B, d, cf.ffn, true, h->tiled))
-    return false;
-  // the rows phases read parameters 16 bytes at a time (as k_resid_ln8 does)
-  auto al = [](const void *p) { return (uintptr_t)p % 16 == 0; };
-  if (!al(h->lnf_g) || !al(h->lnf_b)) return false;
-  for (const he_layer_weights &lw : h->layers)
-    if (!al(lw.b[HE_PROJ_O]) || !al(lw.b[HE_PROJ_FC2]) || !al(lw.ln1_g) || !al(lw.ln1_b) ||
-        !al(lw.ln2_g) || !al(lw.ln2_b))
-      return false;
-  const void *w3[3] = {proj_w(h, 0, HE_PROJ_Q), proj_w(h, 0, HE_PROJ_K), proj_w(h, 0, HE_PROJ_V)};
-  Epi er{};
-  er.kind = EPI_RELU;
-  er.bias[0] = h->layers[0].b[HE_PROJ_FC1];
-  er.out = h->mid.p;
-  er.ldo = cf.ffn;
-  er.out_rows = act_rows(h, B, true);
-  const void *w1[1] = {proj_w(h, 0, HE_PROJ_FC1)};
-  return sk_fixup_ok(chain_gemm(h, h->h.p, w3, 3, d, B, d, qkv_epi(h, 0, 1, 0), nullptr).g) &&
-         sk_fixup_ok(chain_gemm(h, h->h.p, w1, 1, cf.ffn, B, d, er, nullptr).g);
-}
-
-// One decode step's layers, chained (use_chain): layer 0's QKV projection, then per
-// layer the attention and one launch of the rest (with the next layer's QKV).
-void decode_layers_chained(Ctx &c, int B, int pos0) {
-  he_engine *h = c.h;
-  const he_config &cf = h->cfg;
-  const int d = cf.d_model, act = h->act, G = h->num_sms;
-  unsigned *gbar = reinterpret_cast<unsigned *>(static_cast<int *>(h->tilecnt.p) + tile_counters(cf));
-  {
-    const void *w3[3] = {proj_w(h, 0, HE_PROJ_Q), proj_w(h, 0, HE_PROJ_K), proj_w(h, 0, HE_PROJ_V)};
-    gemm(c, HE_KCLASS_GEMM, h->h.p, d, w3, 3, d, B, d, qkv_epi(h, 0, 1, pos0), true, h->tiled, act);
-  }
-  for (int l = 0; l < cf.n_layers; ++l) {
-    const he_layer_weights &lw = h->layers[l];
-    const bool last = l == cf.n_layers - 1;
-    attention(c, l, B, 1, pos0, false);
-    ChainPhase ph[kMaxPhases];
-    int n = 0;
-    SliceInfo si;
-    Epi ep{};
-    ep.kind = EPI_PARTIAL;
-    const void *wo[1] = {proj_w(h, l, HE_PROJ_O)};
-    ph[n++] = chain_gemm(h, h->ctx.p, wo, 1, d, B, d, ep, &si);
-    ph[n++] = chain_rows(h, B, si, lw.b[HE_PROJ_O], lw.ln2_g, lw.ln2_b, act);
-    Epi er{};
-    er.kind = EPI_RELU;
-    er.bias[0] = lw.b[HE_PROJ_FC1];
-    er.out = h->mid.p;
-    er.ldo = cf.ffn;
-    er.out_rows = act_rows(h, B, true);
-    const void *w1[1] = {proj_w(h, l, HE_PROJ_FC1)};
-    ph[n++] = chain_gemm(h, h->h.p, w1, 1, cf.ffn, B, d, er, nullptr);
-    const void *w2[1] = {proj_w(h, l, HE_PROJ_FC2)};
-    ph[n++] = chain_gemm(h, h->mid.p, w2, 1, d, B, cf.ffn, ep, &si);
-    // the last layer's final LayerNorm feeds the LM head (the embedding table's type)
-    ph[n++] = chain_rows(h, B, si, lw.b[HE_PROJ_FC2], last ? h->lnf_g : h->layers[l + 1].ln1_g,
-                         last ? h->lnf_b : h->layers[l + 1].ln1_b, last ? cf.dtype : act);
-    if (!last) {
-      const void *w3[3] = {proj_w(h, l + 1, HE_PROJ_Q), proj_w(h, l + 1, HE_PROJ_K),
-                           proj_w(h, l + 1, HE_PROJ_V)};
-      ph[n++] = chain_gemm(h, h->h.p, w3, 3, d, B, d, qkv_epi(h, l + 1, 1, pos0), nullptr);
-    }
-    Timed t(h, HE_KCLASS_GEMM, c.st);
-    c.check(launch_gemm_chain(ph, n, G, gbar, c.bar_arrivals, static_cast<int *>(h->err.p), c.st), 1);
-    c.bar_arrivals += (unsigned)((n - 1) * G);
-  }
 }
 
 // Logits [B][vocab] (fp32, h->logits) of B row-major rows of the last LayerNorm's
@@ -683,13 +535,9 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
        out_lp, log_map, logits_out);
   record_phase(h, 1, st);
   // ---- decode: token k is fed at position Lp + k - 1 ----
-  const bool chained = use_chain(h, B);
   for (int k = 1; k < Lgen; ++k) {
     const int t = Lp + k - 1;
-    if (chained)
-      decode_layers_chained(c, B, t);
-    else
-      for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, B, 1, t, false);
+    for (int l = 0; l < cf.n_layers; ++l) layer_forward(c, l, B, B, 1, t, false);
     head(c, h->h.p, d, B, k, Lp, Lgen, force, out_ids, out_lp, log_map, logits_out);
   }
   record_phase(h, 2, st);
@@ -744,8 +592,7 @@ he_status generate_internal(he_engine *h, int B, int Lp, int Lgen, cudaStream_t 
       reinterpret_cast<const void *>((uintptr_t)Lgen), reinterpret_cast<const void *>((uintptr_t)act),
       h->kc.p, h->vc.p, h->x.p, h->h.p, h->q.p, h->ctx.p, h->mid.p, h->partial.p, h->logits.p,
       h->attn_part.p, h->ids_in.p, h->ids_out.p, h->lp_out.p, h->err.p, h->tilecnt.p,
-      h->restore.p, reinterpret_cast<const void *>((uintptr_t)h->chain_on),
-      reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
+      h->restore.p, reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
       reinterpret_cast<const void *>((uintptr_t)float_bits(h->top_p)),
       reinterpret_cast<const void *>((uintptr_t)h->seed)};
   if (!h->gexec || key != h->gkey) {
@@ -1092,13 +939,6 @@ he_status he_set_cuda_graph(he_engine *h, int enable) {
   cudaSetDevice(h->device);
   h->graph_on = enable != 0;
   if (!h->graph_on) drop_graph(h);
-  return HE_OK;
-}
-
-he_status he_set_chained_decode(he_engine *h, int enable) {
-  g_err.clear();
-  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
-  h->chain_on = enable != 0;
   return HE_OK;
 }
 

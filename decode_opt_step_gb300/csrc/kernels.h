@@ -186,39 +186,6 @@ bool sk_fixup_ok(const GemmArgs &a);
 // 128 * ceil(N / 128).
 cudaError_t launch_gemm_sk(const GemmArgs &a, int P, float *slices, long long slice_stride,
                            int *tile_cnt, int *dev_err, cudaStream_t st);
-
-// Phases of one launch of the stream-K kernel (launch_gemm_chain), run in order
-// with a grid barrier between consecutive phases.
-enum : int { PH_GEMM = 0, PH_ROWS = 1 };
-constexpr int kMaxPhases = 6;  // phases per launch
-constexpr int kMaxMaps = 6;    // tensor maps (row-major weight groups) per launch
-struct ChainPhase {
-  int kind;
-  // PH_GEMM: a projection as launch_gemm_sk takes it (all of one launch: the same
-  // M, act and sk_kps; P <= the launch's CTA count)
-  GemmArgs g;
-  int P;
-  float *slices;
-  long long slice_stride;
-  int *tile_cnt;
-  // PH_ROWS: the residual + LayerNorm of k_resid_ln8 on the g.M rows (bf16 parameters;
-  // d % 256 == 0, d <= 8192; out_act is the launch's act or ACT_BF16)
-  const float *partial;
-  SliceInfo si;
-  long long split_stride;
-  int ldp;
-  const void *bias, *gamma, *beta;
-  float *x;
-  float eps;
-  void *h;
-  int h_rows, d, out_act;
-};
-// One launch of G CTAs (G <= resident CTAs: one per SM) running n phases.  *gbar
-// counts grid-barrier arrivals (G per phase boundary); it is zero at the start of
-// the sequence of launches that share it, and bar_base is the number of arrivals of
-// the launches before this one.  Results are those of the separate launches.
-cudaError_t launch_gemm_chain(const ChainPhase *ph, int n, int G, unsigned *gbar,
-                              unsigned bar_base, int *dev_err, cudaStream_t st);
 int gemm_pick_split(const GemmArgs &a, int num_sms);  // heuristic for decode shapes
 
 cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int split,

@@ -347,11 +347,10 @@ __device__ __forceinline__ float tile_row_bias(const Epi &e, int n, int N) {
 // other S - 1 runs' fp32 slices in global memory (tile-contiguous: tslices +
 // s * sstride + tok * 128 + feature), once they have all counted themselves in
 // *cnt.  Runs on the NT (256) epilogue threads, two per TMEM lane (et and et +
-// 128 take alternate W-column chunks), after the CTA's last MMA of the tile, in
-// `avail` bytes of pipeline shared memory at `stage` that the caller has made
-// free: per chunk of ch tokens the other slices come in as one bulk copy each
-// (completing on the mbarrier `bar`, whose next phase parity `phase` tracks
-// across calls), each thread adds its row's values in slot order (its own
+// 128 take alternate W-column chunks), after the CTA's
+// last MMA, so the pipeline's shared memory `stage` (avail bytes) is free: per
+// chunk of ch tokens the other slices come in as one bulk copy each (completing
+// on the mbarrier `bar`), each thread adds its row's values in slot order (its own
 // slice is slot 0) and applies the epilogue into a [token][128] fp32 staging
 // tile, which then leaves (rounded to the output type) as 16-byte stores.  `bias`
 // is this thread's row's (tile_row_bias).  `flag` is a shared int; returns with
@@ -361,8 +360,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
                                                     long long sstride, int N, int M, int t, int S,
                                                     uint32_t tl, bool live, int *cnt,
                                                     uint8_t *stage, int avail, uint64_t *bar,
-                                                    uint32_t &phase, int *flag, int *dev_err,
-                                                    float bias) {
+                                                    int *flag, int *dev_err, float bias) {
   static_assert(NT == 256, "two threads per TMEM lane");
   const int et = threadIdx.x, r = et & 127, hf = et >> 7;  // row (feature) of the tile, half
   const int n_row = t * 128 + r;
@@ -387,6 +385,7 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
   const int ch = tile_stage_tokens(S, M, W, avail);
   float *ps = reinterpret_cast<float *>(stage);      // [S-1][ch][128] other slices
   uint8_t *os = stage + (size_t)(S - 1) * ch * 512;  // [ch][128] fp32 outputs
+  uint32_t phase = 0;
   for (int c0 = 0; c0 < M; c0 += ch) {
     const int cn = min(ch, M - c0);
     if (go && S > 1) {

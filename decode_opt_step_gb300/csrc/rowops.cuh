@@ -1,5 +1,5 @@
-// Row helpers shared by the residual + LayerNorm kernels and the rows phase of the
-// chained stream-K kernel (both must give the same bits).
+// Row helpers of the residual + LayerNorm kernels: the slice sums (in slot order, so
+// every variant gives the same bits) and 16-byte parameter loads / output stores.
 #pragma once
 #include <type_traits>
 

@@ -272,18 +272,6 @@ he_status he_set_sampling(he_engine *h, float temperature, float top_p,
  * profiling on, launch directly.  enable == 0 frees the cached graph. */
 he_status he_set_cuda_graph(he_engine *h, int enable);
 
-/* [DSC-gen] (generation is bound by memory bandwidth) -- how decode is launched,
- * not what it computes.  With enable != 0 (the default) a bf16 decode step runs
- * each layer as two launches: the attention, then one persistent stream-K launch
- * of the out projection, residual + LayerNorm, fc1, fc2, residual + LayerNorm
- * and the next layer's QKV projection, separated by grid barriers, so the weight
- * stream does not pause at kernel boundaries.  The arithmetic is that of the
- * separate launches (enable == 0), so the results are bit-identical.  Shapes the
- * chained launch does not take (d_model % 256 != 0 or > 8192, more than 256
- * sequences, the fp32 workload) run the separate launches either way.  A change
- * re-captures the CUDA graph of he_set_cuda_graph. */
-he_status he_set_chained_decode(he_engine *h, int enable);
-
 /* Per-kernel-class event timing of he_generate: class_mask has bit c set for
  * every HE_KCLASS_c to time (0 = off, the default).  Costs two events per
  * timed launch; the totals of the last he_generate appear in he_stats. */
