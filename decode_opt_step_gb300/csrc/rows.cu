@@ -105,12 +105,16 @@ __global__ void __launch_bounds__(MAXT)
                             OT *h, int h_rows, int d) {
   __shared__ float red[33];
   const int c = 8 * threadIdx.x;
-  static_assert(sizeof(PT) == 2, "16-bit parameters");
   float bs[8];
   load8<PT>(bias + c, bs);  // parameters do not depend on the kernel before this one
-  // gamma and beta stay packed (4 registers each) until the end
-  const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(g + c));
-  const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(b + c));
+  // gamma and beta stay packed (4 registers each for 16-bit parameters) until the end
+  constexpr int PW = sizeof(PT) / 2;  // 16-byte words per 8 parameters
+  uint4 graw[PW], braw[PW];
+#pragma unroll
+  for (int k = 0; k < PW; ++k) {
+    graw[k] = __ldg(reinterpret_cast<const uint4 *>(g + c) + k);
+    braw[k] = __ldg(reinterpret_cast<const uint4 *>(b + c) + k);
+  }
   pdl_wait();
   pdl_trigger();
   const long long r = blockIdx.x;
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(MAXT)
   }
   const float var = block_sum(q, red) / (float)d;
   const float rstd = 1.0f / sqrtf(var + eps);
-  const PT *gp = reinterpret_cast<const PT *>(&graw), *bp = reinterpret_cast<const PT *>(&braw);
+  const PT *gp = reinterpret_cast<const PT *>(graw), *bp = reinterpret_cast<const PT *>(braw);
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = v[i] * rstd * to_f<PT>(gp[i]) + to_f<PT>(bp[i]);
   store8<OT>(h + act_index((int)r, c, d, h_rows), v);
@@ -329,50 +333,39 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   pdl_trigger();
   const int b = blockIdx.x;
   const float *lg = a.logits + (long long)b * a.ldl;
-  float best = -INFINITY;
+  // One pass over the row: per thread the maximum with its lowest index (an ascending
+  // scan keeps the first hit of a value) and sum exp(l - max), rescaled when the
+  // maximum grows; 16-byte loads where the row allows.
+  float best = -INFINITY, se = 0.f;
   int bidx = 0x7fffffff;
-  for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) {
-    const float v = lg[i];
-    if (v > best) {  // strided ascending scan: first hit of a value keeps the lowest index
+  auto take = [&](float v, int i) {
+    if (v > best) {
+      se = se * expf(best - v) + 1.f;  // (0 while best is -inf)
       best = v;
       bidx = i;
+    } else {
+      se += expf(v - best);
     }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-    if (ov > best || (ov == best && oi < bidx)) {
-      best = ov;
-      bidx = oi;
+  };
+  int done = 0;
+  if (a.ldl % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0) {
+    const int n4 = a.vocab / 4;
+    const float4 *l4 = reinterpret_cast<const float4 *>(lg);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+      const float4 v = l4[i];
+      take(v.x, 4 * i);
+      take(v.y, 4 * i + 1);
+      take(v.z, 4 * i + 2);
+      take(v.w, 4 * i + 3);
     }
+    done = 4 * n4;
   }
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (lane == 0) {
-    s_val[wid] = best;
-    s_idx[wid] = bidx;
-  }
-  __syncthreads();
-  if (wid == 0) {
-    best = lane < nw ? s_val[lane] : -INFINITY;
-    bidx = lane < nw ? s_idx[lane] : 0x7fffffff;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-      if (ov > best || (ov == best && oi < bidx)) {
-        best = ov;
-        bidx = oi;
-      }
-    }
-    if (lane == 0) {
-      s_val[0] = best;
-      s_idx[0] = bidx;
-    }
-  }
-  __syncthreads();
-  const float m = s_val[0];
-  const int amax = s_idx[0] == 0x7fffffff ? 0 : s_idx[0];
+  // the scalar rest (indices above every vector one: the scan stays ascending)
+  for (int i = done + threadIdx.x; i < a.vocab; i += blockDim.x) take(lg[i], i);
+  const float tmax = best, tse = se;
+  block_argmax(best, bidx, s_val, s_idx);
+  const float m = best;
+  const int amax = bidx == 0x7fffffff ? 0 : bidx;
   if (a.temperature > 0.f) {
     // ---- sampling: q_i = exp((l_i - m) / T), nucleus {q_i >= tau}, Gumbel-max ----
     const float inv_t = 1.f / a.temperature;
@@ -422,9 +415,7 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
       s_tok = tok;
     }
   } else {
-    float se = 0.f;
-    for (int i = threadIdx.x; i < a.vocab; i += blockDim.x) se += expf(lg[i] - m);
-    se = block_sum(se, red);
+    const float se = block_sum(tmax == -INFINITY ? 0.f : tse * expf(tmax - m), red);
     if (threadIdx.x == 0) {
       int tok = amax;
       if (a.force_ids) {
@@ -614,15 +605,14 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
       return launch_resid_rows<PT, CT>(ng, partial, si, split_stride, ldp, (const PT *)bias, x,
                                        (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows, rows,
                                        d, st);
-    if constexpr (sizeof(PT) == 2) {
-      if (reg8) {
-        // register budget by row width (d / 8 threads)
-        auto k = d / 8 <= 512 ? k_resid_ln8<PT, CT, 512>
-                              : d / 8 <= 768 ? k_resid_ln8<PT, CT, 768> : k_resid_ln8<PT, CT, 1024>;
-        return launch_k(k, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si, split_stride, ldp,
-                        (const PT *)bias, x, (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows,
-                        d);
-      }
+    if (reg8) {
+      // register budget by row width (d / 8 threads)
+      auto k = d / 8 <= 512   ? k_resid_ln8<PT, CT, 512>
+               : d / 8 <= 640 ? k_resid_ln8<PT, CT, 640>
+               : d / 8 <= 768 ? k_resid_ln8<PT, CT, 768>
+                              : k_resid_ln8<PT, CT, 1024>;
+      return launch_k(k, dim3(rows), dim3(d / 8), 0, st, g_pdl, partial, si, split_stride, ldp,
+                      (const PT *)bias, x, (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows, d);
     }
     return launch_k(k_resid_ln<PT, CT>, dim3(rows), dim3(row_threads(d)), sm, st, g_pdl, partial,
                     si, split_stride, ldp, (const PT *)bias, x, (const PT *)g, (const PT *)b, eps,
