@@ -1,8 +1,10 @@
 // Prefill (causal) attention for bf16 or fp16 on tensor cores (mma.sync m16n8k16, fp32
 // accumulation), flash-style: one CTA = 4 warps = 64 queries of one (b, h); key
 // and value blocks of 64 rows are staged in shared memory (rows padded by 16
-// bytes so ldmatrix reads are conflict-free); scores, the running softmax and
-// the output stay in registers.  Scores S = Q K^T use ldmatrix fragments of Q
+// bytes so ldmatrix reads are conflict-free), two blocks in flight: the next
+// block's asynchronous copies (cp.async) run while the current one is used; the
+// query tile passes through the second buffer first.  Scores, the running softmax
+// and the output stay in registers.  Scores S = Q K^T use ldmatrix fragments of Q
 // (A, row-major) and K (B, "col" = K rows); the probabilities are re-packed from
 // the S accumulators into A fragments for O += P V, with V read by ldmatrix.trans.
 #include <type_traits>
@@ -51,22 +53,31 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Copies a [64][HD] bf16 tile (rows r0.., row stride `ld` elements, rows >= nrows
-// zero) into shared memory with row stride HD + 8.
+// Asynchronous copy of a [64][HD] 16-bit tile (row stride `ld` elements; rows >= nrows
+// are zero-filled, reading nothing) into shared memory with row stride HD + 8; one
+// 16-byte cp.async per chunk, completed by cp.async.wait_group.
 template <int HD>
-__device__ __forceinline__ void load_tile(uint16_t *dst, const uint16_t *src, long long ld,
-                                          int nrows) {
+__device__ __forceinline__ void load_tile_async(uint16_t *dst, const uint16_t *src, long long ld,
+                                                int nrows) {
   constexpr int CH = HD / 8;  // 16-byte chunks per row
+#pragma unroll
   for (int e = threadIdx.x; e < 64 * CH; e += 128) {
     const int r = e / CH, c = e - r * CH;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < nrows) v = *reinterpret_cast<const uint4 *>(src + r * ld + c * 8);
-    *reinterpret_cast<uint4 *>(dst + r * (HD + 8) + c * 8) = v;
+    const bool ok = r < nrows;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     smem_u32(dst + r * (HD + 8) + c * 8)),
+                 "l"(src + (ok ? (long long)r * ld : 0) + c * 8), "r"(ok ? 16 : 0)
+                 : "memory");
   }
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 3)  // three CTAs (and their 70 KB of tiles) per SM
     k_attn_prefill_mma(const uint16_t *__restrict__ q, const uint16_t *__restrict__ kc,
                        const uint16_t *__restrict__ vc, T *__restrict__ ctx, int H, int Lp,
                        int max_seq) {
@@ -74,9 +85,9 @@ __global__ void __launch_bounds__(128)
   constexpr int KS = HD / 16;  // k-steps of Q K^T
   constexpr int DT = HD / 8;   // 8-wide output tiles
   extern __shared__ __align__(16) uint8_t smraw[];
-  uint16_t *qs = reinterpret_cast<uint16_t *>(smraw);
-  uint16_t *ks = qs + 64 * LD;
-  uint16_t *vs = ks + 64 * LD;
+  // two (K, V) buffers of 64 x LD each; the query tile is staged in buffer 1's K
+  uint16_t *const kbuf0 = reinterpret_cast<uint16_t *>(smraw);
+  const int bstride = 2 * 64 * LD;  // elements per (K, V) buffer
   const int qb = blockIdx.x, bh = blockIdx.y;
   const int b = bh / H, h = bh - b * H;
   const int d = H * HD;
@@ -85,7 +96,13 @@ __global__ void __launch_bounds__(128)
   const long long row0 = ((long long)b * H + h) * max_seq;
 
   pdl_wait();
-  load_tile<HD>(qs, q + ((long long)b * Lp + qb * 64) * d + h * HD, d, Lp - qb * 64);
+  uint16_t *qs = kbuf0 + bstride;
+  load_tile_async<HD>(qs, q + ((long long)b * Lp + qb * 64) * d + h * HD, d, Lp - qb * 64);
+  cp_commit();
+  load_tile_async<HD>(kbuf0, kc + row0 * HD, HD, min(64, Lp));
+  load_tile_async<HD>(kbuf0 + 64 * LD, vc + row0 * HD, HD, min(64, Lp));
+  cp_commit();
+  cp_wait<1>();  // this thread's query copies
   __syncthreads();
   // Q fragments of this warp's 16 rows, all k-steps
   uint32_t qa[KS][4];
@@ -95,6 +112,7 @@ __global__ void __launch_bounds__(128)
     const int c = kk * 16 + 8 * (lane >> 4);
     ldm_x4(qa[kk], qs + r * LD + c);
   }
+  __syncthreads();  // buffer 1 is free for key block 1
   float o[DT][4];
 #pragma unroll
   for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -103,11 +121,19 @@ __global__ void __launch_bounds__(128)
   const int tq1 = tq0 + 8;
 
   for (int kb = 0; kb <= qb; ++kb) {
-    __syncthreads();
-    const int nk = min(64, Lp - kb * 64);
-    load_tile<HD>(ks, kc + (row0 + kb * 64) * HD, HD, nk);
-    load_tile<HD>(vs, vc + (row0 + kb * 64) * HD, HD, nk);
-    __syncthreads();
+    if (kb < qb) {  // the next key block into the other buffer, then wait for this one
+      uint16_t *nb = kbuf0 + ((kb + 1) & 1) * bstride;
+      const int nk = min(64, Lp - (kb + 1) * 64);
+      load_tile_async<HD>(nb, kc + (row0 + (kb + 1) * 64) * HD, HD, nk);
+      load_tile_async<HD>(nb + 64 * LD, vc + (row0 + (kb + 1) * 64) * HD, HD, nk);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();  // every thread's copies of this block have landed
+    const uint16_t *ks = kbuf0 + (kb & 1) * bstride;
+    const uint16_t *vs = ks + 64 * LD;
     // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
     float s[8][4];
 #pragma unroll
@@ -181,6 +207,7 @@ __global__ void __launch_bounds__(128)
         mma_16<T>(o[2 * dp + 1], pa, vf[2], vf[3]);
       }
     }
+    __syncthreads();  // this buffer is refilled at the next block
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -202,7 +229,7 @@ __global__ void __launch_bounds__(128)
 template <typename T, int HD>
 cudaError_t run(const void *q, const void *kc, const void *vc, void *ctx, int B, int Lp, int H,
                 int max_seq, cudaStream_t st) {
-  const size_t sm = (size_t)3 * 64 * (HD + 8) * sizeof(uint16_t);
+  const size_t sm = (size_t)4 * 64 * (HD + 8) * sizeof(uint16_t);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_mma<T, HD>,
