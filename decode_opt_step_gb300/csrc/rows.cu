@@ -469,42 +469,51 @@ __global__ void k_lora_fuse(T *w, const T *A, const T *Bm, T *save, int rows, in
   for (int e = 0; e < 8; ++e) wp[e] = from_f<T>(to_f<T>(wv[e]) + scale * delta[e]);
 }
 
-// One 16-byte chunk of the tiled output per thread: chunk q of tile t holds row
-// r = (q % 1024) / 8, logical 16-byte column chunk (q % 8) ^ (r % 8).
+// The tiled output in 16-byte chunks: chunk q of tile t holds row r = (q % 1024) / 8,
+// logical 16-byte column chunk (q % 8) ^ (r % 8).
 template <typename OT>
-__global__ void k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows,
-                             int cols, int r, float scale) {
-  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nchunks = (long long)rows * cols / 8;
-  if (q >= nchunks) return;
+__global__ void __launch_bounds__(256, 4)
+    k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows, int cols,
+                 int r, float scale) {
+  // One CTA per 128 x 64 tile (1024 chunks).  Thread x takes chunks x + 256 i, i < 4:
+  // rows rr + 32 i of the tile, all with the same column chunk c (the same 16 bytes
+  // of each row of A, cached); the four weight loads are in flight together.
+  const long long t = blockIdx.x;
   const int KT = cols / 64;
-  const long long t = q >> 10;
-  const int rr = (int)((q & 1023) >> 3), slot = (int)(q & 7);
+  const int rr = threadIdx.x >> 3, slot = threadIdx.x & 7;
   const int c = slot ^ (rr & 7);
-  const int n = (int)(t / KT) * 128 + rr;
-  const int k0 = (int)(t % KT) * 64 + c * 8;
-  const uint4 raw = *reinterpret_cast<const uint4 *>(src + (long long)n * cols + k0);
-  const bf16 *wv = reinterpret_cast<const bf16 *>(&raw);
-  float delta[8] = {};
-  if (!A) {
-    if constexpr (sizeof(OT) == 2 && std::is_same<OT, bf16>::value) {
-      out[q] = raw;  // plain re-tiling keeps the bits
+  const int n0 = (int)(t / KT) * 128 + rr, k0 = (int)(t % KT) * 64 + c * 8;
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    raw[i] = *reinterpret_cast<const uint4 *>(src + (long long)(n0 + 32 * i) * cols + k0);
+  uint4 *o = out + t * 1024 + threadIdx.x;
+  const bool lora = A != nullptr && r > 0;
+  if constexpr (std::is_same<OT, bf16>::value) {
+    if (!lora) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[256 * i] = raw[i];  // plain re-tiling keeps the bits
       return;
     }
-    r = 0;
   }
-  for (int j = 0; j < r; ++j) {
-    const float bj = __bfloat162float(Bm[(long long)n * r + j]);
-    const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
-    const bf16 *ap = reinterpret_cast<const bf16 *>(&av);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
+  for (int i = 0; i < 4; ++i) {  // one chunk at a time: eight accumulators live
+    float delta[8] = {};
+    const long long brow = (long long)(n0 + 32 * i) * r;
+    for (int j = 0; j < (lora ? r : 0); ++j) {
+      const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
+      const bf16 *ap = reinterpret_cast<const bf16 *>(&av);
+      const float bj = __bfloat162float(Bm[brow + j]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
+    }
+    const bf16 *wv = reinterpret_cast<const bf16 *>(&raw[i]);
+    uint4 res;
+    OT *rp = reinterpret_cast<OT *>(&res);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(__bfloat162float(wv[e]) + scale * delta[e]);
+    o[256 * i] = res;
   }
-  uint4 res;
-  OT *rp = reinterpret_cast<OT *>(&res);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(__bfloat162float(wv[e]) + scale * delta[e]);
-  out[q] = res;
 }
 
 __global__ void k_tile_act(const uint16_t *x, int M, int K, int ldx, int R, uint16_t *out) {
@@ -666,8 +675,9 @@ cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const voi
                               const void *bm, int rows, int cols, int r, float scale,
                               cudaStream_t st) {
   if (rows % 128 || cols % 64) return cudaErrorInvalidValue;
-  const long long n = (long long)rows * cols / 8;
-  const int blocks = (int)((n + 255) / 256);
+  const long long tiles = (long long)(rows / 128) * (cols / 64);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int blocks = (int)tiles;
   if (out_act == ACT_F16)
     k_fuse_tiled<f16><<<blocks, 256, 0, st>>>((uint4 *)out, (const bf16 *)src, (const bf16 *)a,
                                               (const bf16 *)bm, rows, cols, r, scale);
