@@ -235,7 +235,6 @@ struct Ctx {
   }
 };
 
-inline const char *at(const void *p, size_t off) { return static_cast<const char *>(p) + off; }
 inline char *at(void *p, size_t off) { return static_cast<char *>(p) + off; }
 
 // Decode projections on bf16 run the persistent stream-K kernel when the shape
