@@ -208,18 +208,48 @@ def reduce_max(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
+
+
+def working_set_bytes(cfg):
+    """Parameters plus the KV cache of one full generation (what a step streams)."""
+    elem = 4 if cfg.dtype == "f32" else 2
+    params = (cfg.n_layers * (layer_weight_bytes(cfg, elem)
+                              + (4 * cfg.d_model + 2 * cfg.ffn + 4 * cfg.d_model) * elem)
+              + (cfg.vocab + cfg.max_pos + cfg.pos_offset) * cfg.d_model * elem)
+    kv = 2 * cfg.n_layers * cfg.batch * (cfg.prompt_len + cfg.gen_len) * cfg.d_model * elem
+    return params + kv
+
+
+def flushes_l2(cfg) -> bool:
+    """Whether a step writes an L2-sized buffer first (working sets below 2x L2)."""
+    return working_set_bytes(cfg) < 2 * L2_BYTES
+
+
+def compute_dtype(cfg) -> str:
+    return "f32" if cfg.dtype == "f32" else "f16"
+
+
 def workload_config(cfg):
+    ws = working_set_bytes(cfg)
+    if cfg.dtype == "f32":
+        precision = "fp32 weights, activations, KV cache and arithmetic (CUDA cores)"
+    else:
+        precision = ("bf16 model weights; generation reads them as fp16 (merged with LoRA "
+                     "while fused), with fp16 activations and KV cache and fp32 accumulation; "
+                     "LayerNorm, softmax, logits and log-probs fp32; the tied LM head reads "
+                     "the bf16 embedding")
+    l2 = (f"working set {ws / 1e9:.2f} GB, larger than L2: weights and KV cache stream from "
+          "HBM every step" if not flushes_l2(cfg) else
+          f"working set {ws / 1e6:.1f} MB fits in L2: every step first writes a 256 MiB "
+          "buffer to flush L2")
     return {"workload": f"{cfg.name} greedy generation",
             "layers": cfg.n_layers, "d_model": cfg.d_model, "heads": cfg.n_heads,
             "ffn": cfg.ffn, "vocab": cfg.vocab, "batch": cfg.batch,
             "prompt_len": cfg.prompt_len, "gen_len": cfg.gen_len,
             "lora": f"r={cfg.lora_r} alpha={int(cfg.lora_alpha)} on q,k,v,out,fc1,fc2",
             "step": "fuse + prefill + decode + unfuse + release/retake workspace",
-            "l2": "inputs larger than L2 (weights and KV cache stream from HBM every step)",
-            "precision": ("bf16 model weights; while LoRA is fused the merged weights, "
-                          "activations and KV cache are fp16 with fp32 accumulation; "
-                          "LayerNorm, softmax, logits and log-probs fp32; the tied LM head "
-                          "reads the bf16 embedding")}
+            "l2": l2, "precision": precision}
 
 
 def main():
@@ -282,7 +312,12 @@ def main():
     ids = torch.empty((B, Lgen), dtype=torch.int32, device=dev)
     lps = torch.empty((B, Lgen), dtype=torch.float32, device=dev)
 
+    flush = (torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+             if flushes_l2(cfg) else None)
+
     def step():
+        if flush is not None:
+            flush.fill_(1)
         eng.fuse_lora()
         eng.generate(prompts, Lgen, out=(ids, lps))
         eng.unfuse_lora()
@@ -361,6 +396,8 @@ def main():
         barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
             eng.fuse_lora()
             eng.generate_host(hp, Lgen)  # H2D prompts, generate, D2H ids + log-probs, sync
             eng.unfuse_lora()
@@ -407,7 +444,8 @@ def main():
     metric = METRIC if cfg.name == "opt-13b" else f"{cfg.name} generated tokens/s (B={B}, {Lp}+{Lgen})"
     line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": compute_dtype(cfg),
             "data": "synthetic (N(0,0.02) weights and LoRA factors, uniform prompt ids)",
             "config": {**workload_config(cfg),
                        "launch": ("one CUDA graph per generation" if args.cuda_graph

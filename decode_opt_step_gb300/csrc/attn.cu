@@ -312,13 +312,8 @@ cudaError_t prefill_t(const void *q, const void *kc, const void *vc, void *ctx, 
                       int H, int max_seq, cudaStream_t st) {
   constexpr int LD = HD + 1;
   const size_t sm = (size_t)(64 * LD * 3 + 64 * 65) * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<T, HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_smem_limit<k_attn_prefill<T, HD>>((int)sm);
+  if (e != cudaSuccess) return e;
   dim3 grid((Lp + 63) / 64, B * H);
   k_attn_prefill<T, HD><<<grid, 256, sm, st>>>((const T *)q, (const T *)kc, (const T *)vc,
                                                (T *)ctx, H, Lp, max_seq);

@@ -230,13 +230,8 @@ template <typename T, int HD>
 cudaError_t run(const void *q, const void *kc, const void *vc, void *ctx, int B, int Lp, int H,
                 int max_seq, cudaStream_t st) {
   const size_t sm = (size_t)4 * 64 * (HD + 8) * sizeof(uint16_t);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_mma<T, HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_smem_limit<k_attn_prefill_mma<T, HD>>((int)sm);
+  if (e != cudaSuccess) return e;
   dim3 grid((Lp + 63) / 64, B * H);
   return launch_k(k_attn_prefill_mma<T, HD>, grid, dim3(128), sm, st, g_pdl, (const uint16_t *)q,
                   (const uint16_t *)kc, (const uint16_t *)vc, (T *)ctx, H, Lp, max_seq);

@@ -86,6 +86,9 @@ struct he_engine {
   Buf attncnt;  // per-(sequence, head) counters of the decode attention's slice merge
   // LoRA restore copy (held while fused)
   Buf restore;
+  // BF16 without LoRA fused: the caller's projections as fp16 in the tiled layout,
+  // rewritten at the start of every generation (taken with the workspace)
+  Buf base;
 
   he_stats stats{};
   cudaEvent_t ph[7] = {};  // generate begin/prefill end/end, fuse begin/end, unfuse begin/end
@@ -143,8 +146,13 @@ size_t attncnt_bytes(const he_config &c) { return (size_t)c.max_batch * c.n_head
 
 void free_workspace(he_engine *h, cudaStream_t st) {
   Buf *all[] = {&h->kc, &h->vc, &h->x, &h->h, &h->q, &h->ctx, &h->mid, &h->partial,
-                &h->logits, &h->attn_part, &h->ids_in, &h->ids_out, &h->lp_out, &h->logmap};
+                &h->logits, &h->attn_part, &h->ids_in, &h->ids_out, &h->lp_out, &h->logmap,
+                &h->base};
   for (Buf *b : all) put(h, *b, st);
+  if (!h->fused) {
+    h->fused_w.clear();
+    h->tiled = false;
+  }
   h->taken = false;
   h->stats.workspace_bytes = 0;
   h->stats.kv_bytes = 0;
@@ -494,6 +502,53 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   c.check(launch_head_select(cf.dtype, h->act, ha, c.st), 1);
 }
 
+// Total bytes of the six projections of every layer in the config's dtype.
+size_t all_proj_bytes(const he_engine *h) {
+  const he_config &c = h->cfg;
+  return (size_t)c.n_layers * (4 * (size_t)c.d_model * c.d_model + 2 * (size_t)c.d_model * c.ffn) *
+         h->elem;
+}
+
+// BF16 engines always generate in fp16 from tiled projections.  While LoRA is fused
+// those are he_fuse_lora's merged copies; otherwise every generation first re-tiles
+// the caller's bf16 weights to fp16 into h->base (bf16 activations lose accuracy
+// with depth; the weights may have changed since the last call).  prepare_base takes
+// the buffer, outside any stream capture; retile_base enqueues the conversion.
+he_status prepare_base(he_engine *h, cudaStream_t st) {
+  const he_config &c = h->cfg;
+  if (c.dtype != HE_DTYPE_BF16 || h->fused) return HE_OK;
+  if (!h->base.p && !get(h, h->base, all_proj_bytes(h), st))
+    return fail(HE_ERR_OOM, "fp16 copy of the projections (%zu bytes) failed", all_proj_bytes(h));
+  h->fused_w.assign((size_t)c.n_layers * HE_N_PROJ, nullptr);
+  size_t off = 0;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      h->fused_w[(size_t)l * HE_N_PROJ + p] = at(h->base.p, off);
+      const size_t rows = p == HE_PROJ_FC1 ? c.ffn : c.d_model;
+      const size_t cols = p == HE_PROJ_FC2 ? c.ffn : c.d_model;
+      off += rows * cols * h->elem;
+    }
+  h->tiled = true;
+  return HE_OK;
+}
+
+void retile_base(Ctx &c) {
+  he_engine *h = c.h;
+  const he_config &cf = h->cfg;
+  if (cf.dtype != HE_DTYPE_BF16 || h->fused) return;
+  for (int l = 0; l < cf.n_layers; ++l)
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      const int rows = p == HE_PROJ_FC1 ? cf.ffn : cf.d_model;
+      const int cols = p == HE_PROJ_FC2 ? cf.ffn : cf.d_model;
+      c.check(launch_fuse_tiled(const_cast<void *>(h->fused_w[(size_t)l * HE_N_PROJ + p]), ACT_F16,
+                                h->layers[l].w[p], nullptr, nullptr, rows, cols, 0, 0.f, c.st),
+              1);
+    }
+}
+
+// Activation type of a generation: fp32 engines fp32, bf16 engines fp16.
+int gen_act(const he_engine *h) { return h->cfg.dtype == HE_DTYPE_F32 ? ACT_F32 : ACT_F16; }
+
 // Phase events: recorded as graph nodes while a generation is being captured.
 void record_phase(he_engine *h, int i, cudaStream_t st) {
   if (h->capturing)
@@ -508,11 +563,11 @@ he_status generate_impl(he_engine *h, const int32_t *prompt, int B, int Lp, int 
   const he_config &cf = h->cfg;
   const int d = cf.d_model;
   Ctx c{h, st};
-  // activation type: fp32 workload -> fp32; bf16 workload -> fp16 while fused (the
-  // fused weights are fp16), else bf16 (the caller's bf16 weights as they are)
-  h->act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
+  if (cf.dtype == HE_DTYPE_BF16 && !h->tiled) return fail(HE_ERR_STATE, "projections not prepared");
+  h->act = gen_act(h);
   for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
   ensure_phase_events(h);
+  retile_base(c);  // unfused bf16: this call's fp16 copy of the caller's weights
   record_phase(h, 0, st);
   // the GEMMs leave the tile counters at zero; clearing them here also recovers
   // from a call whose GEMM gave up on a wait part-way
@@ -584,14 +639,14 @@ he_status generate_internal(he_engine *h, int B, int Lp, int Lgen, cudaStream_t 
   float *lp_out = static_cast<float *>(h->lp_out.p);
   if (!h->graph_on || h->prof_mask)
     return generate_impl(h, ids_in, B, Lp, Lgen, ids_out, lp_out, nullptr, nullptr, nullptr, st);
-  const he_config &cf = h->cfg;
-  const int act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
+  const int act = gen_act(h);
   std::vector<const void *> key = {
       reinterpret_cast<const void *>((uintptr_t)B), reinterpret_cast<const void *>((uintptr_t)Lp),
       reinterpret_cast<const void *>((uintptr_t)Lgen), reinterpret_cast<const void *>((uintptr_t)act),
       h->kc.p, h->vc.p, h->x.p, h->h.p, h->q.p, h->ctx.p, h->mid.p, h->partial.p, h->logits.p,
       h->attn_part.p, h->ids_in.p, h->ids_out.p, h->lp_out.p, h->err.p, h->tilecnt.p,
-      h->restore.p, reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
+      h->restore.p, h->base.p, reinterpret_cast<const void *>((uintptr_t)h->fused),
+      reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
       reinterpret_cast<const void *>((uintptr_t)float_bits(h->top_p)),
       reinterpret_cast<const void *>((uintptr_t)h->seed)};
   if (!h->gexec || key != h->gkey) {
@@ -797,6 +852,9 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
   for (int l = 0; l < c.n_layers; ++l)
     for (int p = 0; p < HE_N_PROJ; ++p)
       if (fuse_touches(h, p)) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
+  put(h, h->base, st);  // the unfused generations' fp16 copy: the fused one replaces it
+  h->fused_w.clear();
+  h->tiled = false;
   if (!get(h, h->restore, total, st))
     return fail(HE_ERR_OOM, "LoRA fuse buffer of %zu bytes failed", total);
   ensure_phase_events(h);
@@ -906,6 +964,8 @@ he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, in
   if (s != HE_OK) return s;
   cudaSetDevice(h->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = prepare_base(h, st);
+  if (s != HE_OK) return s;
   cudaError_t e = cudaMemcpyAsync(h->ids_in.p, prompt_ids, (size_t)B * Lp * 4,
                                   cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "prompt copy");
@@ -951,6 +1011,8 @@ he_status he_generate_ex(he_engine *h, const int32_t *prompt_ids, int B, int Lp,
     return fail(HE_ERR_ARG, "n_rows > 0 needs log_rows and logits_out");
   cudaSetDevice(h->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = prepare_base(h, st);
+  if (s != HE_OK) return s;
   const int32_t *log_map = nullptr;
   if (n_rows > 0) {
     std::vector<int32_t> map((size_t)Lgen * B, -1);
@@ -1014,9 +1076,12 @@ he_status he_score(he_engine *h, const int32_t *ids, int B, int L, int Lp, float
     e = cudaMemcpy2DAsync(targets, (size_t)Lgen * 4, ids + Lp, (size_t)L * 4, (size_t)Lgen * 4, B,
                           cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "token copy");
+  he_status ps = prepare_base(h, st);
+  if (ps != HE_OK) return ps;
   Ctx c{h, st};
-  h->act = cf.dtype == HE_DTYPE_F32 ? ACT_F32 : (h->fused ? ACT_F16 : ACT_BF16);
+  h->act = gen_act(h);
   for (int k = 0; k < kClasses; ++k) h->prof_used[k] = 0;
+  retile_base(c);
   c.check(cudaMemsetAsync(h->tilecnt.p, 0, tilecnt_bytes(cf), st), 0);
   // one pass over tokens 0 .. L-2 of every sequence (the prefill kernels)
   {
@@ -1059,6 +1124,8 @@ he_status he_generate_host(he_engine *h, const int32_t *prompt_ids, int B, int L
   if (s != HE_OK) return s;
   cudaSetDevice(h->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = prepare_base(h, st);
+  if (s != HE_OK) return s;
   cudaError_t e = cudaMemcpyAsync(h->ids_in.p, prompt_ids, (size_t)B * Lp * 4,
                                   cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "prompt upload");

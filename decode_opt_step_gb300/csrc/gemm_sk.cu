@@ -369,13 +369,8 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.slices = slices;
   a.slice_stride = slice_stride;
   a.tile_cnt = tile_cnt;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_sk<CT, BN, STAGES, KPS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t ae = ensure_smem_limit<k_gemm_sk<CT, BN, STAGES, KPS>>(C::SMEM);
+  if (ae != cudaSuccess) return ae;
   return launch_k(k_gemm_sk<CT, BN, STAGES, KPS>, dim3(P), dim3(SK_THREADS), C::SMEM, st, g_pdl, tw[0],
                   tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
 }

@@ -432,13 +432,8 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   }
   wt.kt = a.K / BK;
   if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN, tmap_type<CT>())) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<CT, BN, STAGES, ABULK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t ae = ensure_smem_limit<k_gemm_tc<CT, BN, STAGES, ABULK>>(C::SMEM);
+  if (ae != cudaSuccess) return ae;
   const int kb_total = (a.K + BK - 1) / BK;
   const int kb_per_split = split_kblocks(a.K, a.split);
   if (effective_split(a.K, a.split) != a.split) return cudaErrorInvalidValue;
@@ -464,13 +459,8 @@ cudaError_t launch_tcp(const GemmArgs &a, int num_sms, int *dev_err, cudaStream_
   }
   wt.kt = a.K / BK;
   if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, PBN, tmap_type<CT>())) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<CT, ABULK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t ae = ensure_smem_limit<k_gemm_tcp<CT, ABULK>>(C::SMEM);
+  if (ae != cudaSuccess) return ae;
   const int kb_total = (a.K + BK - 1) / BK;
   const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
   const int MT = a.N / BM + (a.N % BM != 0), NT = (a.M + PBN - 1) / PBN;

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace he {
 
 // Activation / operand types (values 0 and 1 double as the parameter dtype).
@@ -51,6 +53,22 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
     cfg.numAttrs = 1;
   }
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Raises Kernel's dynamic shared-memory limit to `bytes` on the current device, once
+// per (kernel, device): the attribute is per device, so an engine on a second GPU
+// of the process sets it again.  Concurrent first calls may both set it (harmless).
+template <auto Kernel>
+inline cudaError_t ensure_smem_limit(int bytes) {
+  static std::atomic<unsigned long long> done{0};  // bit d: device d is set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // Whether decode-path kernels are launched with programmatic dependent launch.

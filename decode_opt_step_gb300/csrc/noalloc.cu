@@ -3,16 +3,18 @@
 // caller-provided buffer.
 //
 // Why: some callers of this library cannot allocate device memory at the moment
-// they need the attention.  Code recorded into a CUDA graph must not call
-// cudaMalloc / cudaFree while capturing; runtimes whose device memory is owned by
-// a pooling allocator or a fixed budget cannot hand out an extra buffer on
-// demand; and latency-critical loops avoid cudaMalloc because it can synchronise
-// the device.  This entry point needs nothing from them but inputs and outputs.
+// they need the attention.  Runtimes whose device memory is owned by a pooling
+// allocator or a fixed budget cannot hand out an extra buffer on demand; plugins
+// hosted by another framework may have no allocator of their own; and
+// latency-critical loops avoid cudaMalloc because it can synchronise the device.
+// This entry point needs nothing from them but inputs and outputs.
 //
 // The scratch is one file-scope __device__ array, so every GPU that loads the
 // library holds it (kNoAllocScratchFloats floats, 16 MiB) until the process ends.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/he.h"
@@ -26,8 +28,48 @@ constexpr long long kNoAllocScratchFloats = 4LL * 1024 * 1024;  // 16 MiB of fp3
 static __device__ __align__(256) float g_attn_partials[kNoAllocScratchFloats];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_addr_mu;
-float *g_addr[kMaxDevices] = {};  // device address of g_attn_partials, per device
+
+// The array's device address is looked up once per device with that device
+// current, and kept with the context it was looked up in: a later call in another
+// context of the same ordinal (after cudaDeviceReset, say) looks it up again.
+// The address is stored before its context, so a reader that finds its context
+// also finds that context's address.
+struct ScratchAddr {
+  std::atomic<CUcontext> ctx{nullptr};
+  std::atomic<float *> addr{nullptr};
+};
+ScratchAddr g_scratch[kMaxDevices];
+std::mutex g_lookup_mu;  // serialises the lookups, not the reads
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Device address of g_attn_partials in the current context, or null.
+float *scratch_address(int dev) {
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  CUcontext cur = nullptr;
+  if (!get_ctx || get_ctx(&cur) != CUDA_SUCCESS || !cur) return nullptr;
+  ScratchAddr &s = g_scratch[dev];
+  if (s.ctx.load(std::memory_order_acquire) == cur) return s.addr.load(std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lock(g_lookup_mu);
+  if (s.ctx.load(std::memory_order_acquire) == cur) return s.addr.load(std::memory_order_relaxed);
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_attn_partials) != cudaSuccess || !p) return nullptr;
+  s.addr.store(static_cast<float *>(p), std::memory_order_relaxed);
+  s.ctx.store(cur, std::memory_order_release);
+  return static_cast<float *>(p);
+}
 
 }  // namespace
 
@@ -53,18 +95,12 @@ extern "C" he_status he_op_attn_decode_noalloc(int dtype, const void *q, const v
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return he::set_error(HE_ERR_CUDA, "cudaGetDevice failed");
-  float *part = nullptr;
-  {
-    // First call on a device: look up the array's device address (with that device
-    // current).  This is host-side set-up only; it allocates nothing.
-    std::lock_guard<std::mutex> lock(g_addr_mu);
-    if (!g_addr[dev]) {
-      void *p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_attn_partials) != cudaSuccess || !p)
-        return he::set_error(HE_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed");
-      g_addr[dev] = static_cast<float *>(p);
-    }
-    part = g_addr[dev];
+  // First call on a device (or in a new context): look up the array's device
+  // address with that device current.  Host-side set-up only; it allocates nothing.
+  float *part = scratch_address(dev);
+  if (!part) {
+    cudaGetLastError();
+    return he::set_error(HE_ERR_CUDA, "device address of the built-in scratch not found");
   }
   // Every slot of the scratch the launch reads is written by the same launch's
   // first kernel before the combine kernel reads it, so nothing is cleared.

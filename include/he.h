@@ -81,10 +81,13 @@ typedef struct {
   int pos_offset;   /* 2 for OPT's learned positions */
   int dtype;        /* HE_DTYPE_F32 or HE_DTYPE_BF16: storage type of every parameter.
                        F32: fp32 CUDA-core kernels throughout.  BF16: tensor cores with
-                       fp32 accumulation; while LoRA is fused the merged projections are
-                       held as fp16 (see he_fuse_lora) and activations, the KV cache and
-                       GEMM operands are fp16; unfused they are bf16.  The residual
-                       stream, LayerNorm, softmax, logits and log-probs are fp32. */
+                       fp32 accumulation on fp16 operands: generation reads the
+                       projections as fp16 (merged while LoRA is fused, see
+                       he_fuse_lora; the caller's weights converted at the start of
+                       each generation otherwise, see he_generate), and activations
+                       and the KV cache are fp16.  The residual stream, LayerNorm,
+                       softmax, logits and log-probs are fp32; the tied LM head reads
+                       the bf16 embedding. */
   float ln_eps;     /* 1e-5 for OPT */
   int max_batch;    /* workspace sizing: every he_generate has B <= max_batch */
   int max_seq;      /* workspace sizing: Lp + Lgen <= max_seq (the KV cache length);
@@ -195,8 +198,14 @@ he_status he_read_fused_weight(he_engine *h, int layer, int proj, void *dst, siz
  * prompts, then Lgen - 1 single-token passes over the KV cache; the last token
  * is not fed back.  Requires 1 <= B <= max_batch, Lp >= 1, Lgen >= 1,
  * Lp + Lgen <= max_seq, Lp + Lgen - 1 <= max_pos, and a taken workspace
- * (HE_ERR_STATE after he_release_workspace).  Runs fused or unfused.  An id out
- * of range is replaced by 0 on the device and reported by he_check. */
+ * (HE_ERR_STATE after he_release_workspace).  Runs fused or unfused.  Unfused
+ * on a BF16 engine, every generation first converts the caller's bf16
+ * projections to fp16 in the tiled layout (one pass over the weights, in the
+ * same stream), into a buffer of that size taken through the allocator on the
+ * first unfused call and held with the workspace (he_release_workspace and
+ * he_fuse_lora give it back); HE_ERR_OOM if it cannot be taken.  The weights may
+ * change between calls.  An id out of range is replaced by 0 on the device and
+ * reported by he_check. */
 he_status he_generate(he_engine *h, const int32_t *prompt_ids, int B, int Lp, int Lgen,
                       int32_t *out_ids, float *out_logprob, void *stream);
 
@@ -222,8 +231,9 @@ he_status he_generate_host(he_engine *h, const int32_t *prompt_ids, int B, int L
 he_status he_check(he_engine *h, void *stream);
 
 /* [HE-guide] release_inference_cache: hands the KV cache and activation
- * workspace back to the allocator (stream-ordered on `stream`).  The LoRA restore
- * copy is kept while fused.  HE_ERR_STATE if already released. */
+ * workspace (and an unfused BF16 engine's fp16 copy of the projections) back to
+ * the allocator (stream-ordered on `stream`).  The LoRA restore copy is kept
+ * while fused.  HE_ERR_STATE if already released. */
 he_status he_release_workspace(he_engine *h, void *stream);
 
 /* Takes the workspace again before the next generation.  HE_ERR_STATE if held;

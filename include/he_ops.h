@@ -60,26 +60,30 @@ he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream
  * q: [B][H*hd] (already scaled by hd^-1/2); kc, vc: [B][H][max_seq][hd];
  * ctx: [B][H*hd] row-major out; keys/values 0..n_keys-1 are used.  split >= 1
  * cuts the keys of each (b, h) into that many slices merged afterwards (part:
- * B*H*split*(hd+2) floats when split > 1).  dtype F32 or BF16 (fp32 softmax and
- * accumulation either way); hd in {32, 64, 128}.  Asynchronous on `stream`. */
+ * B*H*split*(hd+2) floats when split > 1).  dtype F32, BF16 or F16 (fp32 softmax
+ * and accumulation in every case); hd in {32, 64, 128}.  Asynchronous on
+ * `stream`. */
 he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void *vc, void *ctx,
                             int B, int H, int hd, int max_seq, int n_keys, int split, float *part,
                             void *stream);
 
 /* he_op_attn_decode for callers that cannot allocate device memory.  The pages
- * have no counterpart: this is a convenience of this library.  Code being
- * captured into a CUDA graph must not call cudaMalloc/cudaFree, pooled or
- * budgeted runtimes cannot hand out an extra buffer on demand, and latency-bound
- * loops avoid cudaMalloc because it may synchronise the device; such callers
- * pass only inputs and outputs here.  Same arguments and results as
- * he_op_attn_decode, except that the split-over-keys partial results live in a
- * 16 MiB array built into the library (4194304 floats, held on every GPU that
- * loads it until the process exits): B * H * split * (hd + 2) must not exceed
- * 4194304 when split > 1, else HE_ERR_ARG.  It allocates nothing.  The first call
- * on a device looks up that array's device address (host-side set-up); make that
+ * have no counterpart: this is a convenience of this library.  Runtimes whose
+ * device memory belongs to a pooling allocator or a fixed budget cannot hand out
+ * an extra buffer on demand, plugins hosted by another framework may have no
+ * allocator of their own, and latency-bound loops avoid cudaMalloc because it may
+ * synchronise the device; such callers pass only inputs and outputs here.  Same
+ * arguments and results as he_op_attn_decode (dtype F32, BF16 or F16), except
+ * that the split-over-keys partial results live in a 16 MiB array built into the
+ * library (4194304 floats, held on every GPU that loads it until the process
+ * exits): B * H * split * (hd + 2) must not exceed 4194304 when split > 1, else
+ * HE_ERR_ARG.  It calls no allocator.  The first call on a device (and the first
+ * after that device's context changes, e.g. after cudaDeviceReset) looks up the
+ * array's device address with that device current (host-side set-up); make that
  * first call before any stream capture.  Every call shares the one array, so
- * calls whose work overlaps on the GPU (other streams, concurrent graphs) race
- * and must be ordered by the caller; nothing in it needs to start at zero. */
+ * calls whose work overlaps on the GPU (other streams, other threads) race and
+ * must be ordered by the caller; a call writes every partial it reads before
+ * reading it, so nothing needs to start at zero. */
 he_status he_op_attn_decode_noalloc(int dtype, const void *q, const void *kc, const void *vc,
                                     void *ctx, int B, int H, int hd, int max_seq, int n_keys,
                                     int split, void *stream);

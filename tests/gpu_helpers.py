@@ -24,12 +24,13 @@ def engine_for(cfg, inputs, torch, max_batch=None, max_seq=None, **kw):
 
 
 def teacher_forced_check(cfg, torch, seqs=None, steps=None, inputs=None, prompts=None,
-                         oracle_seqs=None):
+                         oracle_seqs=None, fused=True):
     """Runs the GPU path teacher-forced on the oracle's tokens; returns the worst errors.
 
     ``oracle_seqs``: the sequences the oracle computes (batch rows are independent),
     default all; the GPU runs the whole batch.  ``steps``: the decode steps compared
-    (default all).
+    (default all).  ``fused``: LoRA merged before generating (oracle "merged"), or
+    generation on the base weights without a fuse (oracle "none").
     """
     inputs = inputs if inputs is not None else make_model(cfg)
     prompts = prompts if prompts is not None else make_prompts(cfg)
@@ -37,16 +38,19 @@ def teacher_forced_check(cfg, torch, seqs=None, steps=None, inputs=None, prompts
     oseq = list(range(B)) if oracle_seqs is None else list(oracle_seqs)
     osteps = list(range(cfg.gen_len)) if steps is None else list(steps)
     n_or = max(osteps) + 1
-    ref_ids, ref_lps, ref_lg = OracleModel(inputs).generate(prompts[oseq], n_or,
-                                                            log_steps=osteps)
+    oracle = OracleModel(inputs, "merged" if fused else "none")
+    ref_ids, ref_lps, ref_lg = oracle.generate(prompts[oseq], n_or, log_steps=osteps)
+    del oracle
     eng, _w = engine_for(cfg, inputs, torch)
-    eng.fuse_lora()
+    if fused:
+        eng.fuse_lora()
     force = np.full((B, cfg.gen_len), -1, np.int32)
     force[oseq, :n_or] = ref_ids
     rows = [(b, k) for b in (oseq if seqs is None else seqs) for k in osteps]
     ids, lps, lg = eng.generate_ex(torch.from_numpy(prompts).cuda(), cfg.gen_len,
                                    force_ids=torch.from_numpy(force), log_rows=rows)
-    eng.unfuse_lora()
+    if fused:
+        eng.unfuse_lora()
     eng.check()
     torch.cuda.synchronize()
     lg = lg.cpu().numpy()

@@ -173,11 +173,13 @@ def test_minimal_shapes(cuda_device):
     cfg = WORKLOADS["opt-tiny-fp32"].with_(batch=1, prompt_len=1, gen_len=1)
     inputs = make_model(cfg)
     prompts = make_prompts(cfg)
-    ref_ids, ref_lps, _ = OracleModel(inputs).generate(prompts, 1)
+    # no fuse: the engine runs the base weights, the oracle's "none" model
+    ref_ids, ref_lps, _ = OracleModel(inputs, "none").generate(prompts, 1)
     eng, _w = engine_for(cfg, inputs, torch)
     ids, lps = eng.generate(torch.from_numpy(prompts).cuda(), 1)
     torch.cuda.synchronize()
     assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.abs(lps.cpu().numpy() - ref_lps).max() < FP32_LP_TOL
     eng.close()
 
 
