@@ -95,6 +95,8 @@ _SIGNATURES = {
     "he_op_linear": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
                              c_int, c_int, c_void_p, c_void_p]),
     "he_op_tile_weight": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p]),
+    "he_op_head_greedy": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
+                                  c_void_p, c_void_p, c_void_p, c_void_p]),
     "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_op_attn_decode_noalloc": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
@@ -408,6 +410,29 @@ def tile_weight(w, stream=None):
     _check(lib.he_op_tile_weight(w.data_ptr(), out.data_ptr(), w.shape[0], w.shape[1],
                                  _stream_handle(torch, stream)))
     return out
+
+
+def head_greedy(x, w, stream=None):
+    """Greedy choice and its log-prob for each row of the logits x w^T (he_op_head_greedy:
+    the choice is fused into the LM-head GEMM; the logits are never stored)."""
+    import torch
+    lib = load_library()
+    M, K = x.shape
+    N = w.shape[0]
+    if x.dtype != w.dtype or x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("x and w must both be bf16 or both fp16")
+    if x.stride(1) != 1 or not w.is_contiguous():
+        raise ValueError("x rows and w must be dense")
+    R = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+    T = (N + 127) // 128
+    scratch = torch.empty(16 * M * T * 128 + (R * K + 1) // 2 + 8 + T + 4 + 4 * T * M,
+                          dtype=torch.float32, device=x.device)
+    ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    lp = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib.he_op_head_greedy(_dtype_code(torch, x.dtype), x.data_ptr(), x.stride(0),
+                                 w.data_ptr(), M, N, K, ids.data_ptr(), lp.data_ptr(),
+                                 scratch.data_ptr(), _stream_handle(torch, stream)))
+    return ids, lp
 
 
 def linear(x, w, split: int = 1, stream=None, w_tiled=None):

@@ -457,9 +457,37 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   el.kind = EPI_STORE_F32;
   el.partial = static_cast<float *>(h->logits.p);
   el.ldp = cf.vocab;
+  // Greedy decode steps without teacher forcing or logit capture fuse the choice into
+  // the LM head: its epilogue leaves per-tile {max, exp-sum, argmax} statistics
+  // (in the logits buffer) instead of the logits, and a small kernel merges them.
+  const int n_tiles = (cf.vocab + 127) / 128;
+  bool fused_head = false;
   if (dec && use_stream_k(h, B, cf.vocab, cf.d_model, true, false)) {
     const void *we[1] = {h->tok_emb};
-    gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false, cf.dtype);
+    if (h->temperature == 0.f && !force && !log_map) {
+      Epi ea{};
+      ea.kind = EPI_ARGMAX;
+      ea.partial = static_cast<float *>(h->logits.p);
+      ea.ldp = B;
+      GemmArgs probe{};
+      probe.act = cf.dtype;
+      probe.x = hrows;
+      probe.w[0] = h->tok_emb;
+      probe.n_groups = 1;
+      probe.group_rows = cf.vocab;
+      probe.M = B;
+      probe.N = cf.vocab;
+      probe.K = cf.d_model;
+      probe.split = 1;
+      probe.epi = ea;
+      fused_head = sk_argmax_ok(probe, sk_ctas(probe, h->num_sms, true));
+      if (fused_head)
+        gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, ea, true, false,
+             cf.dtype);
+    }
+    if (!fused_head)
+      gemm(c, HE_KCLASS_HEAD, hrows, ldh, we, 1, cf.vocab, B, cf.d_model, el, true, false,
+           cf.dtype);
   } else {
     head_rows_gemm(c, hrows, ldh, B);
   }
@@ -499,6 +527,10 @@ void head(Ctx &c, const void *hrows, int ldh, int B, int step, int Lp, int Lgen,
   ha.temperature = h->temperature;
   ha.top_p = h->top_p;
   ha.seed = h->seed;
+  if (fused_head) {
+    ha.stats = static_cast<const float4 *>(h->logits.p);
+    ha.n_tiles = n_tiles;
+  }
   c.check(launch_head_select(cf.dtype, h->act, ha, c.st), 1);
 }
 
@@ -1231,6 +1263,65 @@ he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream
   cudaError_t r = launch_fuse_tiled(out, ACT_BF16, w, nullptr, nullptr, N, K, 0, 0.f,
                                     static_cast<cudaStream_t>(stream));
   if (r != cudaSuccess) return cuda_fail(r, "he_op_tile_weight");
+  return HE_OK;
+}
+
+he_status he_op_head_greedy(int dtype, const void *x, int ldx, const void *w, int M, int N, int K,
+                            int32_t *out_ids, float *out_lp, float *scratch, void *stream) {
+  g_err.clear();
+  if (!x || !w || !out_ids || !out_lp || !scratch) return fail(HE_ERR_ARG, "NULL buffer");
+  if (dtype != HE_DTYPE_BF16 && dtype != HE_DTYPE_F16) return fail(HE_ERR_ARG, "dtype must be BF16 or F16");
+  if (M < 1 || M > 256 || N < 1 || K < 64 || K % 64 || ldx < K || ldx % 8 || N % 4)
+    return fail(HE_ERR_ARG, "need 1 <= M <= 256, K %% 64 == 0, ldx >= K, ldx %% 8 == 0, N %% 4 == 0");
+  if ((uintptr_t)x % 16 || (uintptr_t)w % 16 || (uintptr_t)scratch % 16)
+    return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long T = (N + 127) / 128;
+  const int R = sk_token_tile(M);
+  // scratch: slices [16][T][M][128] | row-tiled x | tile counters | statistics [T][M]
+  const long long sstride = (long long)M * T * 128;
+  void *xt = scratch + (size_t)16 * sstride;
+  int *cnt = reinterpret_cast<int *>(((uintptr_t)xt + (size_t)R * K * 2 + 15) & ~(uintptr_t)15);
+  float4 *stats = reinterpret_cast<float4 *>(((uintptr_t)(cnt + T) + 15) & ~(uintptr_t)15);
+  GemmArgs a{};
+  a.dtype = HE_DTYPE_BF16;
+  a.act = dtype;
+  a.x = xt;
+  a.ldx = K;
+  a.w[0] = w;
+  a.n_groups = 1;
+  a.group_rows = N;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.split = 1;
+  Epi e{};
+  e.kind = EPI_ARGMAX;
+  e.partial = reinterpret_cast<float *>(stats);
+  e.ldp = M;
+  a.epi = e;
+  const int P = sk_ctas(a, sms, true);
+  if (!sk_argmax_ok(a, P)) return fail(HE_ERR_UNSUPPORTED, "tile statistics need the staged owner path");
+  cudaError_t r = launch_tile_act(x, M, K, ldx, R, xt, st);
+  if (r == cudaSuccess) r = cudaMemsetAsync(cnt, 0, (size_t)T * sizeof(int), st);
+  if (r == cudaSuccess) r = launch_gemm_sk(a, P, scratch, sstride, cnt, nullptr, st);
+  if (r == cudaSuccess) {
+    HeadArgs ha{};
+    ha.vocab = N;
+    ha.B = M;
+    ha.step = 0;
+    ha.gen_len = 1;
+    ha.out_ids = out_ids;
+    ha.out_lp = out_lp;
+    ha.stats = stats;
+    ha.n_tiles = (int)T;
+    ha.d = K;
+    r = launch_head_select(HE_DTYPE_BF16, dtype, ha, st);
+  }
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_head_greedy");
   return HE_OK;
 }
 

@@ -87,6 +87,54 @@ constexpr int EPT = 32 * EPW;        // epilogue threads
 constexpr int SK_THREADS = EPT + 64; // + producer warp + MMA warp
 constexpr int PRODUCER = EPW, MMA = EPW + 1;
 
+// EPI_ARGMAX for a tile stored directly (one run): the greedy statistics of each
+// token column over the tile's 128 rows (features n >= N left out).  Rounds of 32
+// columns, 16 per column half; a warp reduces its 32 rows for 16 columns (a
+// butterfly step over lanes l and l + 16, then a halving exchange after which lane l
+// holds column l % 16), the four lane quarters meet in shared memory and the first
+// warp of each half merges them in quarter order.  Every epilogue warp runs the same
+// rounds (both barriers).
+template <int BN>
+__device__ __forceinline__ void argmax_tile_direct(const Epi &epi, uint32_t tl, int t, int row,
+                                                   int N, int M, int quarter, int half, int lane,
+                                                   bool live, ArgStat (*part)[4][16]) {
+  float4 *stats = reinterpret_cast<float4 *>(epi.partial);
+  for (int r0 = 0; r0 < BN; r0 += 32) {
+    const int c0 = r0 + 16 * half;  // this warp's 16 columns
+    const bool any = c0 < BN;       // (BN 16: the second half has none)
+    ArgStat st[16];
+    if (any) {
+      float v[16];
+      tmem_load_cols<16>(tl + (uint32_t)c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st[j] = row < N ? ArgStat{v[j], 1.f, row} : ArgStat{-INFINITY, 0.f, 0};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st[j] = argstat_merge(st[j], argstat_shfl_xor(st[j], 16));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+          const ArgStat keep = up ? st[j + w] : st[j];
+          const ArgStat give = up ? st[j] : st[j + w];
+          st[j] = argstat_merge(keep, argstat_shfl_xor(give, w));
+        }
+      }
+      if (lane < 16) part[half][quarter][lane] = st[0];
+    }
+    epi_bar_sync<EPT>();
+    if (any && quarter == 0 && lane < 16) {
+      ArgStat m = part[half][0][lane];
+#pragma unroll
+      for (int q = 1; q < 4; ++q) m = argstat_merge(m, part[half][q][lane]);
+      const int tok = c0 + lane;
+      if (live && tok < M)
+        stats[(size_t)t * epi.ldp + tok] = make_float4(m.m, m.s, __int_as_float(m.i), 0.f);
+    }
+    epi_bar_sync<EPT>();
+  }
+}
+
 template <typename CT, int BN, int STAGES, int KPS>
 __global__ void __launch_bounds__(SK_THREADS, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
@@ -247,6 +295,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     // a.tile_cnt, tiles of one run are stored directly and the others are left as
     // slices for a second kernel.
     const bool fix = a.tile_cnt != nullptr && epi.kind != EPI_PARTIAL;
+    __shared__ ArgStat am_part[2][4][16];  // EPI_ARGMAX: per column half, lane quarter, column
     constexpr int W = BN >= 32 ? 32 : 16;
     constexpr int kStageAvail = STAGES * C::STAGE_BYTES;
     // The bias of this thread's row in the tile of the last segment (the one an
@@ -281,6 +330,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         tile_owner_epilogue<CT, W, EPT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride,
                                         a.N, a.M, t, S, tl, live, &a.tile_cnt[t], base,
                                         kStageAvail, fix_bar, last_flag, dev_err, last_bias);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      } else if (S == 1 && epi.kind == EPI_ARGMAX) {
+        argmax_tile_direct<BN>(epi, tl, t, row, a.N, a.M, quarter, half, lane, live, am_part);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -407,9 +461,38 @@ bool sk_fixup_ok(const GemmArgs &g) {
     case EPI_QKV:
       return g.N % 8 == 0 && e.head_dim % 8 == 0 && e.ldo % 8 == 0 && al(e.out) && al(e.kc) &&
              al(e.vc);
+    case EPI_ARGMAX:
+      return g.N % 4 == 0 && e.ldp >= g.M && al(e.partial);
     default:
       return false;
   }
+}
+
+// Shared memory of the pipeline stages of the kernel launch_gemm_sk picks for a.
+static int sk_stage_avail(const GemmArgs &g) {
+  struct Pick { int bn, stages, kps; };
+  Pick p;
+  if (sk_kps(g) == 2)
+    p = g.M <= 16 ? Pick{16, 5, 2} : g.M <= 32 ? Pick{32, 5, 2} : g.M <= 64 ? Pick{64, 4, 2}
+        : g.M <= 128 ? Pick{128, 3, 2} : Pick{256, 2, 2};
+  else
+    p = g.M <= 16 ? Pick{16, 10, 1} : g.M <= 32 ? Pick{32, 9, 1} : g.M <= 64 ? Pick{64, 8, 1}
+        : g.M <= 128 ? Pick{128, 6, 1} : Pick{256, 4, 1};
+  return p.stages * p.kps * (BM * BK * 2 + p.bn * BK * 2);
+}
+
+bool sk_argmax_ok(const GemmArgs &g, int P) {
+  if (g.epi.kind != EPI_ARGMAX || !sk_fixup_ok(g)) return false;
+  const long long T = (g.N + BM - 1) / BM, U = sk_units(g);
+  const int KB = (int)(U / T);
+  int smax = 1;
+  for (long long t = 0; t < T; ++t) {
+    int cf, S;
+    sk_segments((int)t, KB, P, U, &cf, &S);
+    if (S > smax) smax = S;
+  }
+  const int W = g.M <= 16 ? 16 : 32;  // the owner's column chunk (BN >= 32: 32)
+  return tile_stage_tokens(smax, g.M, W, sk_stage_avail(g)) >= W;
 }
 
 cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long slice_stride,
@@ -424,6 +507,7 @@ cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long sl
   if (tile_cnt && (!sk_fixup_ok(g) || (uintptr_t)slices % 16 ||
                    slice_stride < (long long)g.M * ((g.N + BM - 1) / BM) * BM))
     return cudaErrorInvalidValue;
+  if (g.epi.kind == EPI_ARGMAX && (!tile_cnt || !sk_argmax_ok(g, P))) return cudaErrorInvalidValue;
   auto pick = [&](auto ct) -> cudaError_t {
     using CT = decltype(ct);
 #define HE_SK(BN, ST, KPS) \

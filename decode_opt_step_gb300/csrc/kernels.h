@@ -86,7 +86,9 @@ enum EpiKind : int {
   EPI_PARTIAL = 0,  // fp32 partial[split][tok][n] (bias/residual applied later, per row)
   EPI_QKV = 1,      // n < d: q (+bq, * hd^-1/2) -> q_out[tok][n]; else k / v (+bias) -> cache
   EPI_RELU = 2,     // out[tok][n] = relu(C + bias[n]) in the storage type
-  EPI_STORE_F32 = 3 // fp32 out[tok][n] = C (LM-head logits, kernel tests)
+  EPI_STORE_F32 = 3, // fp32 out[tok][n] = C (LM-head logits, kernel tests)
+  EPI_ARGMAX = 4     // per 128-row tile t and token: {max_n C, sum_n exp(C - max), lowest n
+                     // reaching the max (int bits), 0} as a float4 at partial[t * ldp + tok]
 };
 
 struct Epi {
@@ -197,6 +199,9 @@ int sk_ctas(const GemmArgs &a, int num_sms, bool fixup);
 // Whether a.epi can be completed inside the kernel (tile_cnt != null): an
 // element-wise kind, N % 4 == 0 and vector-aligned outputs.
 bool sk_fixup_ok(const GemmArgs &a);
+// EPI_ARGMAX needs every split tile finished by its owner's staged reduction
+// (shared memory for the slices of the tile with the most runs, on P CTAs).
+bool sk_argmax_ok(const GemmArgs &a, int P);
 // tile_cnt: null, or ceil(N / 128) ints that are zero at the launch (and are left
 // zero): the other runs of a split tile count their finished slices there and the
 // tile's owner applies a.epi to the sum, so no reduction kernel follows; the
@@ -249,6 +254,10 @@ struct HeadArgs {
   // Gumbel-max with SplitMix64 uniforms keyed by (seed, b, step, token); 0 = greedy
   float temperature, top_p;
   unsigned long long seed;
+  // greedy from per-tile statistics (EPI_ARGMAX of the LM head) instead of logits:
+  // stats[t * B + b] for the n_tiles 128-row vocabulary tiles (logits unused)
+  const float4 *stats;
+  int n_tiles;
 };
 // h is written in `act`.
 cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st);

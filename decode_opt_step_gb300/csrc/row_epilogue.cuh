@@ -148,7 +148,7 @@ template <typename CT, int NT>
 __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, long long sstride,
                                            int N, int M, int t, int S, int et) {
   const int n0 = t * 128 + 4 * (et & 31);
-  if (n0 >= N) return;
+  if (n0 >= N || e.kind == EPI_ARGMAX) return;  // (EPI_ARGMAX tiles are always staged)
   float b4[4] = {0.f, 0.f, 0.f, 0.f};
   float scale = 1.f;
   int mode = 0;
@@ -254,10 +254,11 @@ __device__ __forceinline__ void tile_fixup(const Epi &e, const float *tslices, l
 }
 
 // Output element type of a stream-K tile's final epilogue: fp32 logits / partial
-// sums, else the activation type.
+// sums (and the raw values EPI_ARGMAX reduces), else the activation type.
 __host__ __device__ inline int tile_out_bytes(int kind, int ct_bytes) {
-  return kind == EPI_STORE_F32 || kind == EPI_PARTIAL ? 4 : ct_bytes;
+  return kind == EPI_STORE_F32 || kind == EPI_PARTIAL || kind == EPI_ARGMAX ? 4 : ct_bytes;
 }
+
 
 // Tokens of a tile that the staged reduction of the tile's owner handles at a
 // time in `avail` bytes of shared memory (a multiple of W; 0 if not even W fit):
@@ -427,7 +428,27 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
       }
     }
     epi_bar_sync<NT>();
-    if (go) {
+    if (e.kind == EPI_ARGMAX) {
+      // two threads per token, 64 features each, then merged: the tile's statistics
+      float4 *stats = reinterpret_cast<float4 *>(e.partial);
+      const int hf2 = et & 1;
+      for (int jb = (et >> 1) & ~15; jb < cn; jb += NT / 2) {  // warp-uniform bound
+        const int jj = jb + ((et >> 1) & 15);
+        ArgStat st{-INFINITY, 0.f, 0};
+        if (jj < cn) {
+          const int f0 = 64 * hf2;
+#pragma unroll 4
+          for (int f = f0; f < f0 + 64; ++f) {
+            const int n = t * 128 + f;
+            if (n < N) argstat_add(st, lds_f32(os_s + (uint32_t)((jj * 128 + f) * 4)), n);
+          }
+        }
+        st = argstat_merge(st, argstat_shfl_xor(st, 1));
+        if (go && jj < cn && hf2 == 0)
+          stats[(size_t)t * e.ldp + c0 + jj] =
+              make_float4(st.m, st.s, __int_as_float(st.i), 0.f);
+      }
+    } else if (go) {
       // 16-byte output groups (4 fp32 values, or 8 values rounded to CT): thread et
       // always takes group et % cpr of rows et / cpr, et / cpr + 128 / cpr, ...
       const int per = 16 / ob, cpr = 128 / per;

@@ -442,6 +442,47 @@ __global__ void __launch_bounds__(1024) k_head_select(HeadArgs a) {
   }
 }
 
+// Greedy head from the LM head's per-tile statistics (EPI_ARGMAX): one CTA per
+// sequence merges the n_tiles {max, exp-sum, lowest index} of its row -- each thread
+// the tiles t, t + 1024, ... in order, then a butterfly over each warp and the warps
+// in order -- so the token is the lowest index of the row's maximum and its
+// log-prob is l_tok - (max + log sum exp(l - max)) = -log(merged sum).  Then, as in
+// k_head_select and with its block size (so the LayerNorm sums, and the next step's
+// input, are the same bits), the token is embedded and normalised for the next step.
+template <typename PT, typename CT>
+__global__ void __launch_bounds__(1024) k_head_stats(HeadArgs a) {
+  extern __shared__ float row[];
+  __shared__ float red[33];
+  __shared__ ArgStat wpart[32];
+  __shared__ int s_tok;
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x;
+  ArgStat st{-INFINITY, 0.f, 0};
+  for (int t = threadIdx.x; t < a.n_tiles; t += blockDim.x) {
+    const float4 v = a.stats[(long long)t * a.B + b];
+    st = argstat_merge(st, ArgStat{v.x, v.y, __float_as_int(v.z)});
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) st = argstat_merge(st, argstat_shfl_xor(st, o));
+  if ((threadIdx.x & 31) == 0) wpart[threadIdx.x >> 5] = st;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ArgStat m = wpart[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = argstat_merge(m, wpart[w]);
+    a.out_ids[(long long)b * a.gen_len + a.step] = m.i;
+    a.out_lp[(long long)b * a.gen_len + a.step] = -logf(m.s);
+    s_tok = m.i;
+  }
+  __syncthreads();
+  if (a.embed_next) {
+    embed_row<PT>(s_tok, a.pos + a.pos_offset, static_cast<const PT *>(a.tok_emb),
+                  static_cast<const PT *>(a.pos_emb), a.d, row, a.x + (long long)b * a.d);
+    ln_store<PT, CT>(row, a.d, static_cast<const PT *>(a.g), static_cast<const PT *>(a.b), a.eps,
+                     static_cast<CT *>(a.h), b, a.h_rows, red);
+  }
+}
+
 // W <- round(W + scale * sum_j B[row][j] A[j][col]) for 8 consecutive columns
 // per thread, after copying the original bits of W to `save`.
 template <typename T>
@@ -651,7 +692,10 @@ cudaError_t launch_reduce_epi(int dtype, int act, const float *partial, int spli
 
 cudaError_t launch_head_select(int dtype, int act, const HeadArgs &a, cudaStream_t st) {
   const size_t sm = (size_t)a.d * sizeof(float);
+  if (a.stats && (a.temperature > 0.f || a.force_ids || a.log_map || a.n_tiles < 1))
+    return cudaErrorInvalidValue;  // the statistics serve greedy choice only
   HE_DISPATCH_PT_CT(dtype, act, {
+    if (a.stats) return launch_k(k_head_stats<PT, CT>, dim3(a.B), dim3(1024), sm, st, g_pdl, a);
     return launch_k(k_head_select<PT, CT>, dim3(a.B), dim3(1024), sm, st, g_pdl, a);
   });
   return cudaSuccess;

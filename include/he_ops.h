@@ -38,6 +38,27 @@ extern "C" {
 he_status he_op_linear(int dtype, const void *x, int ldx, const void *w, int w_layout, float *y,
                        int M, int N, int K, int split, float *scratch, void *stream);
 
+/* Greedy choice fused into the LM-head GEMM, as the decode steps run it when they
+ * neither sample, force tokens nor capture logits ("DeepSpeed-Chat: Easy, Fast and
+ * Affordable RLHF Training of ChatGPT-like Models at All Scales", §3.4 "Inference
+ * Mode: Generation Phase Optimizations", Optimization 1: fused kernels cut the
+ * intermediate reads and writes; "Chapter 11 System Architecture & Infrastructure
+ * at Scale", "The Generation Bottleneck": generation returns the log-probabilities
+ * of the chosen tokens).  For the logits l = x w^T (x [M][K] with row stride ldx,
+ * w [N][K] dense, both dtype BF16 or F16, fp32 accumulation): out_ids[m] = the
+ * lowest n with l[m][n] = max_n l[m][n], and out_lp[m] = log softmax of that
+ * logit, computed without storing the logits: the stream-K kernel's epilogue
+ * reduces each 128-row tile of w to {max, sum of exp(l - max), argmax} per row of
+ * x, and a second kernel merges the tiles.  Needs 1 <= M <= 256, K % 64 == 0,
+ * ldx >= K, ldx % 8 == 0, N % 4 == 0, 16-byte aligned buffers.  scratch: 16 * M *
+ * Np floats (Np = N rounded up to 128) for split-tile slices, then R * K 16-bit
+ * values (R = M rounded up to 16, 32, 64, 128 or 256) for the row-tiled copy of x,
+ * then from the next 16-byte boundary Np / 128 ints of tile counters, then from
+ * the next 16-byte boundary Np / 128 * M float4 of tile statistics.  Device
+ * pointers; asynchronous on `stream`. */
+he_status he_op_head_greedy(int dtype, const void *x, int ldx, const void *w, int M, int N, int K,
+                            int32_t *out_ids, float *out_lp, float *scratch, void *stream);
+
 /* The streaming layout he_fuse_lora writes the bf16 projections in while LoRA
  * is fused ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of
  * ChatGPT-like Models at All Scales", §3.4 "Inference Mode: Generation Phase

@@ -75,6 +75,8 @@ def test_argument_errors_without_gpu(lib):
     assert lib.he_get_stats(None, None) == he.HE_ERR_ARG
     assert lib.he_op_linear(1, None, 8, None, 0, None, 1, 1, 8, 1, None, None) == he.HE_ERR_ARG
     assert lib.he_op_tile_weight(None, None, 128, 64, None) == he.HE_ERR_ARG
+    assert lib.he_op_head_greedy(1, None, 64, None, 1, 128, 64, None, None, None,
+                                 None) == he.HE_ERR_ARG
     assert b"sm_103a" in lib.he_version()
 
 

@@ -73,5 +73,9 @@ def test_graph_mode_with_profiling_and_teacher_forcing(cuda_device):
     eng.set_profiling(())
     force = ref[0].clone()
     ids, lps, _ = eng.generate_ex(prompts, cfg.gen_len, force_ids=force)
-    assert torch.equal(ids, ref[0]) and torch.equal(lps, ref[1])
+    # teacher forcing takes the log-prob from the stored logits, free-running greedy
+    # decode steps from the LM head's merged tile statistics: the same value up to
+    # the order of the fp32 sums
+    assert torch.equal(ids, ref[0]) and (lps - ref[1]).abs().max().item() < 2e-5
+    assert torch.equal(lps[:, 0], ref[1][:, 0])  # the prefill head takes the same path
     eng.close()
