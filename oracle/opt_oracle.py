@@ -52,6 +52,18 @@ over the full vocabulary; 1 prefill pass + (gen_len - 1) single-token passes
 Precision: fp32 weights (bf16 storage widened exactly) and fp32 arithmetic.
 The LoRA-merged weight W + (alpha/r) B A is kept unrounded in fp32.
 
+FP8 weights for generation ("Chapter 11 System Architecture & Infrastructure at
+Scale", "The Generation Bottleneck: Quantitative Analysis", the optimisation stack:
+INT8/FP8 weights for generation halve the bandwidth the weights need).  The page
+names the idea, not a format; the reading taken here (``weights="fp8"``): each of
+the six projections of every layer, after the LoRA merge, is stored as OCP FP8
+E4M3 values (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest finite
+value 448; subnormals down to 2^-9; no infinity) with one fp32 scale per output
+row, s_n = max_k |W[n][k]| / 448, codes q = nearest E4M3 value of W[n][k] / s_n
+(fp32 division, ties to the even mantissa, beyond 448 saturated), and generation
+runs with the dequantized weight q * s_n in fp32.  Activations, the KV cache and
+the tied LM head are not quantized.
+
 Parameters arrive as the synthetic-input dictionaries of ``synth.workloads``:
 projections are [out][in] (y = x W^T + b); bf16 tensors are raw uint16 bits.
 """
@@ -112,6 +124,44 @@ def sample_token(logits: np.ndarray, temperature: float, top_p: float, seed: int
     return tok, float(z[tok] - np.log(total))
 
 
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """Nearest OCP FP8 E4M3 value of each element (ties to the even mantissa); values
+    beyond +-448 saturate to +-448 (the format has no infinity); NaN stays NaN.
+
+    In the binade [2^e, 2^(e+1)), e >= -6, the format has 8 values 2^(e-3) apart;
+    below 2^-6 the subnormals continue with spacing 2^-9.  Rounding |x| / spacing to
+    the nearest integer, half to even, is the round-to-nearest-even of the format
+    (an even integer is an even mantissa, the implicit bit included)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    spacing = np.exp2(e - 3.0)
+    q = np.rint(a / spacing) * spacing
+    q = np.minimum(q, E4M3_MAX)
+    return np.where(np.isnan(x), np.nan, np.copysign(q, x))
+
+
+def quantize_rows_e4m3(w: np.ndarray) -> tuple:
+    """Per output row n of w [out][in] (fp32): scale s_n = max |w[n]| / 448 (1 for an
+    all-zero row) and codes q = e4m3_round(w / s_n), the division in fp32.  Returns
+    (q as fp32 values, s fp32 [out])."""
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.abs(w).max(axis=1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((w / s[:, None]).astype(np.float32)).astype(np.float32)
+    return q, s
+
+
+def dequantize_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """The weight generation runs with: q * s_n per row, fp32."""
+    return (np.asarray(q, np.float32) * np.asarray(s, np.float32)[:, None]).astype(np.float32)
+
+
 def lora_delta(a: np.ndarray, b: np.ndarray, alpha: float, r: int) -> np.ndarray:
     """(alpha / r) * B @ A: the low-rank update of the LoRA passage, [out][in], fp32."""
     return np.float32(alpha / r) * (to_f32(b) @ to_f32(a))
@@ -148,12 +198,17 @@ class OracleModel:
 
     ``lora`` selects how the LoRA factors enter: "merged" (W + (alpha/r) B A, what
     generation runs with), "unmerged" (base projection plus an explicit low-rank
-    branch, the training-mode form) or "none" (base weights only).
+    branch, the training-mode form) or "none" (base weights only).  ``weights``:
+    "exact" (the fp32 values above) or "fp8" (the six projections, after the merge,
+    quantized per row to E4M3 and dequantized; see the module notes; needs lora
+    "merged" or "none").
     """
 
-    def __init__(self, inputs, lora: str = "merged"):
+    def __init__(self, inputs, lora: str = "merged", weights: str = "exact"):
         if lora not in ("merged", "unmerged", "none"):
             raise ValueError(lora)
+        if weights not in ("exact", "fp8") or (weights == "fp8" and lora == "unmerged"):
+            raise ValueError(weights)
         self.cfg = cfg = inputs.cfg
         self.lora_mode = lora
         self.scale = np.float32(cfg.lora_alpha / cfg.lora_r)
@@ -173,6 +228,8 @@ class OracleModel:
                 if lora == "unmerged" and inputs.lora:
                     a, b = inputs.lora[li][name]
                     lw[name + "_A"], lw[name + "_B"] = to_f32(a), to_f32(b)
+                if weights == "fp8":
+                    lw[name] = dequantize_rows(*quantize_rows_e4m3(lw[name]))
             self.layers.append(lw)
 
     # -- one projection: y = x W^T + b (+ (alpha/r) (x A^T) B^T when unmerged) --

@@ -34,8 +34,49 @@ def _ln(x, g, b, eps):
     return [(x[i] - mu) / math.sqrt(var + eps) * g[i] + b[i] for i in range(n)]
 
 
+def e4m3_values():
+    """Every finite OCP FP8 E4M3 value with its code, decoded bit by bit from the
+    format's definition: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+    field 0 is subnormal (2^-6 * m / 8); the pattern S.1111.111 is NaN."""
+    out = []
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            continue  # NaN
+        v = sign * (2.0 ** -6 * m / 8.0 if e == 0 else 2.0 ** (e - 7) * (1.0 + m / 8.0))
+        out.append((v, code))
+    return out
+
+
+def nearest_e4m3(x, table=None):
+    """Nearest E4M3 value of x by search over every finite value (ties: the code
+    with the even mantissa bit); |x| beyond the largest value saturates."""
+    table = table or e4m3_values()
+    best = None
+    for v, code in table:
+        d = abs(x - v)
+        if best is None or d < best[0] or (d == best[0] and (code & 1) == 0 and best[2] & 1):
+            best = (d, v, code)
+    return best[1]
+
+
+def quantize_rows_brute(W):
+    """Per row: scale = max |w| / 448 (fp32, as the format's scale is stored), each
+    element the nearest E4M3 value of w / scale (fp32 division), times the scale."""
+    table = e4m3_values()
+    out = []
+    for row in W:
+        amax = np.float32(max(abs(v) for v in row))
+        s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+        out.append([nearest_e4m3(float(np.float32(np.float32(v) / s)), table) * float(s)
+                    for v in row])
+    return out
+
+
 class BruteForce:
-    def __init__(self, inputs, lora: bool = True):
+    def __init__(self, inputs, lora: bool = True, fp8: bool = False):
         cfg = self.cfg = inputs.cfg
         g = inputs.globals
         self.E = _f64(g["tok_emb"])
@@ -54,6 +95,9 @@ class BruteForce:
                     for o in range(len(W)):
                         for i in range(len(W[0])):
                             W[o][i] += s * sum(B[o][j] * A[j][i] for j in range(cfg.lora_r))
+            if fp8:
+                for name in ("wq", "wk", "wv", "wo", "w1", "w2"):
+                    lw[name] = quantize_rows_brute(lw[name])
             self.layers.append(lw)
 
     def last_logits(self, seq):

@@ -357,3 +357,74 @@ def test_sampler_logprob_is_tempered_log_softmax():
         tok, lp = sample_token(lg, t, 0.9, 7, 1, 2)
         ref = torch.log_softmax(torch.from_numpy(lg).double() / t, 0)[tok].item()
         assert abs(lp - ref) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) weights: the rounding, the per-row scale, and the model that uses them
+# ---------------------------------------------------------------------------
+from tests.brute_force import e4m3_values, nearest_e4m3  # noqa: E402
+
+
+def test_e4m3_grid_round_trips_and_has_the_format_extremes():
+    vals = sorted({v for v, _ in e4m3_values()})
+    assert len(vals) == 253  # 254 finite codes, +0 and -0 the same value
+    assert max(vals) == 448.0 and min(vals) == -448.0
+    pos = [v for v in vals if v > 0]
+    assert pos[0] == 2.0 ** -9 and pos[1] == 2.0 ** -8  # subnormal spacing
+    np.testing.assert_array_equal(oo.e4m3_round(np.array(vals)), np.array(vals))
+
+
+def test_e4m3_round_is_the_nearest_value_ties_to_even_by_brute_force():
+    table = e4m3_values()
+    vals = np.array(sorted({v for v, _ in table}))
+    rng = np.random.default_rng(8)
+    mids = (vals[1:] + vals[:-1]) / 2  # every exact tie
+    xs = np.concatenate([mids, rng.normal(0, 60, 400), rng.normal(0, 0.02, 200),
+                         rng.uniform(-600, 600, 100), [448.0, 463.9, 464.0, 1e6, -1e6]])
+    got = oo.e4m3_round(xs)
+    want = np.array([nearest_e4m3(float(x), table) for x in xs])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_row_quantization_scale_and_error_bound():
+    rng = np.random.default_rng(3)
+    w = (rng.normal(0, 0.02, (64, 300)) * rng.uniform(0.1, 10, (64, 1))).astype(np.float32)
+    w[5] = 0.0
+    q, s = oo.quantize_rows_e4m3(w)
+    assert s.dtype == np.float32 and s[5] == 1.0 and (q[5] == 0).all()
+    amax = np.abs(w).max(axis=1)
+    np.testing.assert_allclose(s[amax > 0], amax[amax > 0] / 448.0, rtol=1e-7)
+    assert (np.abs(q).max(axis=1)[amax > 0] == 448.0).all()  # the largest element: +-448
+    wq = oo.dequantize_rows(q, s)
+    # half a spacing: 2^-4 relative in the normal range, 2^-10 * s below 2^-6 * s
+    bound = np.maximum(np.abs(w) * 2.0 ** -4, 2.0 ** -10 * s[:, None]) * (1 + 1e-6)
+    assert (np.abs(wq - w) <= bound).all()
+
+
+def test_fp8_model_matches_brute_force_with_quantized_weights():
+    inputs, prompts = _bf_case(BF_CFG2)
+    bf = BruteForce(inputs, fp8=True)
+    ids, lps, logged = OracleModel(inputs, weights="fp8").generate(
+        prompts, BF_CFG2.gen_len, log_steps=range(BF_CFG2.gen_len))
+    for b in range(BF_CFG2.batch):
+        bids, blps, brows = bf.generate(prompts[b], BF_CFG2.gen_len)
+        assert list(ids[b]) == bids
+        np.testing.assert_allclose(lps[b], blps, atol=1e-5, rtol=0)
+        for k in range(BF_CFG2.gen_len):
+            np.testing.assert_allclose(logged[k][b], brows[k], atol=1e-5, rtol=1e-5)
+    # the quantization is visible: the exact-weight model gives other logits
+    _, _, exact = OracleModel(inputs).generate(prompts, BF_CFG2.gen_len, log_steps=[0])
+    assert np.abs(exact[0] - logged[0]).max() > 1e-3
+
+
+def test_fp8_quantizes_after_the_lora_merge():
+    """Quantizing the base weight and adding the delta afterwards (a plausible slip) is
+    not what the fp8 model does."""
+    inputs, _ = _bf_case(BF_CFG)
+    m = OracleModel(inputs, weights="fp8")
+    a, b = inputs.lora[0]["wq"]
+    merged = oo.merge_lora(inputs.layers[0]["wq"], a, b, BF_CFG.lora_alpha, BF_CFG.lora_r)
+    np.testing.assert_array_equal(m.layers[0]["wq"], oo.dequantize_rows(*oo.quantize_rows_e4m3(merged)))
+    base_first = oo.dequantize_rows(*oo.quantize_rows_e4m3(oo.to_f32(inputs.layers[0]["wq"])))
+    slip = base_first + oo.lora_delta(a, b, BF_CFG.lora_alpha, BF_CFG.lora_r)
+    assert np.abs(slip - m.layers[0]["wq"]).max() > 1e-4
