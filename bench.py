@@ -52,10 +52,13 @@ def layer_weight_bytes(cfg, elem=2):
     return (4 * d * d + 2 * d * f) * elem
 
 
-def decode_step_bytes(cfg, k, B, Lp, elem=2):
-    """Bytes one decode step (token k >= 1 at position Lp + k - 1) must move."""
+def decode_step_bytes(cfg, k, B, Lp, elem=2, welem=None):
+    """Bytes one decode step (token k >= 1 at position Lp + k - 1) must move.  welem:
+    bytes per projection weight (1 with fp8 weights, plus a 4-byte scale per row; the
+    tied LM head stays 16-bit), default elem."""
     n_keys = Lp + k
-    w = cfg.n_layers * layer_weight_bytes(cfg, elem) + cfg.vocab * cfg.d_model * elem
+    w = cfg.n_layers * proj_weight_bytes(cfg, elem if welem is None else welem) \
+        + cfg.vocab * cfg.d_model * elem
     kv_read = cfg.n_layers * 2 * B * n_keys * cfg.d_model * elem
     kv_write = cfg.n_layers * 2 * B * cfg.d_model * elem
     return w + kv_read + kv_write, w, kv_read + kv_write
@@ -66,8 +69,15 @@ def attn_decode_bytes(cfg, k, B, Lp, elem=2):
     return 2 * B * (Lp + k) * cfg.d_model * elem
 
 
-def decode_gemm_bytes_per_layer(cfg, elem=2):
-    return layer_weight_bytes(cfg, elem)
+def proj_weight_bytes(cfg, welem):
+    """One layer's six projections as generation streams them (fp8: codes + row scales)."""
+    if welem == 1:
+        return layer_weight_bytes(cfg, 1) + (5 * cfg.d_model + cfg.ffn) * 4
+    return layer_weight_bytes(cfg, welem)
+
+
+def decode_gemm_bytes_per_layer(cfg, elem=2, welem=None):
+    return proj_weight_bytes(cfg, elem if welem is None else welem)
 
 
 def prefill_flops(cfg, B, Lp):
@@ -264,6 +274,9 @@ def main():
     ap.add_argument("--no-score", action="store_true")
     ap.add_argument("--sampling", default=None, metavar="T,TOP_P,SEED",
                     help="sampled instead of greedy generation, e.g. 0.7,0.9,1234")
+    ap.add_argument("--weights", default="f16", choices=["f16", "fp8"],
+                    help="projection weight format during generation (fp8: E4M3 codes with "
+                         "per-row scales, decoded to fp16 on the chip)")
     ap.add_argument("--no-cuda-graph", dest="cuda_graph", action="store_false",
                     help="launch every kernel directly instead of replaying the captured "
                          "CUDA graph of the generation (enable_cuda_graph)")
@@ -303,6 +316,8 @@ def main():
     del inputs
     B, Lp, Lgen = cfg.batch, cfg.prompt_len, cfg.gen_len
     eng = he.Engine(cfg, w, max_batch=B, max_seq=Lp + Lgen)
+    if args.weights != "f16":
+        eng.set_weight_format(args.weights)
     if args.cuda_graph:
         eng.set_cuda_graph(True)
     if args.sampling:
@@ -410,8 +425,9 @@ def main():
 
     # ---- roofline of the dominant kernel and the decode phase ----
     steps = args.steps
+    welem = 1 if args.weights == "fp8" else 2
     attn_bytes = sum(attn_decode_bytes(cfg, k, B, Lp) for k in range(1, Lgen)) * cfg.n_layers
-    gemm_bytes = decode_gemm_bytes_per_layer(cfg) * cfg.n_layers * (Lgen - 1)
+    gemm_bytes = decode_gemm_bytes_per_layer(cfg, welem=welem) * cfg.n_layers * (Lgen - 1)
     per_kernel = {}
     for name, byts in (("attn_decode", attn_bytes), ("gemm", gemm_bytes)):
         ms = kls[name] / steps
@@ -427,6 +443,8 @@ def main():
     # launch here) and k_gemm_sk on the fc1 shape.  Set to None when the kernel changes.
     traffic_ratio = {"attn_decode": (1.007987e9 + 4.402432e6) / 1.00663296e9,
                      "gemm": (211.110656e6 + 6.247168e6) / 209.7152e6}
+    if args.weights != "f16":
+        traffic_ratio.pop("gemm")  # captured on the 16-bit kernel only
     traffic = (pk["bytes_per_launch"] * traffic_ratio[dom]
                if pk["bytes_per_launch"] and dom in traffic_ratio else None)
     roofline = {"bound": "hbm",
@@ -436,18 +454,23 @@ def main():
                 "peak_kind": f"{peak_kind} HBM copy bandwidth",
                 "timing": ("CUDA events around every launch of the kernel class on the engine's "
                            "stream, over a second pass of the timed steps")}
-    dec_total = sum(decode_step_bytes(cfg, k, B, Lp)[0] for k in range(1, Lgen))
+    dec_total = sum(decode_step_bytes(cfg, k, B, Lp, welem=welem)[0] for k in range(1, Lgen))
     dec_ms = phase["decode_ms"] / steps
     dec_gbs = dec_total / (dec_ms / 1000.0) / 1e9
     pf_flops, _ = prefill_flops(cfg, B, Lp)
     pf_ms = phase["prefill_ms"] / steps
     metric = METRIC if cfg.name == "opt-13b" else f"{cfg.name} generated tokens/s (B={B}, {Lp}+{Lgen})"
+    if args.weights != "f16":
+        metric += f" [{args.weights} projection weights]"
     line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": compute_dtype(cfg),
             "data": "synthetic (N(0,0.02) weights and LoRA factors, uniform prompt ids)",
-            "config": {**workload_config(cfg),
+            "config": {**workload_config(cfg), "weights": (
+                           "fp16 projections (bf16 weights merged with LoRA)" if args.weights == "f16"
+                           else "fp8 E4M3 projections, one fp32 scale per output row, decoded to "
+                                "fp16 on the chip; the tied LM head bf16"),
                        "launch": ("one CUDA graph per generation" if args.cuda_graph
                                   else "direct launches, programmatic dependent launch"),
                        "decoding": (f"sampled (temperature, top_p, seed = {args.sampling})"

@@ -21,6 +21,7 @@ _LIB_PATH = Path(__file__).resolve().parent / "libhe.so"
 HE_OK, HE_ERR_ARG, HE_ERR_STATE, HE_ERR_OOM = 0, -1, -2, -3
 HE_ERR_CUDA, HE_ERR_UNSUPPORTED, HE_ERR_DEVICE_CHECK = -4, -5, -6
 HE_DTYPE_F32, HE_DTYPE_BF16, HE_DTYPE_F16 = 0, 1, 2
+HE_WEIGHTS_F16, HE_WEIGHTS_FP8 = 0, 1
 HE_PROJ_Q, HE_PROJ_K, HE_PROJ_V, HE_PROJ_O, HE_PROJ_FC1, HE_PROJ_FC2 = range(6)
 PROJ = ("wq", "wk", "wv", "wo", "w1", "w2")
 BIAS = ("bq", "bk", "bv", "bo", "b1", "b2")
@@ -97,6 +98,11 @@ _SIGNATURES = {
     "he_op_tile_weight": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p]),
     "he_op_head_greedy": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                   c_void_p, c_void_p, c_void_p, c_void_p]),
+    "he_op_linear_fp8": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                 c_int, c_int, c_void_p, c_void_p]),
+    "he_set_weight_format": (c_int, [c_void_p, c_int]),
+    "he_read_fused_fp8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p,
+                                  c_void_p]),
     "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_op_attn_decode_noalloc": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
@@ -252,6 +258,25 @@ class Engine:
         _check(self._lib.he_read_fused_weight(self._h, layer, proj, out.data_ptr(),
                                               out.numel() * out.element_size(), self._s(stream)))
         return out
+
+    def read_fused_fp8(self, layer: int, proj: int, stream=None):
+        """With fp8 weights fused: (codes, scales) of projection `proj` of `layer`: the
+        E4M3 codes as uint8 in the fp8 tiled layout (flat) and the fp32 row scales."""
+        import torch
+        c = self.cfg
+        rows = c.ffn if proj == HE_PROJ_FC1 else c.d_model
+        cols = c.ffn if proj == HE_PROJ_FC2 else c.d_model
+        codes = torch.empty(rows * cols, dtype=torch.uint8, device=self.device)
+        scales = torch.empty(rows, dtype=torch.float32, device=self.device)
+        _check(self._lib.he_read_fused_fp8(self._h, layer, proj, codes.data_ptr(), rows * cols,
+                                           scales.data_ptr(), self._s(stream)))
+        return codes, scales
+
+    def set_weight_format(self, fmt: str):
+        """'f16' (default) or 'fp8': the format generation reads the projections in, from
+        the next fuse (or unfused generation) on (he_set_weight_format)."""
+        code = {"f16": HE_WEIGHTS_F16, "fp8": HE_WEIGHTS_FP8}[fmt]
+        _check(self._lib.he_set_weight_format(self._h, code))
 
     def release_workspace(self, stream=None):
         _check(self._lib.he_release_workspace(self._h, self._s(stream)))
@@ -433,6 +458,24 @@ def head_greedy(x, w, stream=None):
                                  w.data_ptr(), M, N, K, ids.data_ptr(), lp.data_ptr(),
                                  scratch.data_ptr(), _stream_handle(torch, stream)))
     return ids, lp
+
+
+def linear_fp8(x, w8_tiled, scale, N: int, K: int, split: int = 0, stream=None):
+    """y = (x codes^T) * scale[n] in fp32 (he_op_linear_fp8): x fp16 [M][K], w8_tiled the
+    E4M3 codes (one byte each, uint8) in the fp8 tiled layout, scale fp32 [N]."""
+    import torch
+    lib = load_library()
+    M = x.shape[0]
+    if x.dtype != torch.float16 or x.stride(1) != 1 or x.shape[1] != K:
+        raise TypeError("x must be fp16 [M][K] with dense rows")
+    R = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    scratch = torch.empty(16 * M * N + (R * K + 1) // 2 + 8 + N // 128, dtype=torch.float32,
+                          device=x.device)
+    _check(lib.he_op_linear_fp8(x.data_ptr(), x.stride(0), w8_tiled.data_ptr(), scale.data_ptr(),
+                                y.data_ptr(), M, N, K, split, scratch.data_ptr(),
+                                _stream_handle(torch, stream)))
+    return y
 
 
 def linear(x, w, split: int = 1, stream=None, w_tiled=None):

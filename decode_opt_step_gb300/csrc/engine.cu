@@ -72,6 +72,11 @@ struct he_engine {
   // BF16 while fused: the merged fp16 projections in the tiled layout, one per
   // (layer, projection), inside `restore`; generation reads these instead of w[]
   std::vector<const void *> fused_w;
+  // he_set_weight_format: HE_WEIGHTS_FP8 keeps E4M3 codes and row scales next to
+  // fused_w (which then holds the same codes as fp16 values, for the prefill GEMMs)
+  int wfmt = HE_WEIGHTS_F16;
+  std::vector<const void *> fused_w8;
+  std::vector<const float *> fused_scale;
   he_allocator alloc{};
 
   bool taken = false, fused = false;
@@ -151,6 +156,8 @@ void free_workspace(he_engine *h, cudaStream_t st) {
   for (Buf *b : all) put(h, *b, st);
   if (!h->fused) {
     h->fused_w.clear();
+    h->fused_w8.clear();
+    h->fused_scale.clear();
     h->tiled = false;
   }
   h->taken = false;
@@ -262,8 +269,13 @@ int act_rows(const he_engine *h, int B, bool decode) {
 // reduced by a second kernel); for EPI_PARTIAL the
 // fp32 slices stay in h->partial and the returned SliceInfo tells the row
 // consumer how to add them.
+// With fp8 weights (w8 and scales per row group, w the same codes as fp16 values):
+// the decode projections stream the fp8 codes through the stream-K kernel when it
+// takes them (at most 128 tokens, K % 128 == 0); every other GEMM reads the fp16
+// codes and applies the row scales in its epilogue.
 SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
-               int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w, int act) {
+               int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w, int act,
+               const void *const *w8 = nullptr, const float *const *scales = nullptr) {
   he_engine *h = c.h;
   GemmArgs a{};
   a.dtype = h->cfg.dtype;
@@ -271,6 +283,8 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   a.x = x;
   a.ldx = ldx;
   for (int g = 0; g < n_groups; ++g) a.w[g] = w[g];
+  if (scales)
+    for (int g = 0; g < n_groups; ++g) a.w_scale[g] = scales[g];
   a.n_groups = n_groups;
   a.group_rows = group_rows;
   a.M = M;
@@ -281,7 +295,12 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   float *part = static_cast<float *>(h->partial.p);
   long long stride = (long long)M * a.N;
   Timed t(h, cls, c.st);
-  if (use_stream_k(h, M, a.N, K, decode, tiled_w)) {
+  const bool fp8_sk = w8 && scales && M <= 128 && K % 128 == 0 && act == ACT_F16;
+  if (use_stream_k(h, M, a.N, K, decode, tiled_w) && (!scales || fp8_sk)) {
+    if (fp8_sk) {
+      a.w_fp8 = 1;
+      for (int g = 0; g < n_groups; ++g) a.w[g] = w8[g];
+    }
     a.split = 1;
     a.epi = epi;
     // element-wise epilogues finish inside the kernel (last run of each tile)
@@ -361,8 +380,15 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   // LN1 + QKV (+ KV append at the tokens' positions)
   // projections as generation reads them: the fused copies while fused on BF16
   auto W = [&](int p) { return tw ? h->fused_w[(size_t)l * HE_N_PROJ + p] : lw.w[p]; };
+  // fp8 weights: codes and row scales next to the fp16 codes
+  const bool f8 = tw && h->wfmt == HE_WEIGHTS_FP8;
+  auto W8 = [&](int p) { return f8 ? h->fused_w8[(size_t)l * HE_N_PROJ + p] : nullptr; };
+  auto SC = [&](int p) { return f8 ? h->fused_scale[(size_t)l * HE_N_PROJ + p] : nullptr; };
   const void *wqkv[3] = {W(HE_PROJ_Q), W(HE_PROJ_K), W(HE_PROJ_V)};
-  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw, act);
+  const void *w8qkv[3] = {W8(HE_PROJ_Q), W8(HE_PROJ_K), W8(HE_PROJ_V)};
+  const float *sqkv[3] = {SC(HE_PROJ_Q), SC(HE_PROJ_K), SC(HE_PROJ_V)};
+  gemm(c, cls_g, h->h.p, d, wqkv, 3, d, M, d, qkv_epi(h, l, tok_per_seq, pos0), dec, tw, act,
+       f8 ? w8qkv : nullptr, f8 ? sqkv : nullptr);
   Epi ep{};
   ep.kind = EPI_PARTIAL;
   // attention
@@ -386,7 +412,10 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   }
   // out projection -> partials; + bo + residual; LN2
   const void *wo[1] = {W(HE_PROJ_O)};
-  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw, act);
+  const void *w8o[1] = {W8(HE_PROJ_O)};
+  const float *so[1] = {SC(HE_PROJ_O)};
+  SliceInfo si = gemm(c, cls_g, h->ctx.p, d, wo, 1, d, M, d, ep, dec, tw, act,
+                      f8 ? w8o : nullptr, f8 ? so : nullptr);
   {
     Timed t(h, HE_KCLASS_NORM, c.st);
     c.check(launch_resid_ln(cf.dtype, act, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
@@ -402,10 +431,16 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   er.ldo = cf.ffn;
   er.out_rows = R;
   const void *w1[1] = {W(HE_PROJ_FC1)};
-  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw, act);
+  const void *w81[1] = {W8(HE_PROJ_FC1)};
+  const float *s1[1] = {SC(HE_PROJ_FC1)};
+  gemm(c, cls_g, h->h.p, d, w1, 1, cf.ffn, M, d, er, dec, tw, act, f8 ? w81 : nullptr,
+       f8 ? s1 : nullptr);
   // fc2 -> partials; + b2 + residual; next LN
   const void *w2[1] = {W(HE_PROJ_FC2)};
-  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw, act);
+  const void *w82[1] = {W8(HE_PROJ_FC2)};
+  const float *s2[1] = {SC(HE_PROJ_FC2)};
+  si = gemm(c, cls_g, h->mid.p, cf.ffn, w2, 1, d, M, cf.ffn, ep, dec, tw, act, f8 ? w82 : nullptr,
+            f8 ? s2 : nullptr);
   const bool last = l == cf.n_layers - 1;
   const void *g = last ? h->lnf_g : h->layers[l + 1].ln1_g;
   const void *bb = last ? h->lnf_b : h->layers[l + 1].ln1_b;
@@ -540,26 +575,71 @@ size_t all_proj_bytes(const he_engine *h) {
   return (size_t)c.n_layers * (4 * (size_t)c.d_model * c.d_model + 2 * (size_t)c.d_model * c.ffn) *
          h->elem;
 }
+int proj_rows(const he_config &c, int p) { return p == HE_PROJ_FC1 ? c.ffn : c.d_model; }
+int proj_cols(const he_config &c, int p) { return p == HE_PROJ_FC2 ? c.ffn : c.d_model; }
+
+// The generation copy of the projections on a BF16 engine: the fp16 tiled weights
+// (all of them), then, with fp8 weights, the fp8 tiled codes and the fp32 row
+// scales.  proj_copy_bytes sizes it; assign_proj_copy points fused_w (and fused_w8,
+// fused_scale) into it.
+size_t proj_copy_bytes(const he_engine *h) {
+  const size_t w16 = all_proj_bytes(h);
+  if (h->wfmt != HE_WEIGHTS_FP8) return w16;
+  const he_config &c = h->cfg;
+  const size_t rows = (size_t)c.n_layers * (5 * (size_t)c.d_model + c.ffn);
+  return w16 + w16 / 2 + rows * sizeof(float);
+}
+
+void assign_proj_copy(he_engine *h, void *buf) {
+  const he_config &c = h->cfg;
+  const size_t n = (size_t)c.n_layers * HE_N_PROJ;
+  const bool fp8 = h->wfmt == HE_WEIGHTS_FP8;
+  h->fused_w.assign(n, nullptr);
+  h->fused_w8.assign(fp8 ? n : 0, nullptr);
+  h->fused_scale.assign(fp8 ? n : 0, nullptr);
+  const size_t w16 = all_proj_bytes(h);
+  size_t o16 = 0, o8 = w16, os = w16 + w16 / 2;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int p = 0; p < HE_N_PROJ; ++p) {
+      const size_t i = (size_t)l * HE_N_PROJ + p, rc = (size_t)proj_rows(c, p) * proj_cols(c, p);
+      h->fused_w[i] = at(buf, o16);
+      o16 += rc * 2;
+      if (fp8) {
+        h->fused_w8[i] = at(buf, o8);
+        h->fused_scale[i] = reinterpret_cast<const float *>(at(buf, os));
+        o8 += rc;
+        os += (size_t)proj_rows(c, p) * sizeof(float);
+      }
+    }
+}
+
+// Writes projection (l, p) of the generation copy from the caller's bf16 weight,
+// merged with its LoRA pair when `lora`: fp16 tiled, or fp8 codes + scales.
+cudaError_t convert_proj(he_engine *h, int l, int p, bool lora, cudaStream_t st) {
+  const he_config &c = h->cfg;
+  const he_layer_weights &lw = h->layers[l];
+  const size_t i = (size_t)l * HE_N_PROJ + p;
+  const float scale = lora ? c.lora_alpha / (float)c.lora_r : 0.f;
+  const void *a = lora ? lw.lora_a[p] : nullptr, *b = lora ? lw.lora_b[p] : nullptr;
+  if (h->wfmt == HE_WEIGHTS_FP8)
+    return launch_fuse_fp8(const_cast<void *>(h->fused_w8[i]), const_cast<void *>(h->fused_w[i]),
+                           const_cast<float *>(h->fused_scale[i]), lw.w[p], a, b, proj_rows(c, p),
+                           proj_cols(c, p), c.lora_r, scale, st);
+  return launch_fuse_tiled(const_cast<void *>(h->fused_w[i]), ACT_F16, lw.w[p], a, b,
+                           proj_rows(c, p), proj_cols(c, p), c.lora_r, scale, st);
+}
 
 // BF16 engines always generate in fp16 from tiled projections.  While LoRA is fused
-// those are he_fuse_lora's merged copies; otherwise every generation first re-tiles
-// the caller's bf16 weights to fp16 into h->base (bf16 activations lose accuracy
-// with depth; the weights may have changed since the last call).  prepare_base takes
-// the buffer, outside any stream capture; retile_base enqueues the conversion.
+// those are he_fuse_lora's merged copies; otherwise every generation first converts
+// the caller's bf16 weights into h->base (bf16 activations lose accuracy with depth;
+// the weights may have changed since the last call).  prepare_base takes the
+// buffer, outside any stream capture; retile_base enqueues the conversion.
 he_status prepare_base(he_engine *h, cudaStream_t st) {
   const he_config &c = h->cfg;
   if (c.dtype != HE_DTYPE_BF16 || h->fused) return HE_OK;
-  if (!h->base.p && !get(h, h->base, all_proj_bytes(h), st))
-    return fail(HE_ERR_OOM, "fp16 copy of the projections (%zu bytes) failed", all_proj_bytes(h));
-  h->fused_w.assign((size_t)c.n_layers * HE_N_PROJ, nullptr);
-  size_t off = 0;
-  for (int l = 0; l < c.n_layers; ++l)
-    for (int p = 0; p < HE_N_PROJ; ++p) {
-      h->fused_w[(size_t)l * HE_N_PROJ + p] = at(h->base.p, off);
-      const size_t rows = p == HE_PROJ_FC1 ? c.ffn : c.d_model;
-      const size_t cols = p == HE_PROJ_FC2 ? c.ffn : c.d_model;
-      off += rows * cols * h->elem;
-    }
+  if (!h->base.p && !get(h, h->base, proj_copy_bytes(h), st))
+    return fail(HE_ERR_OOM, "copy of the projections (%zu bytes) failed", proj_copy_bytes(h));
+  assign_proj_copy(h, h->base.p);
   h->tiled = true;
   return HE_OK;
 }
@@ -569,13 +649,8 @@ void retile_base(Ctx &c) {
   const he_config &cf = h->cfg;
   if (cf.dtype != HE_DTYPE_BF16 || h->fused) return;
   for (int l = 0; l < cf.n_layers; ++l)
-    for (int p = 0; p < HE_N_PROJ; ++p) {
-      const int rows = p == HE_PROJ_FC1 ? cf.ffn : cf.d_model;
-      const int cols = p == HE_PROJ_FC2 ? cf.ffn : cf.d_model;
-      c.check(launch_fuse_tiled(const_cast<void *>(h->fused_w[(size_t)l * HE_N_PROJ + p]), ACT_F16,
-                                h->layers[l].w[p], nullptr, nullptr, rows, cols, 0, 0.f, c.st),
-              1);
-    }
+    for (int p = 0; p < HE_N_PROJ; ++p)
+      c.check(convert_proj(h, l, p, false, c.st), h->wfmt == HE_WEIGHTS_FP8 ? 3 : 1);
 }
 
 // Activation type of a generation: fp32 engines fp32, bf16 engines fp16.
@@ -678,6 +753,7 @@ he_status generate_internal(he_engine *h, int B, int Lp, int Lgen, cudaStream_t 
       h->kc.p, h->vc.p, h->x.p, h->h.p, h->q.p, h->ctx.p, h->mid.p, h->partial.p, h->logits.p,
       h->attn_part.p, h->ids_in.p, h->ids_out.p, h->lp_out.p, h->err.p, h->tilecnt.p,
       h->restore.p, h->base.p, reinterpret_cast<const void *>((uintptr_t)h->fused),
+      reinterpret_cast<const void *>((uintptr_t)h->wfmt),
       reinterpret_cast<const void *>((uintptr_t)float_bits(h->temperature)),
       reinterpret_cast<const void *>((uintptr_t)float_bits(h->top_p)),
       reinterpret_cast<const void *>((uintptr_t)h->seed)};
@@ -878,48 +954,49 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
   cudaSetDevice(h->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const he_config &c = h->cfg;
-  auto rows_of = [&](int p) { return p == HE_PROJ_FC1 ? c.ffn : c.d_model; };
-  auto cols_of = [&](int p) { return p == HE_PROJ_FC2 ? c.ffn : c.d_model; };
+  const bool bf = c.dtype == HE_DTYPE_BF16;
   size_t total = 0;
-  for (int l = 0; l < c.n_layers; ++l)
-    for (int p = 0; p < HE_N_PROJ; ++p)
-      if (fuse_touches(h, p)) total += (size_t)rows_of(p) * cols_of(p) * h->elem;
-  put(h, h->base, st);  // the unfused generations' fp16 copy: the fused one replaces it
+  if (bf) {
+    total = proj_copy_bytes(h);
+  } else {
+    for (int l = 0; l < c.n_layers; ++l)
+      for (int p = 0; p < HE_N_PROJ; ++p)
+        if (fuse_touches(h, p)) total += (size_t)proj_rows(c, p) * proj_cols(c, p) * h->elem;
+  }
+  put(h, h->base, st);  // the unfused generations' copy: the fused one replaces it
   h->fused_w.clear();
+  h->fused_w8.clear();
+  h->fused_scale.clear();
   h->tiled = false;
   if (!get(h, h->restore, total, st))
     return fail(HE_ERR_OOM, "LoRA fuse buffer of %zu bytes failed", total);
   ensure_phase_events(h);
   cudaEventRecord(h->ph[3], st);
   const float scale = c.lora_targets ? c.lora_alpha / (float)c.lora_r : 0.f;
-  const bool bf = c.dtype == HE_DTYPE_BF16;
-  h->fused_w.assign((size_t)c.n_layers * HE_N_PROJ, nullptr);
-  size_t off = 0;
   cudaError_t err = cudaSuccess;
   auto chk = [&](cudaError_t e, int n) {
     if (e != cudaSuccess && err == cudaSuccess) err = e;
     h->stats.launches += n;
   };
-  for (int l = 0; l < c.n_layers; ++l) {
-    const he_layer_weights &lw = h->layers[l];
-    for (int p = 0; p < HE_N_PROJ; ++p) {
-      if (!fuse_touches(h, p)) continue;
-      const size_t bytes = (size_t)rows_of(p) * cols_of(p) * h->elem;
-      void *save = at(h->restore.p, off);
-      const bool lora = (c.lora_targets >> p) & 1u;
-      if (bf) {
-        // the merged weight, tiled, into the engine's buffer; w[] stays as it is
-        chk(launch_fuse_tiled(save, ACT_F16, lw.w[p], lora ? lw.lora_a[p] : nullptr,
-                              lora ? lw.lora_b[p] : nullptr, rows_of(p), cols_of(p), c.lora_r,
-                              scale, st),
+  if (bf) {
+    // the merged weights (all six projections, tiled; fp8 codes and scales with fp8
+    // weights) into the engine's buffer; w[] stays as it is
+    assign_proj_copy(h, h->restore.p);
+    for (int l = 0; l < c.n_layers; ++l)
+      for (int p = 0; p < HE_N_PROJ; ++p)
+        chk(convert_proj(h, l, p, (c.lora_targets >> p) & 1u, st),
+            h->wfmt == HE_WEIGHTS_FP8 ? 3 : 1);
+  } else {
+    size_t off = 0;
+    for (int l = 0; l < c.n_layers; ++l) {
+      const he_layer_weights &lw = h->layers[l];
+      for (int p = 0; p < HE_N_PROJ; ++p) {
+        if (!fuse_touches(h, p)) continue;
+        chk(launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p], at(h->restore.p, off),
+                             proj_rows(c, p), proj_cols(c, p), c.lora_r, scale, st),
             1);
-        h->fused_w[(size_t)l * HE_N_PROJ + p] = save;
-      } else {
-        chk(launch_lora_fuse(c.dtype, lw.w[p], lw.lora_a[p], lw.lora_b[p], save, rows_of(p),
-                             cols_of(p), c.lora_r, scale, st),
-            1);
+        off += (size_t)proj_rows(c, p) * proj_cols(c, p) * h->elem;
       }
-      off += bytes;
     }
   }
   cudaEventRecord(h->ph[4], st);
@@ -928,6 +1005,45 @@ he_status he_fuse_lora(he_engine *h, void *stream) {
   h->tiled = bf;
   h->stats.restore_bytes = total;
   if (err != cudaSuccess) return cuda_fail(err, "LoRA fuse launch");
+  return HE_OK;
+}
+
+he_status he_set_weight_format(he_engine *h, int format) {
+  g_err.clear();
+  if (!h) return fail(HE_ERR_ARG, "engine is NULL");
+  if (format != HE_WEIGHTS_F16 && format != HE_WEIGHTS_FP8) return fail(HE_ERR_ARG, "bad format");
+  if (h->cfg.dtype != HE_DTYPE_BF16 && format != HE_WEIGHTS_F16)
+    return fail(HE_ERR_UNSUPPORTED, "fp8 weights need a BF16 engine");
+  if (h->fused) return fail(HE_ERR_STATE, "unfuse LoRA before changing the weight format");
+  if (format == h->wfmt) return HE_OK;
+  cudaSetDevice(h->device);
+  put(h, h->base, nullptr);  // its layout depends on the format
+  h->fused_w.clear();
+  h->fused_w8.clear();
+  h->fused_scale.clear();
+  h->tiled = false;
+  h->wfmt = format;
+  return HE_OK;
+}
+
+he_status he_read_fused_fp8(he_engine *h, int layer, int proj, void *codes, size_t code_bytes,
+                            float *scales, void *stream) {
+  g_err.clear();
+  if (!h || !codes || !scales) return fail(HE_ERR_ARG, "NULL argument");
+  if (!h->fused || h->wfmt != HE_WEIGHTS_FP8)
+    return fail(HE_ERR_STATE, "LoRA is not fused with fp8 weights");
+  const he_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || proj < 0 || proj >= HE_N_PROJ)
+    return fail(HE_ERR_ARG, "bad layer or projection");
+  const size_t rows = proj_rows(c, proj), cols = proj_cols(c, proj);
+  if (code_bytes != rows * cols) return fail(HE_ERR_ARG, "code_bytes must be %zu", rows * cols);
+  cudaSetDevice(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t i = (size_t)layer * HE_N_PROJ + proj;
+  cudaError_t e = cudaMemcpyAsync(codes, h->fused_w8[i], rows * cols, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(scales, h->fused_scale[i], rows * sizeof(float), cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "he_read_fused_fp8");
   return HE_OK;
 }
 
@@ -978,6 +1094,8 @@ he_status he_unfuse_lora(he_engine *h, void *stream) {
   h->unfuse_pending = true;
   put(h, h->restore, st);
   h->fused_w.clear();
+  h->fused_w8.clear();
+  h->fused_scale.clear();
   h->fused = false;
   h->tiled = false;
   h->stats.restore_bytes = 0;
@@ -1322,6 +1440,57 @@ he_status he_op_head_greedy(int dtype, const void *x, int ldx, const void *w, in
     r = launch_head_select(HE_DTYPE_BF16, dtype, ha, st);
   }
   if (r != cudaSuccess) return cuda_fail(r, "he_op_head_greedy");
+  return HE_OK;
+}
+
+he_status he_op_linear_fp8(const void *x, int ldx, const void *w8, const float *scale, float *y,
+                           int M, int N, int K, int split, float *scratch, void *stream) {
+  g_err.clear();
+  if (!x || !w8 || !scale || !y || !scratch) return fail(HE_ERR_ARG, "NULL buffer");
+  if (M < 1 || M > 128 || N < 128 || N % 128 || K < 128 || K % 128 || ldx < K || ldx % 8)
+    return fail(HE_ERR_UNSUPPORTED,
+                "fp8 GEMM needs 1 <= M <= 128, N and K multiples of 128, ldx >= K, ldx %% 8 == 0");
+  if ((uintptr_t)x % 16 || (uintptr_t)w8 % 16 || (uintptr_t)y % 16 || (uintptr_t)scratch % 16)
+    return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  GemmArgs a{};
+  a.dtype = HE_DTYPE_BF16;
+  a.act = ACT_F16;
+  a.ldx = K;
+  a.w[0] = w8;
+  a.w_scale[0] = scale;
+  a.w_fp8 = 1;
+  a.w_tiled = 1;
+  a.n_groups = 1;
+  a.group_rows = N;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.split = 1;
+  Epi e{};
+  e.kind = EPI_STORE_F32;
+  e.partial = y;
+  e.ldp = N;
+  a.epi = e;
+  const long long T = N / 128, U = sk_units(a);
+  int P = sk_ctas(a, sms, true);
+  if (split < 0) {
+    if (-split > U || -split > 15 * T)
+      return fail(HE_ERR_ARG, "stream-K CTA count %d above min(units, 15 * tiles)", -split);
+    P = -split;
+  }
+  const int R = sk_token_tile(M);
+  const long long sstride = (long long)M * N;
+  void *xt = scratch + (size_t)16 * sstride;
+  int *cnt = reinterpret_cast<int *>(((uintptr_t)xt + (size_t)R * K * 2 + 15) & ~(uintptr_t)15);
+  a.x = xt;
+  cudaError_t r = launch_tile_act(x, M, K, ldx, R, xt, st);
+  if (r == cudaSuccess) r = cudaMemsetAsync(cnt, 0, (size_t)T * sizeof(int), st);
+  if (r == cudaSuccess) r = launch_gemm_sk(a, P, scratch, sstride, cnt, nullptr, st);
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_linear_fp8");
   return HE_OK;
 }
 

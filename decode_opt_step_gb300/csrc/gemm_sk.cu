@@ -70,8 +70,27 @@ struct SkCfg {
   static constexpr uint32_t TMEM_COLS = pow2_cols(2 * BN);
 };
 
+// FP8 weights (W8): the weights of a stage are one 128 x 128 E4M3 tile (16 KB) that
+// converter warps decode to fp16 (exactly: every E4M3 value is an fp16 value) and
+// store into tensor memory as the MMA's A operand; the stage's activations still come
+// from shared memory.  Weights and activations have rings of their own (S8 and SB
+// stages).  TMEM holds the two accumulators (2 BN columns) and SA decoded A stages
+// of 64 columns each.
+constexpr int W8_BYTES = 128 * 128;  // one fp8 weight stage: 128 rows x 128 k
+template <int BN> struct Sk8Cfg {
+  static constexpr int SB = BN >= 128 ? 3 : BN == 64 ? 4 : BN == 32 ? 5 : 6;  // activation stages
+  static constexpr int S8 = BN >= 128 ? 6 : BN == 64 ? 8 : BN == 32 ? 9 : 10; // weight stages
+  static constexpr int STAGE_B = 2 * BN * BK * 2;
+  static constexpr int SA = (512 - 2 * BN) / 64 < 6 ? (512 - 2 * BN) / 64 : 6;
+  static constexpr uint32_t A_COL0 = 2 * BN;
+  static constexpr int RING = S8 * W8_BYTES + SB * STAGE_B;
+  static constexpr int SMEM = 1024 + RING + 512;
+};
+
 struct SkArgs {
   const uint16_t *wt[3]; // tiled weights per row group (tiled == 1), 16-bit elements
+  const uint8_t *w8[3];  // fp8 tiled weights per row group (W8 kernels)
+  const float *wscale[3];// per-row fp32 scales of the fp8 weights (W8 kernels)
   int tiled;
   int tiles_per_group;   // 128-row tiles per group (multiple groups only)
   int n_groups;
@@ -86,6 +105,8 @@ constexpr int EPW = 8;              // epilogue warps
 constexpr int EPT = 32 * EPW;        // epilogue threads
 constexpr int SK_THREADS = EPT + 64; // + producer warp + MMA warp
 constexpr int PRODUCER = EPW, MMA = EPW + 1;
+constexpr int CONV0 = EPW + 2;       // W8: four converter warps (one per TMEM lane quarter)
+constexpr int SK8_THREADS = SK_THREADS + 128;
 
 // EPI_ARGMAX for a tile stored directly (one run): the greedy statistics of each
 // token column over the tile's 128 rows (features n >= N left out).  Rounds of 32
@@ -135,24 +156,33 @@ __device__ __forceinline__ void argmax_tile_direct(const Epi &epi, uint32_t tl, 
   }
 }
 
-template <typename CT, int BN, int STAGES, int KPS>
-__global__ void __launch_bounds__(SK_THREADS, 1)
+template <typename CT, int BN, int STAGES, int KPS, bool W8 = false>
+__global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const uint16_t *x,
               int ldx, int *dev_err) {
   using C = SkCfg<BN, STAGES, KPS>;
+  using C8 = Sk8Cfg<BN>;
+  static_assert(!W8 || (KPS == 2 && BN <= 128), "fp8 weights: 128-k stages, at most 128 tokens");
+  constexpr uint32_t kTmemCols = W8 ? 512u : C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  // 16-bit weights: [STAGES x (A | B)]; W8: [S8 fp8 weight stages][SB activation stages]
   uint8_t *smA = base;
-  uint8_t *smB = base + STAGES * C::STAGE_A;
-  uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES);
-  uint64_t *empty = full + STAGES;
-  uint64_t *acc_full = empty + STAGES;   // [2]
+  uint8_t *smW8 = base;
+  uint8_t *smB = W8 ? base + C8::S8 * W8_BYTES : base + STAGES * C::STAGE_A;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + (W8 ? C8::RING : STAGES * C::STAGE_BYTES));
+  uint64_t *empty = full + (W8 ? C8::SB : STAGES);
+  uint64_t *acc_full = empty + (W8 ? C8::SB : STAGES);  // [2]
   uint64_t *acc_empty = acc_full + 2;    // [2]
   uint64_t *fix_bar = acc_empty + 2;     // the owner's slice copies (tile_owner_epilogue)
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 1);
+  uint64_t *w8_full = fix_bar + 1;       // W8 only: [S8]
+  uint64_t *w8_empty = w8_full + (W8 ? C8::S8 : 0);  // [S8]
+  uint64_t *a_full = w8_empty + (W8 ? C8::S8 : 0);   // [SA] decoded A stage in TMEM
+  uint64_t *a_empty = a_full + (W8 ? C8::SA : 0);    // [SA]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(a_empty + (W8 ? C8::SA : 0));
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
   int *last_flag = abort_flag + 1;
 
@@ -161,7 +191,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const long long u_begin = (long long)c * a.U / P, u_end = (long long)(c + 1) * a.U / P;
 
   if (warp == PRODUCER && lane == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    const int nst = W8 ? C8::SB : STAGES;
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -170,11 +201,21 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       mbar_init(&acc_empty[b], EPW);  // one arrival per epilogue warp
     }
     mbar_init(fix_bar, 1);
+    if constexpr (W8) {
+      for (int s = 0; s < C8::S8; ++s) {
+        mbar_init(&w8_full[s], 1);
+        mbar_init(&w8_empty[s], 4);  // one arrival per converter warp
+      }
+      for (int s = 0; s < C8::SA; ++s) {
+        mbar_init(&a_full[s], 4);
+        mbar_init(&a_empty[s], 1);  // the MMAs reading the stage have completed
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == MMA) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -183,7 +224,93 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();  // one CTA per SM: the next kernel may start its set-up
 
-  if (warp == PRODUCER && lane == 0) {
+  if (W8 && warp == PRODUCER && lane < 2) {
+    // ---------------- loads, fp8 weights ----------------
+    // lane 0 streams the weight stages (before waiting on the kernel before this one:
+    // they do not depend on it), lane 1 the activation stages; each ring runs on its
+    // own, so the weights may run ahead of the activations.
+    const bool wts = lane == 0;
+    const int NS = wts ? C8::S8 : C8::SB;
+    const uint32_t bytes = wts ? (uint32_t)W8_BYTES : (uint32_t)C8::STAGE_B;
+    uint64_t *fb = wts ? w8_full : full;
+    uint64_t *eb = wts ? w8_empty : empty;
+    const uint64_t pol = l2_evict_first_policy();
+    if (!wts) pdl_wait();
+    long long issued = 0;
+    for (long long u = u_begin; u < u_end; ++u) {
+      const long long i = u - u_begin;
+      const int s = (int)(i % NS);
+      if (i >= NS && !mbar_wait_bounded(&eb[s], (uint32_t)((i / NS - 1) & 1))) {
+        *(volatile int *)abort_flag = 1;
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (*(volatile int *)abort_flag) break;
+      const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
+      mbar_arrive_expect_tx(&fb[s], bytes);
+      if (wts) {
+        const int group = a.n_groups > 1 ? t / a.tiles_per_group : 0;
+        const int lt = t - group * (a.n_groups > 1 ? a.tiles_per_group : 0);
+        bulk_load_hint(smW8 + s * W8_BYTES, a.w8[group] + ((long long)lt * a.KB + kb) * W8_BYTES,
+                       bytes, &fb[s], pol);
+      } else {
+        bulk_load(smB + s * C8::STAGE_B, x + (long long)kb * KPS * BN * BK, bytes, &fb[s]);
+      }
+      issued = i + 1;
+    }
+    // every requested stage lands before the CTA can finish
+    for (long long i = issued > NS ? issued - NS : 0; i < issued; ++i)
+      if (!mbar_wait_bounded(&fb[i % NS], (uint32_t)((i / NS) & 1)))
+        set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+  } else if (W8 && warp >= CONV0) {
+    // ---------------- fp8 -> fp16 into TMEM (A operand) ----------------
+    // Thread = weight row r (TMEM lane r; warp w reaches lanes 32 (w % 4) ..): its 128
+    // fp8 values are eight 16-byte chunks, chunk j (k = 16 j ..) at slot j ^ (r % 8) of
+    // the row's 128 bytes; decoded pairs go to TMEM columns 8 j .. 8 j + 7 of the stage.
+    const int quarter = warp & 3, r = quarter * 32 + lane;
+    const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + C8::A_COL0;
+    for (long long u = u_begin; u < u_end; ++u) {
+      const long long i = u - u_begin;
+      const int s8 = (int)(i % C8::S8), sa = (int)(i % C8::SA);
+      bool ok = mbar_wait_bounded(&w8_full[s8], (uint32_t)((i / C8::S8) & 1));
+      if (ok && i >= C8::SA)
+        ok = mbar_wait_bounded(&a_empty[sa], (uint32_t)((i / C8::SA - 1) & 1));
+      if (!ok || *(volatile int *)abort_flag) {
+        if (!ok) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+        *(volatile int *)abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t row_s = smem_u32(smW8 + s8 * W8_BYTES + r * 128);
+      uint4 ch[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ch[j] = lds_u128(row_s + (uint32_t)((j ^ (r & 7)) * 16));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&w8_empty[s8]);  // the fp8 stage may be refilled
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t *q = reinterpret_cast<const uint32_t *>(&ch[2 * g + h]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                (__nv_fp8x2_storage_t)(q[e] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                (__nv_fp8x2_storage_t)(q[e] >> 16), __NV_E4M3);
+            w[8 * h + 2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+            w[8 * h + 2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+          }
+        }
+        tmem_st16(trow + (uint32_t)(sa * 64 + g * 16), w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[sa]);
+    }
+  } else if (!W8 && warp == PRODUCER && lane == 0) {
     // ---------------- loads ----------------
     if (!a.tiled) {
       prefetch_tmap(&tm_w0);
@@ -256,6 +383,35 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       }
       tc_fence_after();
       const uint32_t acc = tmem_base + (uint32_t)(buf * BN);
+      if constexpr (W8) {
+        for (int j = 0; j < n; ++j) {
+          const long long i = u - u_begin + j;
+          const int sb = (int)(i % C8::SB), sa = (int)(i % C8::SA);
+          if (!mbar_wait_bounded(&full[sb], (uint32_t)((i / C8::SB) & 1)) ||
+              !mbar_wait_bounded(&a_full[sa], (uint32_t)((i / C8::SA) & 1)) ||
+              *(volatile int *)abort_flag) {
+            *(volatile int *)abort_flag = 1;
+            set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < KPS; ++q) {
+            const uint32_t b0 = smem_u32(smB + sb * C8::STAGE_B + q * C::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              tc_mma_f16_tmem_a(acc, tmem_base + C8::A_COL0 + (uint32_t)(sa * 64 + (q * 4 + kk) * 8),
+                                sdesc_sw128(b0 + kk * UMMA_K * 2), idesc, (j | q | kk) != 0);
+          }
+          tc_commit(&empty[sb]);
+          tc_commit(&a_empty[sa]);
+        }
+        tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
+        u += n;
+        ++seg;
+        continue;
+      }
       for (int j = 0; j < n; ++j) {
         const long long i = u - u_begin + j;
         const int s = (int)(i % STAGES);
@@ -297,7 +453,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const bool fix = a.tile_cnt != nullptr && epi.kind != EPI_PARTIAL;
     __shared__ ArgStat am_part[2][4][16];  // EPI_ARGMAX: per column half, lane quarter, column
     constexpr int W = BN >= 32 ? 32 : 16;
-    constexpr int kStageAvail = STAGES * C::STAGE_BYTES;
+    constexpr int kStageAvail = W8 ? C8::RING : STAGES * C::STAGE_BYTES;
     // The bias of this thread's row in the tile of the last segment (the one an
     // owner finishes at the end of the run), read before waiting on the kernel
     // before this one: parameters do not depend on it.
@@ -323,13 +479,20 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       const int slot = c - cf;
       const int row = t * BM + quarter * 32 + lane;
       const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+      // W8: this row's fp8 scale, applied as the accumulator leaves TMEM
+      float rs = 1.f;
+      if constexpr (W8) {
+        const int group = a.n_groups > 1 ? t / a.tiles_per_group : 0;
+        const int gr = row - group * (a.n_groups > 1 ? a.tiles_per_group : 0) * BM;
+        if (row < a.N) rs = a.wscale[group][gr];
+      }
       // (all conditions below are uniform over the four epilogue warps)
       const bool staged = fix && slot == 0 && u + n == u_end &&
                           tile_stage_tokens(S, a.M, W, kStageAvail) >= W;
       if (staged) {
         tile_owner_epilogue<CT, W, EPT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride,
                                         a.N, a.M, t, S, tl, live, &a.tile_cnt[t], base,
-                                        kStageAvail, fix_bar, last_flag, dev_err, last_bias);
+                                        kStageAvail, fix_bar, last_flag, dev_err, last_bias, rs);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -356,6 +519,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         for (int c0 = c_begin; c0 < c_end; c0 += WH) {
           float v[WH];
           tmem_load_cols<WH>(tl + c0, v);
+          if constexpr (W8) {
+#pragma unroll
+            for (int j = 0; j < WH; ++j) v[j] *= rs;
+          }
           if (live && row < a.N && c0 < a.M) row_epi_store<CT, WH>(re, c0, min(WH, a.M - c0), v);
         }
         tc_fence_before();
@@ -392,15 +559,16 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   __syncthreads();
   if (warp == MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <typename CT, int BN, int STAGES, int KPS>
+template <typename CT, int BN, int STAGES, int KPS, bool W8 = false>
 cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slice_stride,
                          int *tile_cnt, int *dev_err, cudaStream_t st) {
   using C = SkCfg<BN, STAGES, KPS>;
   constexpr bool fp16 = !std::is_same<CT, bf16>::value;
+  constexpr int kSmem = W8 ? Sk8Cfg<BN>::SMEM : C::SMEM;
   CUtensorMap tw[3], tx;
   memset(tw, 0, sizeof tw);
   SkArgs a{};
@@ -409,10 +577,15 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.tiles_per_group = g.n_groups > 1 ? g.group_rows / BM : 1;
   for (int i = 0; i < 3; ++i) {
     const void *p = g.w[i < g.n_groups ? i : 0];
-    if (g.w_tiled)
+    if (W8) {
+      a.w8[i] = static_cast<const uint8_t *>(p);
+      a.wscale[i] = g.w_scale[i < g.n_groups ? i : 0];
+      if ((uintptr_t)p % 16 || !a.wscale[i]) return cudaErrorInvalidValue;
+    } else if (g.w_tiled) {
       a.wt[i] = static_cast<const uint16_t *>(p);
-    else if (i < g.n_groups && !make_tmap_16(&tw[i], p, g.group_rows, g.K, g.K, BM, fp16))
+    } else if (i < g.n_groups && !make_tmap_16(&tw[i], p, g.group_rows, g.K, g.K, BM, fp16)) {
       return cudaErrorInvalidValue;
+    }
   }
   memset(&tx, 0, sizeof tx);  // activations arrive by bulk copy (row-tiled layout)
   if ((uintptr_t)g.x % 16) return cudaErrorInvalidValue;
@@ -423,10 +596,11 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.slices = slices;
   a.slice_stride = slice_stride;
   a.tile_cnt = tile_cnt;
-  cudaError_t ae = ensure_smem_limit<k_gemm_sk<CT, BN, STAGES, KPS>>(C::SMEM);
+  cudaError_t ae = ensure_smem_limit<k_gemm_sk<CT, BN, STAGES, KPS, W8>>(kSmem);
   if (ae != cudaSuccess) return ae;
-  return launch_k(k_gemm_sk<CT, BN, STAGES, KPS>, dim3(P), dim3(SK_THREADS), C::SMEM, st, g_pdl, tw[0],
-                  tw[1], tw[2], tx, a, g.epi, static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
+  return launch_k(k_gemm_sk<CT, BN, STAGES, KPS, W8>, dim3(P), dim3(W8 ? SK8_THREADS : SK_THREADS),
+                  kSmem, st, g_pdl, tw[0], tw[1], tw[2], tx, a, g.epi,
+                  static_cast<const uint16_t *>(g.x), g.ldx, dev_err);
 }
 
 }  // namespace
@@ -508,6 +682,20 @@ cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long sl
                    slice_stride < (long long)g.M * ((g.N + BM - 1) / BM) * BM))
     return cudaErrorInvalidValue;
   if (g.epi.kind == EPI_ARGMAX && (!tile_cnt || !sk_argmax_ok(g, P))) return cudaErrorInvalidValue;
+  if (g.w_fp8) {
+    // fp8 weights (fp8 tiled layout, K % 128 == 0, whole 128-row tiles) with fp16
+    // activations, at most 128 tokens
+    if (g.act != ACT_F16 || g.M > 128 || g.K % 128 || (g.group_rows % BM) ||
+        g.epi.kind == EPI_ARGMAX)
+      return cudaErrorInvalidValue;
+#define HE_SK8(BN) \
+  return launch_sk_bn<f16, BN, Sk8Cfg<BN>::SB, 2, true>(g, P, slices, slice_stride, tile_cnt, dev_err, st)
+    if (g.M <= 16) HE_SK8(16);
+    if (g.M <= 32) HE_SK8(32);
+    if (g.M <= 64) HE_SK8(64);
+    HE_SK8(128);
+#undef HE_SK8
+  }
   auto pick = [&](auto ct) -> cudaError_t {
     using CT = decltype(ct);
 #define HE_SK(BN, ST, KPS) \

@@ -63,7 +63,18 @@ struct Cfg {
 struct WTiles {
   const uint16_t *p[3];  // tiled weights of each row group (ABULK), 16-bit elements
   int kt;                // 64-wide k tiles per 128-row tile row
+  // per-row scales of each row group, or null: the weights hold fp8 codes (as exact
+  // 16-bit values) and output row n is scaled by its group's scale[n - group start]
+  const float *scale[3];
+  int group_rows;
 };
+
+// The scale of output feature `row` (1 without scales).
+__device__ __forceinline__ float wt_row_scale(const WTiles &wt, int row, int N) {
+  if (!wt.scale[0] || row >= N) return 1.f;
+  const int g = wt.group_rows > 0 ? row / wt.group_rows : 0;
+  return wt.scale[g][row - g * wt.group_rows];
+}
 
 template <typename CT, int BN, int STAGES, bool ABULK>
 __global__ void __launch_bounds__(192, 1)
@@ -175,10 +186,13 @@ __global__ void __launch_bounds__(192, 1)
     const RowEpi<CT> re = row_epi_prepare<CT>(epi, row < N ? row : 0, part ? epi.partial : nullptr,
                                               epi.split_stride, split, epi.ldp);
     const int tok_base = n_tile * BN;
+    const float rs = wt_row_scale(wt, row, N);
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += W) {
       float v[W];
       tmem_load_cols<W>(tl + c0, v);
+#pragma unroll
+      for (int j = 0; j < W; ++j) v[j] *= rs;
       if (live && row < N && tok_base + c0 < M)
         row_epi_store<CT, W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
     }
@@ -359,10 +373,13 @@ __global__ void __launch_bounds__(192, 1)
                                                 part ? epi.partial : nullptr, epi.split_stride,
                                                 0, epi.ldp);
       const int tok_base = nt * PBN;
+      const float rs = wt_row_scale(wt, row, N);
 #pragma unroll 1
       for (int c0 = 0; c0 < PBN; c0 += W) {
         float v[W];
         tmem_load_cols<W>(tl + c0, v);
+#pragma unroll
+        for (int j = 0; j < W; ++j) v[j] *= rs;
         if (live && row < N && tok_base + c0 < M)
           row_epi_store<CT, W>(re, tok_base + c0, min(W, M - tok_base - c0), v);
       }
@@ -431,6 +448,9 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   wt.kt = a.K / BK;
+  wt.group_rows = a.group_rows;
+  if (a.w_scale[0])
+    for (int g = 0; g < 3; ++g) wt.scale[g] = a.w_scale[g < a.n_groups ? g : 0];
   if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, BN, tmap_type<CT>())) return cudaErrorInvalidValue;
   cudaError_t ae = ensure_smem_limit<k_gemm_tc<CT, BN, STAGES, ABULK>>(C::SMEM);
   if (ae != cudaSuccess) return ae;
@@ -458,6 +478,9 @@ cudaError_t launch_tcp(const GemmArgs &a, int num_sms, int *dev_err, cudaStream_
       return cudaErrorInvalidValue;
   }
   wt.kt = a.K / BK;
+  wt.group_rows = a.group_rows;
+  if (a.w_scale[0])
+    for (int g = 0; g < 3; ++g) wt.scale[g] = a.w_scale[g < a.n_groups ? g : 0];
   if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, PBN, tmap_type<CT>())) return cudaErrorInvalidValue;
   cudaError_t ae = ensure_smem_limit<k_gemm_tcp<CT, ABULK>>(C::SMEM);
   if (ae != cudaSuccess) return ae;

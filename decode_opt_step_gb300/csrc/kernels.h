@@ -112,7 +112,7 @@ struct Epi {
 // tile (mt, kt) contiguous at element (mt * K/64 + kt) * 8192; inside a tile, row r
 // occupies 128 bytes whose 16-byte chunk c sits at slot c ^ (r % 8) -- the image
 // the tensor cores read with 128-byte swizzling, so one bulk copy fills a stage.
-inline long long tiled_index(long long n, long long k, long long K) {
+__host__ __device__ inline long long tiled_index(long long n, long long k, long long K) {
   return ((n / 128) * (K / 64) + k / 64) * 8192 + (n % 128) * 64 +
          ((((k % 64) / 8) ^ (n % 8)) * 8) + (k % 8);
 }
@@ -138,8 +138,21 @@ struct GemmArgs {
   int M, N, K;           // tokens, output features (= n_groups * group_rows), reduction
   int split;             // split-K factor (EPI_PARTIAL writes split slices)
   int w_tiled;           // bf16 only: w[] hold the tiled layout above
+  // fp8 weights (stream-K only): w[] hold E4M3 codes in the fp8 tiled layout below and
+  // w_scale[] the fp32 scale of every row of each group; output = scale * (codes . x)
+  int w_fp8;
+  const float *w_scale[3];
   Epi epi;
 };
+
+// FP8 tiled weight layout: W [N][K] with N % 128 == 0 and K % 128 == 0 as (N/128) x
+// (K/128) tiles of 128 x 128 one-byte E4M3 codes, tile (mt, kt) contiguous at byte
+// (mt * K/128 + kt) * 16384; inside a tile row r occupies 128 bytes whose 16-byte
+// chunk c (k = 16 c .. 16 c + 15) sits at slot c ^ (r % 8).
+__host__ __device__ inline long long tiled8_index(long long n, long long k, long long K) {
+  return ((n / 128) * (K / 128) + k / 128) * 16384 + (n % 128) * 128 +
+         ((((k % 128) / 16) ^ (n % 8)) * 16) + (k % 16);
+}
 
 // Split-K works in blocks of 64 along K; a split covers split_kblocks(K, S)
 // consecutive blocks.  effective_split(K, S) is the number of non-empty slices,
@@ -288,5 +301,14 @@ cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const voi
                               const void *bm, int rows, int cols, int r, float scale,
                               cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
+// FP8 weights of a projection W [rows][cols] (bf16, rows and cols multiples of 128):
+// the merged weight W + scale B A (A / B may be null) gets the row scales
+// rscale[n] = max_k |W'[n][k]| / 448 (1 for a zero row), its E4M3 codes (nearest,
+// ties to even, saturated) in the fp8 tiled layout (out8, rows * cols bytes) and the
+// same codes as exact fp16 values in the 16-bit tiled layout (out16).  3 launches
+// and a memset of rscale.
+cudaError_t launch_fuse_fp8(void *out8, void *out16, float *rscale, const void *src, const void *a,
+                            const void *bm, int rows, int cols, int r, float scale,
+                            cudaStream_t st);
 
 }  // namespace he

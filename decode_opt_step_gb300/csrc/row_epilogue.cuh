@@ -354,14 +354,17 @@ __device__ __forceinline__ float tile_row_bias(const Epi &e, int n, int N) {
 // on the mbarrier `bar`), each thread adds its row's values in slot order (its own
 // slice is slot 0) and applies the epilogue into a [token][128] fp32 staging
 // tile, which then leaves (rounded to the output type) as 16-byte stores.  `bias`
-// is this thread's row's (tile_row_bias).  `flag` is a shared int; returns with
+// is this thread's row's (tile_row_bias); `rs` scales this thread's own accumulator
+// (the row scale of fp8 weights, else 1; the other slices arrive scaled).  `flag` is
+// a shared int; returns with
 // every epilogue thread past the same barriers.
 template <typename CT, int W, int NT>
 __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *tslices,
                                                     long long sstride, int N, int M, int t, int S,
                                                     uint32_t tl, bool live, int *cnt,
                                                     uint8_t *stage, int avail, uint64_t *bar,
-                                                    int *flag, int *dev_err, float bias) {
+                                                    int *flag, int *dev_err, float bias,
+                                                    float rs = 1.f) {
   static_assert(NT == 256, "two threads per TMEM lane");
   const int et = threadIdx.x, r = et & 127, hf = et >> 7;  // row (feature) of the tile, half
   const int n_row = t * 128 + r;
@@ -409,6 +412,8 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
       // stay inside the chunk's staging (ch is a multiple of W)
       float v[W];
       tmem_load_cols<W>(tl + (uint32_t)(c0 + j0), v);
+#pragma unroll
+      for (int j = 0; j < W; ++j) v[j] *= rs;  // (the row's fp8 weight scale, else 1)
       for (int s = 0; s < S - 1; ++s) {
         const uint32_t src = ps_s + (uint32_t)((((size_t)s * ch + j0) * 128 + r) * 4);
         float p[W];

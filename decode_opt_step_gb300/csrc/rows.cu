@@ -557,6 +557,116 @@ __global__ void __launch_bounds__(256, 4)
   }
 }
 
+// FP8 weights, pass 1: per row of the merged weight W + scale B A (bf16 W, A, B),
+// the largest |value| as float bits (atomicMax on non-negative bits is the float
+// maximum, whatever the order of the tiles) into amax_bits[row], zero on entry.
+// One CTA per 128 x 64 tile, the thread layout of k_fuse_tiled.
+__global__ void __launch_bounds__(256, 4)
+    k_fuse_amax(unsigned *amax_bits, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows,
+                int cols, int r, float scale) {
+  const long long t = blockIdx.x;
+  const int KT = cols / 64;
+  const int rr = threadIdx.x >> 3, c = threadIdx.x & 7;
+  const int n0 = (int)(t / KT) * 128 + rr, k0 = (int)(t % KT) * 64 + c * 8;
+  const bool lora = A != nullptr && r > 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + 32 * i;
+    const uint4 raw = *reinterpret_cast<const uint4 *>(src + (long long)n * cols + k0);
+    float delta[8] = {};
+    for (int j = 0; j < (lora ? r : 0); ++j) {
+      const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
+      const bf16 *ap = reinterpret_cast<const bf16 *>(&av);
+      const float bj = __bfloat162float(Bm[(long long)n * r + j]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
+    }
+    const bf16 *wv = reinterpret_cast<const bf16 *>(&raw);
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(__bfloat162float(wv[e]) + scale * delta[e]));
+    // the eight threads of a row (lanes 8 rr' .. 8 rr' + 7 of the warp)
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (c == 0) atomicMax(&amax_bits[n], __float_as_uint(m));
+  }
+}
+
+// amax bits -> the row's fp8 scale max|W| / 448 (1 for an all-zero row), in place.
+__global__ void k_amax_to_scale(float *s, int rows) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= rows) return;
+  const float m = __uint_as_float(reinterpret_cast<const unsigned *>(s)[n]);
+  s[n] = m > 0.f ? m / 448.f : 1.f;
+}
+
+// FP8 weights, pass 2: the merged weight divided by its row scale, rounded to the
+// nearest E4M3 value (ties to even, saturating at 448), into the fp8 tiled layout
+// (out8), and the same codes as exact fp16 values into the 16-bit tiled layout
+// (out16, read by the prefill GEMMs, which apply the scale in their epilogue).  One
+// CTA per 128 x 128 fp8 tile; thread (rr, c) takes 16-byte chunk c of rows rr + 32 i.
+__global__ void __launch_bounds__(256, 4)
+    k_fuse_q8(uint8_t *out8, uint16_t *out16, const float *rscale, const bf16 *src, const bf16 *A,
+              const bf16 *Bm, int rows, int cols, int r, float scale) {
+  const long long t = blockIdx.x;
+  const int KT8 = cols / 128;
+  const int rr = threadIdx.x >> 3, c = threadIdx.x & 7;
+  const int tr = (int)(t / KT8), kt = (int)(t % KT8);
+  const int k0 = kt * 128 + c * 16;
+  const bool lora = A != nullptr && r > 0;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const int n = tr * 128 + rr + 32 * i;
+    const uint4 *sp = reinterpret_cast<const uint4 *>(src + (long long)n * cols + k0);
+    const uint4 raw0 = sp[0], raw1 = sp[1];
+    float v[16];
+    const bf16 *w0 = reinterpret_cast<const bf16 *>(&raw0);
+    const bf16 *w1 = reinterpret_cast<const bf16 *>(&raw1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[e] = __bfloat162float(w0[e]);
+      v[8 + e] = __bfloat162float(w1[e]);
+    }
+    if (lora) {
+      float delta[16] = {};
+      for (int j = 0; j < r; ++j) {
+        const uint4 *ap = reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
+        const uint4 a0 = ap[0], a1 = ap[1];
+        const bf16 *x0 = reinterpret_cast<const bf16 *>(&a0);
+        const bf16 *x1 = reinterpret_cast<const bf16 *>(&a1);
+        const float bj = __bfloat162float(Bm[(long long)n * r + j]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          delta[e] = fmaf(bj, __bfloat162float(x0[e]), delta[e]);
+          delta[8 + e] = fmaf(bj, __bfloat162float(x1[e]), delta[8 + e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = v[e] + scale * delta[e];
+    }
+    const float s = rscale[n];
+    uint32_t q[4];
+    uint4 h16[2];
+    uint32_t *hw = reinterpret_cast<uint32_t *>(h16);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const __nv_fp8x2_storage_t p2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[2 * e] / s, v[2 * e + 1] / s), __NV_SATFINITE,
+                                   __NV_E4M3);
+      if (e % 2 == 0)
+        q[e / 2] = p2;
+      else
+        q[e / 2] |= (uint32_t)p2 << 16;
+      const __half2_raw hp = __nv_cvt_fp8x2_to_halfraw2(p2, __NV_E4M3);
+      hw[e] = (uint32_t)hp.x | ((uint32_t)hp.y << 16);
+    }
+    *reinterpret_cast<uint4 *>(out8 + tiled8_index(n, k0, cols)) = make_uint4(q[0], q[1], q[2], q[3]);
+    // the 16 codes as fp16: two 8-element chunks of the 16-bit tiled layout
+    *reinterpret_cast<uint4 *>(out16 + tiled_index(n, k0, cols)) = h16[0];
+    *reinterpret_cast<uint4 *>(out16 + tiled_index(n, k0 + 8, cols)) = h16[1];
+  }
+}
+
 __global__ void k_tile_act(const uint16_t *x, int M, int K, int ldx, int R, uint16_t *out) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= (long long)R * K) return;
@@ -730,6 +840,24 @@ cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const voi
                                                (const bf16 *)bm, rows, cols, r, scale);
   else
     return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fuse_fp8(void *out8, void *out16, float *rscale, const void *src, const void *a,
+                            const void *bm, int rows, int cols, int r, float scale,
+                            cudaStream_t st) {
+  if (rows % 128 || cols % 128 || !out8 || !out16 || !rscale) return cudaErrorInvalidValue;
+  const long long tiles64 = (long long)(rows / 128) * (cols / 64);
+  if (tiles64 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(rscale, 0, (size_t)rows * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  k_fuse_amax<<<(int)tiles64, 256, 0, st>>>(reinterpret_cast<unsigned *>(rscale),
+                                            (const bf16 *)src, (const bf16 *)a, (const bf16 *)bm,
+                                            rows, cols, r, scale);
+  k_amax_to_scale<<<(rows + 255) / 256, 256, 0, st>>>(rscale, rows);
+  k_fuse_q8<<<(int)(tiles64 / 2), 256, 0, st>>>((uint8_t *)out8, (uint16_t *)out16, rscale,
+                                                (const bf16 *)src, (const bf16 *)a,
+                                                (const bf16 *)bm, rows, cols, r, scale);
   return cudaGetLastError();
 }
 

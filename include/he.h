@@ -182,6 +182,32 @@ he_status he_fuse_lora(he_engine *h, void *stream);
  * dtypes: frees the buffer he_fuse_lora took.  HE_ERR_STATE if not fused. */
 he_status he_unfuse_lora(he_engine *h, void *stream);
 
+/* Weight formats of he_set_weight_format. */
+enum { HE_WEIGHTS_F16 = 0, HE_WEIGHTS_FP8 = 1 };
+
+/* [RLHF-ch11] "The Generation Bottleneck: Quantitative Analysis" (the optimisation
+ * stack: INT8/FP8 weights for generation halve the bandwidth the weights need):
+ * the format generation reads the six projections in, from the next he_fuse_lora
+ * (or the next unfused generation) on.  HE_WEIGHTS_F16 (the default): fp16, as
+ * described at he_fuse_lora.  HE_WEIGHTS_FP8 (BF16 engines): each projection,
+ * after the LoRA merge, is stored as OCP FP8 E4M3 codes with one fp32 scale per
+ * output row, s_n = max_k |W[n][k]| / 448, codes = W / s_n rounded to the nearest
+ * E4M3 value (ties to even, saturated at 448); generation computes with the
+ * weights codes * s_n.  The decode projections stream the one-byte codes (half
+ * the weight bytes), decoded exactly to fp16 on the chip, with fp16 activations
+ * and fp32 accumulation; the prefill GEMMs read the same codes as fp16 values.  The
+ * tied LM head, the KV cache and the activations are unchanged.  The copy takes
+ * 3 bytes per projection weight plus 4 per row (the fp16 copy: 2).  HE_ERR_STATE
+ * while fused; HE_ERR_UNSUPPORTED for FP8 on an F32 engine. */
+he_status he_set_weight_format(he_engine *h, int format);
+
+/* With HE_WEIGHTS_FP8 fused: copies projection `proj` of `layer`'s E4M3 codes (device
+ * `codes`, rows * cols bytes in the fp8 tiled layout of he_ops.h) and its fp32 row
+ * scales (device `scales`, rows floats).  For tests and inspection.  HE_ERR_STATE if
+ * not fused with fp8 weights.  Asynchronous on `stream`. */
+he_status he_read_fused_fp8(he_engine *h, int layer, int proj, void *codes, size_t code_bytes,
+                            float *scales, void *stream);
+
 /* Copies projection `proj` of `layer` as generation reads it while fused into
  * dst (device, `bytes` = rows * cols * element size of the config's dtype): the
  * merged weight in place for F32, the fp16 tiled copy for BF16 (element layout

@@ -73,6 +73,21 @@ he_status he_op_head_greedy(int dtype, const void *x, int ldx, const void *w, in
  * overlap with w) from the row-major w; asynchronous on `stream`. */
 he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream);
 
+/* The fp8 tiled layout (he_set_weight_format HE_WEIGHTS_FP8): for W [N][K] with
+ * N % 128 == 0 and K % 128 == 0, the one-byte code of element (n, k) sits at
+ *   ((n / 128) * (K / 128) + k / 128) * 16384 + (n % 128) * 128
+ *     + (((k % 128) / 16) ^ (n % 8)) * 16 + k % 16,
+ * 128 x 128 tiles of 16 KB, each a single bulk copy of a decode GEMM stage.
+ * y[M][N] (fp32) = (x[M][K] codes^T) * scale[n]: the stream-K decode GEMM on fp8
+ * weights (codes in that layout, fp32 scales per row) and fp16 activations x
+ * (row stride ldx; 1 <= M <= 128, ldx >= K, ldx % 8 == 0, 16-byte aligned).
+ * split < 0 runs on -split CTAs (at most min(units, 15 * tiles)), otherwise one
+ * per SM.  scratch: as he_op_linear's stream-K scratch (16 * M * N floats of
+ * slices, then R * K fp16 of row-tiled x, then N / 128 counters).  Asynchronous
+ * on `stream`. */
+he_status he_op_linear_fp8(const void *x, int ldx, const void *w8, const float *scale, float *y,
+                           int M, int N, int K, int split, float *scratch, void *stream);
+
 /* Single-query attention of one decode step over the KV cache
  * ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of ChatGPT-like
  * Models at All Scales", §3.4 "Inference Mode: Generation Phase Optimizations",

@@ -69,6 +69,9 @@ projections are [out][in] (y = x W^T + b); bf16 tensors are raw uint16 bits.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 TARGETS = ("wq", "wk", "wv", "wo", "w1", "w2")
@@ -134,16 +137,16 @@ def e4m3_round(x: np.ndarray) -> np.ndarray:
     In the binade [2^e, 2^(e+1)), e >= -6, the format has 8 values 2^(e-3) apart;
     below 2^-6 the subnormals continue with spacing 2^-9.  Rounding |x| / spacing to
     the nearest integer, half to even, is the round-to-nearest-even of the format
-    (an even integer is an even mantissa, the implicit bit included)."""
-    x = np.asarray(x, dtype=np.float64)
+    (an even integer is an even mantissa, the implicit bit included).  fp32 in and out:
+    every E4M3 value and every spacing is exact in fp32."""
+    x = np.asarray(x, dtype=np.float32)
     a = np.abs(x)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(e, -6.0)
-    spacing = np.exp2(e - 3.0)
-    q = np.rint(a / spacing) * spacing
-    q = np.minimum(q, E4M3_MAX)
-    return np.where(np.isnan(x), np.nan, np.copysign(q, x))
+    _, e = np.frexp(a)  # a = m 2^e with m in [0.5, 1): the binade is 2^(e - 1)
+    e = np.maximum(e - 1, -6)
+    spacing = np.ldexp(np.float32(1.0), e - 3).astype(np.float32)
+    q = np.rint(a / spacing) * spacing  # exact: spacing is a power of two
+    q = np.minimum(q, np.float32(E4M3_MAX))
+    return np.where(np.isnan(x), np.float32(np.nan), np.copysign(q, x)).astype(np.float32)
 
 
 def quantize_rows_e4m3(w: np.ndarray) -> tuple:
@@ -153,7 +156,13 @@ def quantize_rows_e4m3(w: np.ndarray) -> tuple:
     w = np.asarray(w, dtype=np.float32)
     amax = np.abs(w).max(axis=1)
     s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    q = e4m3_round((w / s[:, None]).astype(np.float32)).astype(np.float32)
+    q = np.empty_like(w)
+
+    def rows(i):  # a block of rows at a time (bounded temporaries, one per thread)
+        q[i:i + 256] = e4m3_round(w[i:i + 256] / s[i:i + 256, None])
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(rows, range(0, w.shape[0], 256)))
     return q, s
 
 

@@ -24,13 +24,14 @@ def engine_for(cfg, inputs, torch, max_batch=None, max_seq=None, **kw):
 
 
 def teacher_forced_check(cfg, torch, seqs=None, steps=None, inputs=None, prompts=None,
-                         oracle_seqs=None, fused=True):
+                         oracle_seqs=None, fused=True, weights="f16"):
     """Runs the GPU path teacher-forced on the oracle's tokens; returns the worst errors.
 
     ``oracle_seqs``: the sequences the oracle computes (batch rows are independent),
     default all; the GPU runs the whole batch.  ``steps``: the decode steps compared
     (default all).  ``fused``: LoRA merged before generating (oracle "merged"), or
-    generation on the base weights without a fuse (oracle "none").
+    generation on the base weights without a fuse (oracle "none").  ``weights``: the
+    engine's weight format, "f16" (oracle weights "exact") or "fp8" (oracle "fp8").
     """
     inputs = inputs if inputs is not None else make_model(cfg)
     prompts = prompts if prompts is not None else make_prompts(cfg)
@@ -38,10 +39,13 @@ def teacher_forced_check(cfg, torch, seqs=None, steps=None, inputs=None, prompts
     oseq = list(range(B)) if oracle_seqs is None else list(oracle_seqs)
     osteps = list(range(cfg.gen_len)) if steps is None else list(steps)
     n_or = max(osteps) + 1
-    oracle = OracleModel(inputs, "merged" if fused else "none")
+    oracle = OracleModel(inputs, "merged" if fused else "none",
+                         weights="fp8" if weights == "fp8" else "exact")
     ref_ids, ref_lps, ref_lg = oracle.generate(prompts[oseq], n_or, log_steps=osteps)
     del oracle
     eng, _w = engine_for(cfg, inputs, torch)
+    if weights != "f16":
+        eng.set_weight_format(weights)
     if fused:
         eng.fuse_lora()
     force = np.full((B, cfg.gen_len), -1, np.int32)

@@ -77,6 +77,10 @@ def test_argument_errors_without_gpu(lib):
     assert lib.he_op_tile_weight(None, None, 128, 64, None) == he.HE_ERR_ARG
     assert lib.he_op_head_greedy(1, None, 64, None, 1, 128, 64, None, None, None,
                                  None) == he.HE_ERR_ARG
+    assert lib.he_op_linear_fp8(None, 128, None, None, None, 1, 128, 128, 0, None,
+                                None) == he.HE_ERR_ARG
+    assert lib.he_set_weight_format(None, 1) == he.HE_ERR_ARG
+    assert lib.he_read_fused_fp8(None, 0, 0, None, 0, None, None) == he.HE_ERR_ARG
     assert b"sm_103a" in lib.he_version()
 
 
