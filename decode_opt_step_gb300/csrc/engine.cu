@@ -271,7 +271,7 @@ int act_rows(const he_engine *h, int B, bool decode) {
 // consumer how to add them.
 // With fp8 weights (w8 and scales per row group, w the same codes as fp16 values):
 // the decode projections stream the fp8 codes through the stream-K kernel when it
-// takes them (at most 128 tokens, K % 128 == 0); every other GEMM reads the fp16
+// takes them (at most 128 tokens, K % 256 == 0); every other GEMM reads the fp16
 // codes and applies the row scales in its epilogue.
 SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, int n_groups,
                int group_rows, int M, int K, Epi epi, bool decode, bool tiled_w, int act,
@@ -295,7 +295,7 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
   float *part = static_cast<float *>(h->partial.p);
   long long stride = (long long)M * a.N;
   Timed t(h, cls, c.st);
-  const bool fp8_sk = w8 && scales && M <= 128 && K % 128 == 0 && act == ACT_F16;
+  const bool fp8_sk = w8 && scales && M <= 128 && K % 256 == 0 && act == ACT_F16;
   if (use_stream_k(h, M, a.N, K, decode, tiled_w) && (!scales || fp8_sk)) {
     if (fp8_sk) {
       a.w_fp8 = 1;
@@ -1447,9 +1447,9 @@ he_status he_op_linear_fp8(const void *x, int ldx, const void *w8, const float *
                            int M, int N, int K, int split, float *scratch, void *stream) {
   g_err.clear();
   if (!x || !w8 || !scale || !y || !scratch) return fail(HE_ERR_ARG, "NULL buffer");
-  if (M < 1 || M > 128 || N < 128 || N % 128 || K < 128 || K % 128 || ldx < K || ldx % 8)
-    return fail(HE_ERR_UNSUPPORTED,
-                "fp8 GEMM needs 1 <= M <= 128, N and K multiples of 128, ldx >= K, ldx %% 8 == 0");
+  if (M < 1 || M > 128 || N < 128 || N % 128 || K < 256 || K % 256 || ldx < K || ldx % 8)
+    return fail(HE_ERR_UNSUPPORTED, "fp8 GEMM needs 1 <= M <= 128, N %% 128 == 0, K %% 256 == 0, "
+                                    "ldx >= K, ldx %% 8 == 0");
   if ((uintptr_t)x % 16 || (uintptr_t)w8 % 16 || (uintptr_t)y % 16 || (uintptr_t)scratch % 16)
     return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

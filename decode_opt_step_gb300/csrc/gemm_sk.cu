@@ -70,20 +70,24 @@ struct SkCfg {
   static constexpr uint32_t TMEM_COLS = pow2_cols(2 * BN);
 };
 
-// FP8 weights (W8): the weights of a stage are one 128 x 128 E4M3 tile (16 KB) that
-// converter warps decode to fp16 (exactly: every E4M3 value is an fp16 value) and
-// store into tensor memory as the MMA's A operand; the stage's activations still come
-// from shared memory.  Weights and activations have rings of their own (S8 and SB
-// stages).  TMEM holds the two accumulators (2 BN columns) and SA decoded A stages
-// of 64 columns each.
-constexpr int W8_BYTES = 128 * 128;  // one fp8 weight stage: 128 rows x 128 k
-template <int BN> struct Sk8Cfg {
-  static constexpr int SB = BN >= 128 ? 3 : BN == 64 ? 4 : BN == 32 ? 5 : 6;  // activation stages
-  static constexpr int S8 = BN >= 128 ? 6 : BN == 64 ? 8 : BN == 32 ? 9 : 10; // weight stages
-  static constexpr int STAGE_B = 2 * BN * BK * 2;
-  static constexpr int SA = (512 - 2 * BN) / 64 < 6 ? (512 - 2 * BN) / 64 : 6;
+// FP8 weights (W8): the weights of a stage are KPS / 2 consecutive 128 x 128 E4M3
+// tiles (16 KB each, one bulk copy) that converter warps decode to fp16 (exactly:
+// every E4M3 value is an fp16 value) and store into tensor memory as the MMA's A
+// operand; the stage's activations still come from shared memory.  Weights and
+// activations have rings of their own (S8 and SB stages).  The SM's copy engine
+// takes a roughly fixed time per bulk request, so a stage spans 256 k (KPS 4): one
+// 32 KB weight request and one activation request per stage.  TMEM holds the two
+// accumulators (2 BN columns) and SA decoded A stages of 32 KPS columns each.
+constexpr int W8_TILE = 128 * 128;  // one fp8 tile: 128 rows x 128 k
+template <int BN, int KPS> struct Sk8Cfg {
+  static constexpr int W8_STAGE = KPS / 2 * W8_TILE;
+  static constexpr int STAGE_B = KPS * BN * BK * 2;
+  static constexpr int SB = BN >= 128 ? 2 : BN == 64 ? 3 : BN == 32 ? 4 : 5;  // activation stages
+  static constexpr int S8 = BN >= 128 ? 3 : BN == 64 ? 4 : 5;                 // weight stages
+  static constexpr int A_COLS = 32 * KPS;
+  static constexpr int SA = (512 - 2 * BN) / A_COLS < 4 ? (512 - 2 * BN) / A_COLS : 4;
   static constexpr uint32_t A_COL0 = 2 * BN;
-  static constexpr int RING = S8 * W8_BYTES + SB * STAGE_B;
+  static constexpr int RING = S8 * W8_STAGE + SB * STAGE_B;
   static constexpr int SMEM = 1024 + RING + 512;
 };
 
@@ -105,8 +109,9 @@ constexpr int EPW = 8;              // epilogue warps
 constexpr int EPT = 32 * EPW;        // epilogue threads
 constexpr int SK_THREADS = EPT + 64; // + producer warp + MMA warp
 constexpr int PRODUCER = EPW, MMA = EPW + 1;
-constexpr int CONV0 = EPW + 2;       // W8: four converter warps (one per TMEM lane quarter)
-constexpr int SK8_THREADS = SK_THREADS + 128;
+constexpr int CONV0 = EPW + 2;       // W8: converter warps, two per TMEM lane quarter
+constexpr int NCONV = 8;             // (a pair of warps per quarter takes alternate stages)
+constexpr int SK8_THREADS = SK_THREADS + 32 * NCONV;
 
 // EPI_ARGMAX for a tile stored directly (one run): the greedy statistics of each
 // token column over the tile's 128 rows (features n >= N left out).  Rounds of 32
@@ -163,8 +168,8 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
               const __grid_constant__ SkArgs a, const __grid_constant__ Epi epi, const uint16_t *x,
               int ldx, int *dev_err) {
   using C = SkCfg<BN, STAGES, KPS>;
-  using C8 = Sk8Cfg<BN>;
-  static_assert(!W8 || (KPS == 2 && BN <= 128), "fp8 weights: 128-k stages, at most 128 tokens");
+  using C8 = Sk8Cfg<BN, KPS>;
+  static_assert(!W8 || ((KPS == 2 || KPS == 4) && BN <= 128), "fp8 weights: 128- or 256-k stages, at most 128 tokens");
   constexpr uint32_t kTmemCols = W8 ? 512u : C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
   // 16-bit weights: [STAGES x (A | B)]; W8: [S8 fp8 weight stages][SB activation stages]
   uint8_t *smA = base;
   uint8_t *smW8 = base;
-  uint8_t *smB = W8 ? base + C8::S8 * W8_BYTES : base + STAGES * C::STAGE_A;
+  uint8_t *smB = W8 ? base + C8::S8 * C8::W8_STAGE : base + STAGES * C::STAGE_A;
   uint64_t *full = reinterpret_cast<uint64_t *>(base + (W8 ? C8::RING : STAGES * C::STAGE_BYTES));
   uint64_t *empty = full + (W8 ? C8::SB : STAGES);
   uint64_t *acc_full = empty + (W8 ? C8::SB : STAGES);  // [2]
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     // own, so the weights may run ahead of the activations.
     const bool wts = lane == 0;
     const int NS = wts ? C8::S8 : C8::SB;
-    const uint32_t bytes = wts ? (uint32_t)W8_BYTES : (uint32_t)C8::STAGE_B;
+    const uint32_t bytes = wts ? (uint32_t)C8::W8_STAGE : (uint32_t)C8::STAGE_B;
     uint64_t *fb = wts ? w8_full : full;
     uint64_t *eb = wts ? w8_empty : empty;
     const uint64_t pol = l2_evict_first_policy();
@@ -251,8 +256,9 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
       if (wts) {
         const int group = a.n_groups > 1 ? t / a.tiles_per_group : 0;
         const int lt = t - group * (a.n_groups > 1 ? a.tiles_per_group : 0);
-        bulk_load_hint(smW8 + s * W8_BYTES, a.w8[group] + ((long long)lt * a.KB + kb) * W8_BYTES,
-                       bytes, &fb[s], pol);
+        bulk_load_hint(smW8 + s * C8::W8_STAGE,
+                       a.w8[group] + ((long long)lt * a.KB + kb) * C8::W8_STAGE, bytes, &fb[s],
+                       pol);
       } else {
         bulk_load(smB + s * C8::STAGE_B, x + (long long)kb * KPS * BN * BK, bytes, &fb[s]);
       }
@@ -264,12 +270,14 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
         set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
   } else if (W8 && warp >= CONV0) {
     // ---------------- fp8 -> fp16 into TMEM (A operand) ----------------
-    // Thread = weight row r (TMEM lane r; warp w reaches lanes 32 (w % 4) ..): its 128
-    // fp8 values are eight 16-byte chunks, chunk j (k = 16 j ..) at slot j ^ (r % 8) of
-    // the row's 128 bytes; decoded pairs go to TMEM columns 8 j .. 8 j + 7 of the stage.
+    // Thread = weight row r (TMEM lane r; warp w reaches lanes 32 (w % 4) ..): in each
+    // fp8 tile of the stage its 128 values are eight 16-byte chunks, chunk j (k = 16 j
+    // ..) at slot j ^ (r % 8) of the row's 128 bytes; decoded pairs go to TMEM columns
+    // 64 tt + 8 j .. + 7 of the stage (tile tt).
     const int quarter = warp & 3, r = quarter * 32 + lane;
+    const int pair = (warp - CONV0) / 4;  // this warp's stages: pair, pair + 2, ...
     const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + C8::A_COL0;
-    for (long long u = u_begin; u < u_end; ++u) {
+    for (long long u = u_begin + pair; u < u_end; u += NCONV / 4) {
       const long long i = u - u_begin;
       const int s8 = (int)(i % C8::S8), sa = (int)(i % C8::SA);
       bool ok = mbar_wait_bounded(&w8_full[s8], (uint32_t)((i / C8::S8) & 1));
@@ -281,29 +289,34 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t row_s = smem_u32(smW8 + s8 * W8_BYTES + r * 128);
-      uint4 ch[8];
+#pragma unroll 1
+      for (int tt = 0; tt < KPS / 2; ++tt) {  // the stage's fp8 tiles, 64 TMEM columns each
+        const uint32_t row_s = smem_u32(smW8 + s8 * C8::W8_STAGE + tt * W8_TILE + r * 128);
+        uint4 ch[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ch[j] = lds_u128(row_s + (uint32_t)((j ^ (r & 7)) * 16));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&w8_empty[s8]);  // the fp8 stage may be refilled
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t w[16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t *q = reinterpret_cast<const uint32_t *>(&ch[2 * g + h]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                (__nv_fp8x2_storage_t)(q[e] & 0xFFFFu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                (__nv_fp8x2_storage_t)(q[e] >> 16), __NV_E4M3);
-            w[8 * h + 2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-            w[8 * h + 2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-          }
+        for (int j = 0; j < 8; ++j) ch[j] = lds_u128(row_s + (uint32_t)((j ^ (r & 7)) * 16));
+        if (tt == KPS / 2 - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&w8_empty[s8]);  // the fp8 stage may be refilled
         }
-        tmem_st16(trow + (uint32_t)(sa * 64 + g * 16), w);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(&ch[2 * g + h]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                  (__nv_fp8x2_storage_t)(q[e] & 0xFFFFu), __NV_E4M3);
+              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                  (__nv_fp8x2_storage_t)(q[e] >> 16), __NV_E4M3);
+              w[8 * h + 2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+              w[8 * h + 2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+            }
+          }
+          tmem_st16(trow + (uint32_t)(sa * C8::A_COLS + tt * 64 + g * 16), w);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
             const uint32_t b0 = smem_u32(smB + sb * C8::STAGE_B + q * C::B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              tc_mma_f16_tmem_a(acc, tmem_base + C8::A_COL0 + (uint32_t)(sa * 64 + (q * 4 + kk) * 8),
+              tc_mma_f16_tmem_a(acc, tmem_base + C8::A_COL0 + (uint32_t)(sa * C8::A_COLS + (q * 4 + kk) * 8),
                                 sdesc_sw128(b0 + kk * UMMA_K * 2), idesc, (j | q | kk) != 0);
           }
           tc_commit(&empty[sb]);
@@ -451,7 +464,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     // a.tile_cnt, tiles of one run are stored directly and the others are left as
     // slices for a second kernel.
     const bool fix = a.tile_cnt != nullptr && epi.kind != EPI_PARTIAL;
-    __shared__ ArgStat am_part[2][4][16];  // EPI_ARGMAX: per column half, lane quarter, column
+    __shared__ ArgStat am_part[W8 ? 1 : 2][4][16];  // EPI_ARGMAX (16-bit weights only)
     constexpr int W = BN >= 32 ? 32 : 16;
     constexpr int kStageAvail = W8 ? C8::RING : STAGES * C::STAGE_BYTES;
     // The bias of this thread's row in the tile of the last segment (the one an
@@ -568,7 +581,7 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
                          int *tile_cnt, int *dev_err, cudaStream_t st) {
   using C = SkCfg<BN, STAGES, KPS>;
   constexpr bool fp16 = !std::is_same<CT, bf16>::value;
-  constexpr int kSmem = W8 ? Sk8Cfg<BN>::SMEM : C::SMEM;
+  constexpr int kSmem = W8 ? Sk8Cfg<BN, KPS>::SMEM : C::SMEM;
   CUtensorMap tw[3], tx;
   memset(tw, 0, sizeof tw);
   SkArgs a{};
@@ -605,7 +618,10 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
 
 }  // namespace
 
-int sk_kps(const GemmArgs &g) { return g.K % 128 == 0 ? 2 : 1; }
+int sk_kps(const GemmArgs &g) {
+  if (g.w_fp8) return 4;  // fp8 weights: 256-k stages (K % 256 == 0)
+  return g.K % 128 == 0 ? 2 : 1;
+}
 
 long long sk_units(const GemmArgs &g) {
   return (long long)((g.N + 127) / 128) * (g.K / (64 * sk_kps(g)));
@@ -685,11 +701,11 @@ cudaError_t launch_gemm_sk(const GemmArgs &g, int P, float *slices, long long sl
   if (g.w_fp8) {
     // fp8 weights (fp8 tiled layout, K % 128 == 0, whole 128-row tiles) with fp16
     // activations, at most 128 tokens
-    if (g.act != ACT_F16 || g.M > 128 || g.K % 128 || (g.group_rows % BM) ||
+    if (g.act != ACT_F16 || g.M > 128 || g.K % 256 || (g.group_rows % BM) ||
         g.epi.kind == EPI_ARGMAX)
       return cudaErrorInvalidValue;
 #define HE_SK8(BN) \
-  return launch_sk_bn<f16, BN, Sk8Cfg<BN>::SB, 2, true>(g, P, slices, slice_stride, tile_cnt, dev_err, st)
+  return launch_sk_bn<f16, BN, Sk8Cfg<BN, 4>::SB, 4, true>(g, P, slices, slice_stride, tile_cnt, dev_err, st)
     if (g.M <= 16) HE_SK8(16);
     if (g.M <= 32) HE_SK8(32);
     if (g.M <= 64) HE_SK8(64);

@@ -80,7 +80,8 @@ he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream
  * 128 x 128 tiles of 16 KB, each a single bulk copy of a decode GEMM stage.
  * y[M][N] (fp32) = (x[M][K] codes^T) * scale[n]: the stream-K decode GEMM on fp8
  * weights (codes in that layout, fp32 scales per row) and fp16 activations x
- * (row stride ldx; 1 <= M <= 128, ldx >= K, ldx % 8 == 0, 16-byte aligned).
+ * (row stride ldx; 1 <= M <= 128, K % 256 == 0, ldx >= K, ldx % 8 == 0,
+ * 16-byte aligned).
  * split < 0 runs on -split CTAs (at most min(units, 15 * tiles)), otherwise one
  * per SM.  scratch: as he_op_linear's stream-K scratch (16 * M * N floats of
  * slices, then R * K fp16 of row-tiled x, then N / 128 counters).  Asynchronous
