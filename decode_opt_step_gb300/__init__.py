@@ -101,6 +101,8 @@ _SIGNATURES = {
     "he_op_linear_fp8": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                  c_int, c_int, c_void_p, c_void_p]),
     "he_set_weight_format": (c_int, [c_void_p, c_int]),
+    "he_op_fuse_tiled": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p, c_int,
+                                 c_int, c_void_p]),
     "he_read_fused_fp8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p,
                                   c_void_p]),
     "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
@@ -423,6 +425,19 @@ def attn_decode_noalloc(q, kc, vc, n_keys: int, split: int = 1, out=None, stream
                                          vc.data_ptr(), ctx.data_ptr(), B, H, hd, T, n_keys,
                                          split, _stream_handle(torch, stream)))
     return ctx
+
+
+def fuse_tiled(w, lora_a=None, lora_b=None, scale: float = 0.0, stream=None):
+    """he_op_fuse_tiled: W + scale * B A as fp16 in the tiled layout (flat), bf16 inputs."""
+    import torch
+    lib = load_library()
+    N, K = w.shape
+    r = 0 if lora_a is None else lora_a.shape[0]
+    out = torch.empty(N * K, dtype=torch.float16, device=w.device)
+    _check(lib.he_op_fuse_tiled(w.data_ptr(), lora_a.data_ptr() if r else None,
+                                lora_b.data_ptr() if r else None, r, float(scale),
+                                out.data_ptr(), N, K, _stream_handle(torch, stream)))
+    return out
 
 
 def tile_weight(w, stream=None):

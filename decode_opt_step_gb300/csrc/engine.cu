@@ -1372,6 +1372,22 @@ he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void
   return HE_OK;
 }
 
+he_status he_op_fuse_tiled(const void *w, const void *lora_a, const void *lora_b, int r, float scale,
+                           void *out, int N, int K, void *stream) {
+  g_err.clear();
+  if (!w || !out || (r > 0 && (!lora_a || !lora_b))) return fail(HE_ERR_ARG, "NULL buffer");
+  if (N < 128 || K < 64 || N % 128 || K % 64)
+    return fail(HE_ERR_UNSUPPORTED, "tiled layout needs N %% 128 == 0 and K %% 64 == 0");
+  if (r < 0 || r > 64) return fail(HE_ERR_ARG, "r %d outside [0, 64]", r);
+  if ((uintptr_t)w % 16 || (uintptr_t)out % 16 || (r > 0 && (uintptr_t)lora_a % 16))
+    return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
+  cudaError_t e = launch_fuse_tiled(out, ACT_F16, w, r > 0 ? lora_a : nullptr,
+                                    r > 0 ? lora_b : nullptr, N, K, r, scale,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "he_op_fuse_tiled");
+  return HE_OK;
+}
+
 he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream) {
   g_err.clear();
   if (!w || !out) return fail(HE_ERR_ARG, "NULL buffer");

@@ -517,8 +517,10 @@ __global__ void __launch_bounds__(256, 4)
     k_fuse_tiled(uint4 *out, const bf16 *src, const bf16 *A, const bf16 *Bm, int rows, int cols,
                  int r, float scale) {
   // One CTA per 128 x 64 tile (1024 chunks).  Thread x takes chunks x + 256 i, i < 4:
-  // rows rr + 32 i of the tile, all with the same column chunk c (the same 16 bytes
-  // of each row of A, cached); the four weight loads are in flight together.
+  // rows rr + 32 i of the tile, all with the same column chunk c; the four weight
+  // loads are in flight together.  The delta of two rows at a time: each 16-byte
+  // chunk of a row of A is widened once for both, and a row's r factors of B are one
+  // 16-byte load (r % 8 == 0).
   const long long t = blockIdx.x;
   const int KT = cols / 64;
   const int rr = threadIdx.x >> 3, slot = threadIdx.x & 7;
@@ -537,23 +539,60 @@ __global__ void __launch_bounds__(256, 4)
       return;
     }
   }
+  auto widen = [](uint32_t u, float &lo, float &hi) {  // two bf16 -> fp32 (exact)
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xFFFF0000u);
+  };
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // one chunk at a time: eight accumulators live
-    float delta[8] = {};
-    const long long brow = (long long)(n0 + 32 * i) * r;
-    for (int j = 0; j < (lora ? r : 0); ++j) {
-      const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)j * cols + k0);
-      const bf16 *ap = reinterpret_cast<const bf16 *>(&av);
-      const float bj = __bfloat162float(Bm[brow + j]);
+  for (int pr = 0; pr < 2; ++pr) {  // rows 2 pr and 2 pr + 1 of this thread
+    float delta[2][8] = {};
+    for (int j0 = 0; j0 < (lora ? r : 0); j0 += 8) {
+      uint4 bu[2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) delta[e] = fmaf(bj, __bfloat162float(ap[e]), delta[e]);
+      for (int i = 0; i < 2; ++i) {
+        const bf16 *bp = Bm + (long long)(n0 + 32 * (2 * pr + i)) * r + j0;
+        if (r % 8 == 0) {
+          bu[i] = *reinterpret_cast<const uint4 *>(bp);
+        } else {
+          uint16_t h[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) h[q] = j0 + q < r ? __bfloat16_as_ushort(bp[q]) : (uint16_t)0;
+          bu[i] = make_uint4(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16,
+                             h[4] | (uint32_t)h[5] << 16, h[6] | (uint32_t)h[7] << 16);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (j0 + q >= r) break;
+        const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)(j0 + q) * cols + k0);
+        float a[8];
+        widen(av.x, a[0], a[1]);
+        widen(av.y, a[2], a[3]);
+        widen(av.z, a[4], a[5]);
+        widen(av.w, a[6], a[7]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t word = q < 2 ? bu[i].x : q < 4 ? bu[i].y : q < 6 ? bu[i].z : bu[i].w;
+          const float b = __uint_as_float(q & 1 ? (word & 0xFFFF0000u) : (word << 16));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) delta[i][e] = fmaf(b, a[e], delta[i][e]);
+        }
+      }
     }
-    const bf16 *wv = reinterpret_cast<const bf16 *>(&raw[i]);
-    uint4 res;
-    OT *rp = reinterpret_cast<OT *>(&res);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(__bfloat162float(wv[e]) + scale * delta[e]);
-    o[256 * i] = res;
+    for (int i = 0; i < 2; ++i) {
+      const uint4 rw = raw[2 * pr + i];
+      float w[8];
+      widen(rw.x, w[0], w[1]);
+      widen(rw.y, w[2], w[3]);
+      widen(rw.z, w[4], w[5]);
+      widen(rw.w, w[6], w[7]);
+      uint4 res;
+      OT *rp = reinterpret_cast<OT *>(&res);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(w[e] + scale * delta[i][e]);
+      o[256 * (2 * pr + i)] = res;
+    }
   }
 }
 

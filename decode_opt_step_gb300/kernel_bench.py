@@ -1,6 +1,7 @@
 """Microbenchmark of single kernels at the OPT-13B decode shapes (B = 128).
 
-    python -m decode_opt_step_gb300.kernel_bench [attn_decode|gemm_sk|all] [--iters N]
+    python -m decode_opt_step_gb300.kernel_bench [attn_decode|gemm_sk|gemm_prefill|fuse|all]
+        [--iters N]
 
 Small, self-contained cases (a few GB on the device) that run one kernel of the
 generation path the way a decode step does, for profiling one kernel at a time:
@@ -9,6 +10,8 @@ generation path the way a decode step does, for profiling one kernel at a time:
   keys (1.0 GB of K and V, above the 126 MB L2);
 * gemm_sk: the fc1 projection, 128 tokens x 5120 -> 20480, tiled weights,
   stream-K over one CTA per SM (210 MB of weights, two copies alternated);
+* fuse: the LoRA merge of the fc1 projection, 20480 x 5120, r = 8, bf16 in and fp16
+  out in the tiled layout (420 MB moved, two weights alternated);
 * gemm_prefill: the fc1 projection of a prefill, 32768 tokens (128 prompts of
   256) x 5120 -> 20480, tiled weights, the persistent tensor-core kernel
   (fp32 output, 3.3 GB in all).
@@ -49,6 +52,17 @@ def attn_decode(iters):
           f"{byts / (ms / 1e3) / 1e9:.0f} GB/s")
 
 
+def fuse(iters):
+    N, K, r = 20480, 5120, 8
+    ws = [torch.randn(N, K, device="cuda").to(torch.bfloat16) * 0.02 for _ in range(2)]
+    a = (torch.randn(r, K, device="cuda") * 0.02).to(torch.bfloat16)
+    b = (torch.randn(N, r, device="cuda") * 0.02).to(torch.bfloat16)
+    ms = _time(lambda i: he.fuse_tiled(ws[i % 2], a, b, 2.0), iters)
+    byts = N * K * 4
+    print(f"fuse (LoRA merge into the fp16 tiled layout) N={N} K={K} r={r}: {ms * 1e3:.1f} "
+          f"us/launch, {byts / (ms / 1e3) / 1e9:.0f} GB/s (bf16 read + fp16 write)")
+
+
 def gemm_sk(iters):
     M, N, K = 128, 20480, 5120
     ws = [torch.randn(N, K, device="cuda").to(torch.bfloat16) for _ in range(2)]
@@ -72,7 +86,7 @@ def gemm_prefill(iters):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", nargs="?", default="all",
-                    choices=["attn_decode", "gemm_sk", "gemm_prefill", "all"])
+                    choices=["attn_decode", "gemm_sk", "gemm_prefill", "fuse", "all"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
@@ -82,6 +96,8 @@ def main():
         gemm_sk(args.iters)
     if args.case in ("gemm_prefill", "all"):
         gemm_prefill(args.iters)
+    if args.case in ("fuse", "all"):
+        fuse(args.iters)
 
 
 if __name__ == "__main__":

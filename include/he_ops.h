@@ -73,6 +73,17 @@ he_status he_op_head_greedy(int dtype, const void *x, int ldx, const void *w, in
  * overlap with w) from the row-major w; asynchronous on `stream`. */
 he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream);
 
+/* One projection of he_fuse_lora on a BF16 engine ("DeepSpeed-Chat 选型指南", §三:
+ * the LoRA weights are fused into the inference model before generation; "DeepSpeed-
+ * Chat: Easy, Fast and Affordable RLHF Training of ChatGPT-like Models at All
+ * Scales", §3.4 "Training Mode: ZeRO and LoRA Optimizations", Optimization 2):
+ * out = W + scale * B A (fp32 arithmetic, one rounding to fp16) in the tiled
+ * streaming layout above (fp16 elements).  w: bf16 [N][K] (N % 128 == 0, K % 64 ==
+ * 0); lora_a: bf16 [r][K], lora_b: bf16 [N][r] (r = 0: no delta, w converted to
+ * fp16).  For tests and profiling.  Asynchronous on `stream`. */
+he_status he_op_fuse_tiled(const void *w, const void *lora_a, const void *lora_b, int r, float scale,
+                           void *out, int N, int K, void *stream);
+
 /* The fp8 tiled layout (he_set_weight_format HE_WEIGHTS_FP8): for W [N][K] with
  * N % 128 == 0 and K % 128 == 0, the one-byte code of element (n, k) sits at
  *   ((n / 128) * (K / 128) + k / 128) * 16384 + (n % 128) * 128

@@ -162,3 +162,22 @@ def test_attn_decode_matches_softmax(cuda_device, dtype, B, H, hd, T, n, split):
     got = ctx.double().cpu().numpy()
     tol = {torch.float32: 1e-5, torch.bfloat16: 1e-2, torch.float16: 2e-3}[dtype]  # output rounding
     np.testing.assert_allclose(got, ref, atol=tol, rtol=tol)
+
+
+def test_fuse_tiled_is_one_rounding_of_the_merge(cuda_device):
+    """he_op_fuse_tiled (one projection of the bf16 fuse): fp16 of W + scale B A, tiled."""
+    N, K, r, scale = 256, 192, 8, 2.0
+    g = torch.Generator().manual_seed(11)
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    a = (torch.randn(r, K, generator=g) * 0.02).to(torch.bfloat16)
+    b = (torch.randn(N, r, generator=g) * 0.02).to(torch.bfloat16)
+    out = he.fuse_tiled(w.cuda(), a.cuda(), b.cuda(), scale)
+    torch.cuda.synchronize()
+    exact = w.double() + scale * (b.double() @ a.double())
+    got = out.double().cpu().numpy()[tiled_positions(N, K)]
+    ex = exact.numpy()
+    assert (np.abs(got - ex) <= np.abs(ex) * 2.0 ** -11 * 1.001 + 2.0 ** -24).all()
+    plain = he.fuse_tiled(w.cuda())  # r = 0: the weight rounded to fp16 (exact above 2^-14)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(plain.double().cpu().numpy()[tiled_positions(N, K)],
+                                  w.to(torch.float16).double().numpy())
