@@ -27,19 +27,20 @@ template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __flo
 template <> __device__ __forceinline__ f16 from_f<f16>(float v) { return __float2half_rn(v); }
 
 // Greedy head statistics of a set of logits: the maximum m, the sum s of exp(l - m)
-// and the lowest index i reaching m.  Merging two sets rescales the sum of the one
-// with the smaller maximum; the merge is symmetric in its arguments (so both lanes
-// of a butterfly get the same bits), and an empty set (m = -inf) is neutral.
+// and the lowest index i reaching m.  Merging two sets rescales both sums to the
+// larger maximum; the merge is symmetric in its arguments (so both lanes of a
+// butterfly get the same bits), and an empty set (m = -inf) is neutral.
 struct ArgStat {
   float m, s;
   int i;
 };
 __device__ __forceinline__ ArgStat argstat_merge(const ArgStat &a, const ArgStat &b) {
-  if (b.m == -INFINITY) return a;
-  if (a.m == -INFINITY) return b;
-  if (a.m > b.m) return {a.m, fmaf(b.s, expf(b.m - a.m), a.s), a.i};
-  if (b.m > a.m) return {b.m, fmaf(a.s, expf(a.m - b.m), b.s), b.i};
-  return {a.m, a.s + b.s, min(a.i, b.i)};
+  // branch-free (the lanes of a warp take the same path); exp through the fast ex2
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return a;
+  const float s = a.s * __expf(a.m - m) + b.s * __expf(b.m - m);
+  const int i = (a.m > b.m || (a.m == b.m && a.i < b.i)) ? a.i : b.i;
+  return {m, s, i};
 }
 __device__ __forceinline__ ArgStat argstat_shfl_xor(const ArgStat &a, int o) {
   return {__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o),
@@ -47,15 +48,11 @@ __device__ __forceinline__ ArgStat argstat_shfl_xor(const ArgStat &a, int o) {
 }
 // One more value v at index i, after the values already in a (ascending indices).
 __device__ __forceinline__ void argstat_add(ArgStat &a, float v, int i) {
-  if (v > a.m) {
-    a.s = a.m == -INFINITY ? 1.f : fmaf(a.s, expf(a.m - v), 1.f);
-    a.m = v;
-    a.i = i;
-  } else {
-    a.s += expf(v - a.m);
-  }
+  const float m = fmaxf(a.m, v);
+  a.s = a.s * __expf(a.m - m) + __expf(v - m);
+  a.i = v > a.m ? i : a.i;
+  a.m = m;
 }
-
 __device__ __forceinline__ void set_dev_error(int *flag, int bit) {
   if (flag) atomicOr(flag, bit);
 }

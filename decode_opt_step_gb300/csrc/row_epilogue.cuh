@@ -443,9 +443,13 @@ __device__ __forceinline__ void tile_owner_epilogue(const Epi &e, const float *t
         if (jj < cn) {
           const int f0 = 64 * hf2;
 #pragma unroll 4
-          for (int f = f0; f < f0 + 64; ++f) {
-            const int n = t * 128 + f;
-            if (n < N) argstat_add(st, lds_f32(os_s + (uint32_t)((jj * 128 + f) * 4)), n);
+          for (int f = f0; f < f0 + 64; f += 4) {
+            const uint4 q4 = lds_u128(os_s + (uint32_t)((jj * 128 + f) * 4));
+            const float q[4] = {__uint_as_float(q4.x), __uint_as_float(q4.y),
+                                __uint_as_float(q4.z), __uint_as_float(q4.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (t * 128 + f + e < N) argstat_add(st, q[e], t * 128 + f + e);
           }
         }
         st = argstat_merge(st, argstat_shfl_xor(st, 1));
