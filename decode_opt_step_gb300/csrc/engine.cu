@@ -303,6 +303,9 @@ SliceInfo gemm(Ctx &c, int cls, const void *x, int ldx, const void *const *w, in
     }
     a.split = 1;
     a.epi = epi;
+    // the projections' element-wise epilogues (QKV, fc1) take the stream-K +
+    // data-parallel split when every run has a whole tile
+    a.sk_hybrid = epi.kind == EPI_QKV || epi.kind == EPI_RELU;
     // element-wise epilogues finish inside the kernel (last run of each tile)
     const bool fix = sk_fixup_ok(a);
     const int P = sk_ctas(a, h->num_sms, fix);

@@ -103,6 +103,12 @@ struct SkArgs {
   float *slices;         // fp32 slices: [slot][M][N], or [slot][tile][M][128] with tile_cnt
   long long slice_stride;
   int *tile_cnt;         // per-tile arrival counters (zero between launches); null: no fix-up
+  // Stream-K + data-parallel split (dp > 0): run c first takes its stream-K share
+  // [c U_sk / P_sk, (c + 1) U_sk / P_sk) of the units of the leftover tiles t_sk0 .. T-1
+  // (none for c >= P_sk), then its dp whole tiles c dp .. c dp + dp - 1.  dp == 0:
+  // plain stream-K over all U units on the P runs.
+  int dp, P_sk, t_sk0;
+  long long U_sk;
 };
 
 constexpr int EPW = 8;              // epilogue warps
@@ -193,7 +199,29 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = gridDim.x, c = blockIdx.x;
-  const long long u_begin = (long long)c * a.U / P, u_end = (long long)(c + 1) * a.U / P;
+  // This run's units in order: v = 0 .. nv-1 -> global unit unit_of(v) (tile * KB + k-block).
+  long long sk_b = 0, sk_n = 0, dp_t0 = 0;
+  int dp_n = 0;
+  if (a.dp == 0) {
+    sk_b = (long long)c * a.U / P;
+    sk_n = (long long)(c + 1) * a.U / P - sk_b;
+  } else {
+    if (c < a.P_sk) {
+      sk_b = (long long)c * a.U_sk / a.P_sk;
+      sk_n = (long long)(c + 1) * a.U_sk / a.P_sk - sk_b;
+    }
+    dp_t0 = (long long)c * a.dp;
+    dp_n = a.dp;
+  }
+  const long long nv = sk_n + (long long)dp_n * a.KB;
+  auto unit_of = [&](long long v) -> long long {
+    return v < sk_n ? (long long)a.t_sk0 * a.KB + sk_b + v : dp_t0 * a.KB + (v - sk_n);
+  };
+  // units of the segment starting at v (k-block kb0 of its tile): to the tile's end, and
+  // the stream-K share never runs into the whole tiles
+  auto seg_len = [&](long long v, int kb0) -> int {
+    return (int)(v < sk_n ? min((long long)(a.KB - kb0), sk_n - v) : (long long)(a.KB - kb0));
+  };
 
   if (warp == PRODUCER && lane == 0) {
     const int nst = W8 ? C8::SB : STAGES;
@@ -242,8 +270,8 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     const uint64_t pol = l2_evict_first_policy();
     if (!wts) pdl_wait();
     long long issued = 0;
-    for (long long u = u_begin; u < u_end; ++u) {
-      const long long i = u - u_begin;
+    for (long long i = 0; i < nv; ++i) {
+      const long long u = unit_of(i);
       const int s = (int)(i % NS);
       if (i >= NS && !mbar_wait_bounded(&eb[s], (uint32_t)((i / NS - 1) & 1))) {
         *(volatile int *)abort_flag = 1;
@@ -277,8 +305,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     const int quarter = warp & 3, r = quarter * 32 + lane;
     const int pair = (warp - CONV0) / 4;  // this warp's stages: pair, pair + 2, ...
     const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + C8::A_COL0;
-    for (long long u = u_begin + pair; u < u_end; u += NCONV / 4) {
-      const long long i = u - u_begin;
+    for (long long i = pair; i < nv; i += NCONV / 4) {
       const int s8 = (int)(i % C8::S8), sa = (int)(i % C8::SA);
       bool ok = mbar_wait_bounded(&w8_full[s8], (uint32_t)((i / C8::S8) & 1));
       if (ok && i >= C8::SA)
@@ -354,16 +381,16 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
       const int t = (int)(u / a.KB), kb = (int)(u - (long long)t * a.KB);
       bulk_load(smB + s * C::STAGE_B, x + (long long)kb * KPS * BN * BK, C::STAGE_B, &full[s]);
     };
-    const long long pre = min((long long)STAGES, u_end - u_begin);
+    const long long pre = min((long long)STAGES, nv);
     for (long long i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-      load_a(u_begin + i, (int)i);
+      load_a(unit_of(i), (int)i);
     }
     pdl_wait();
-    for (long long i = 0; i < pre; ++i) load_b(u_begin + i, (int)i);
+    for (long long i = 0; i < pre; ++i) load_b(unit_of(i), (int)i);
     issued = pre;
-    for (long long u = u_begin + pre; u < u_end; ++u) {
-      const long long i = u - u_begin;
+    for (long long i = pre; i < nv; ++i) {
+      const long long u = unit_of(i);
       const int s = (int)(i % STAGES);
       if (!mbar_wait_bounded(&empty[s], (uint32_t)((i / STAGES - 1) & 1))) {
         *(volatile int *)abort_flag = 1;
@@ -384,9 +411,10 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     constexpr uint32_t idesc = idesc_f16kind<CT>(BN);
     int seg = 0;
     bool ok = true;
-    for (long long u = u_begin; u < u_end && ok;) {
+    for (long long v = 0; v < nv && ok;) {
+      const long long u = unit_of(v);
       const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
-      const int n = (int)min((long long)(a.KB - kb0), u_end - u);
+      const int n = seg_len(v, kb0);
       const int buf = seg & 1;
       if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1))) {
         *(volatile int *)abort_flag = 1;
@@ -398,7 +426,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
       const uint32_t acc = tmem_base + (uint32_t)(buf * BN);
       if constexpr (W8) {
         for (int j = 0; j < n; ++j) {
-          const long long i = u - u_begin + j;
+          const long long i = v + j;
           const int sb = (int)(i % C8::SB), sa = (int)(i % C8::SA);
           if (!mbar_wait_bounded(&full[sb], (uint32_t)((i / C8::SB) & 1)) ||
               !mbar_wait_bounded(&a_full[sa], (uint32_t)((i / C8::SA) & 1)) ||
@@ -421,12 +449,12 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
           tc_commit(&a_empty[sa]);
         }
         tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
-        u += n;
+        v += n;
         ++seg;
         continue;
       }
       for (int j = 0; j < n; ++j) {
-        const long long i = u - u_begin + j;
+        const long long i = v + j;
         const int s = (int)(i % STAGES);
         if (!mbar_wait_bounded(&full[s], (uint32_t)((i / STAGES) & 1)) ||
             *(volatile int *)abort_flag) {
@@ -448,7 +476,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
         tc_commit(&empty[s]);
       }
       tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
-      u += n;
+      v += n;
       ++seg;
     }
   } else if (warp < EPW) {
@@ -472,23 +500,31 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
     // before this one: parameters do not depend on it.
     const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32 quarter.., column half
     float last_bias = 0.f;
-    if (fix && u_end > u_begin) {
-      const int t_last = (int)((u_end - 1) / a.KB);
+    if (fix && nv > 0) {
+      const int t_last = (int)(unit_of(nv - 1) / a.KB);
       last_bias = tile_row_bias(epi, t_last * BM + quarter * 32 + lane, a.N);
     }
     pdl_wait();  // outputs may still be read by the kernel before this one
     int seg = 0;
-    for (long long u = u_begin; u < u_end;) {
+    for (long long v = 0; v < nv;) {
+      const long long u = unit_of(v);
       const int t = (int)(u / a.KB), kb0 = (int)(u - (long long)t * a.KB);
-      const int n = (int)min((long long)(a.KB - kb0), u_end - u);
+      const int n = seg_len(v, kb0);
       const int buf = seg & 1;
       const bool ok = !*(volatile int *)abort_flag &&
                       mbar_wait_bounded(&acc_full[buf], (uint32_t)((seg >> 1) & 1));
       if (!ok) set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
       tc_fence_after();
       const bool live = ok && !*(volatile int *)abort_flag;
-      int cf, S;
-      sk_segments(t, a.KB, P, a.U, &cf, &S);
+      // the runs that share tile t: stream-K tiles among the P (or P_sk) runs, whole
+      // tiles of the data-parallel part by this run alone
+      int cf = c, S = 1;
+      if (v < sk_n) {
+        if (a.dp == 0)
+          sk_segments(t, a.KB, P, a.U, &cf, &S);
+        else
+          sk_segments(t - a.t_sk0, a.KB, a.P_sk, a.U_sk, &cf, &S);
+      }
       const int slot = c - cf;
       const int row = t * BM + quarter * 32 + lane;
       const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
@@ -500,7 +536,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
         if (row < a.N) rs = a.wscale[group][gr];
       }
       // (all conditions below are uniform over the four epilogue warps)
-      const bool staged = fix && slot == 0 && u + n == u_end &&
+      const bool staged = fix && slot == 0 && v + n == nv &&
                           tile_stage_tokens(S, a.M, W, kStageAvail) >= W;
       if (staged) {
         tile_owner_epilogue<CT, W, EPT>(epi, a.slices + (size_t)t * a.M * BM, a.slice_stride,
@@ -564,7 +600,7 @@ __global__ void __launch_bounds__(W8 ? SK8_THREADS : SK_THREADS, 1)
           }
         }
       }
-      u += n;
+      v += n;
       ++seg;
     }
   }
@@ -609,6 +645,21 @@ cudaError_t launch_sk_bn(const GemmArgs &g, int P, float *slices, long long slic
   a.slices = slices;
   a.slice_stride = slice_stride;
   a.tile_cnt = tile_cnt;
+  // With the in-kernel fix-up, at least one whole tile per run and 16-bit weights: each
+  // run first takes its share of the leftover tiles, split stream-K over at most 15 runs
+  // a tile, then its whole tiles, so that no run ends in an owner's fix-up (the owners
+  // of the leftover tiles finish them while the whole tiles stream).
+  const long long T = (g.N + BM - 1) / BM;
+  if (g.sk_hybrid && !W8 && tile_cnt && g.epi.kind != EPI_ARGMAX && T >= P) {
+    a.dp = (int)(T / P);
+    a.t_sk0 = a.dp * P;
+    const long long L = T - a.t_sk0;
+    a.U_sk = L * a.KB;
+    long long psk = P;
+    if (psk > 15 * L) psk = 15 * L;
+    if (psk > a.U_sk) psk = a.U_sk;
+    a.P_sk = (int)psk;
+  }
   cudaError_t ae = ensure_smem_limit<k_gemm_sk<CT, BN, STAGES, KPS, W8>>(kSmem);
   if (ae != cudaSuccess) return ae;
   return launch_k(k_gemm_sk<CT, BN, STAGES, KPS, W8>, dim3(P), dim3(W8 ? SK8_THREADS : SK_THREADS),

@@ -142,6 +142,10 @@ struct GemmArgs {
   // w_scale[] the fp32 scale of every row of each group; output = scale * (codes . x)
   int w_fp8;
   const float *w_scale[3];
+  // stream-K with the in-kernel fix-up and at least one whole tile per run: each run
+  // takes its share of the leftover tiles first and whole tiles after (no run ends in
+  // an owner's fix-up).  Results match plain stream-K up to the order of the fp32 sums.
+  int sk_hybrid;
   Epi epi;
 };
 
