@@ -181,8 +181,17 @@ inline int effective_split(int K, int split) {
 __host__ __device__ inline void sk_segments(int t, int KB, int P, long long U, int *c_first,
                                             int *S) {
   const long long x0 = (long long)t * KB, x1 = x0 + KB - 1;
-  const int cf = (int)(((x0 + 1) * P - 1) / U);
-  const int cl = (int)(((x1 + 1) * P - 1) / U);
+  int cf, cl;
+  if (U * P < (1LL << 32)) {
+    // the same quotients in 32-bit arithmetic ((x + 1) P <= U P fits): a 64-bit
+    // division is a long software routine on the GPU, and row kernels ask per thread
+    const unsigned u = (unsigned)U, p = (unsigned)P;
+    cf = (int)(((unsigned)(x0 + 1) * p - 1u) / u);
+    cl = (int)(((unsigned)(x1 + 1) * p - 1u) / u);
+  } else {
+    cf = (int)(((x0 + 1) * P - 1) / U);
+    cl = (int)(((x1 + 1) * P - 1) / U);
+  }
   *c_first = cf;
   *S = cl - cf + 1;
 }
