@@ -22,6 +22,7 @@ HE_OK, HE_ERR_ARG, HE_ERR_STATE, HE_ERR_OOM = 0, -1, -2, -3
 HE_ERR_CUDA, HE_ERR_UNSUPPORTED, HE_ERR_DEVICE_CHECK = -4, -5, -6
 HE_DTYPE_F32, HE_DTYPE_BF16, HE_DTYPE_F16 = 0, 1, 2
 HE_WEIGHTS_F16, HE_WEIGHTS_FP8 = 0, 1
+HE_ATTN_PREFILL_MMA_SYNC = 1
 HE_PROJ_Q, HE_PROJ_K, HE_PROJ_V, HE_PROJ_O, HE_PROJ_FC1, HE_PROJ_FC2 = range(6)
 PROJ = ("wq", "wk", "wv", "wo", "w1", "w2")
 BIAS = ("bq", "bk", "bv", "bo", "b1", "b2")
@@ -105,6 +106,8 @@ _SIGNATURES = {
                                  c_int, c_void_p]),
     "he_read_fused_fp8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p,
                                   c_void_p]),
+    "he_op_attn_prefill": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                   c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_op_attn_decode": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "he_op_attn_decode_noalloc": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
@@ -410,6 +413,22 @@ def attn_decode(q, kc, vc, n_keys: int, split: int = 1, stream=None):
                                  B, H, hd, T, n_keys, split,
                                  part.data_ptr() if part is not None else None,
                                  _stream_handle(torch, stream)))
+    return ctx
+
+
+def attn_prefill(q, kc, vc, Lp: int, mma_sync: bool = False, dev_flags=None, stream=None):
+    """Prompt attention through he_op_attn_prefill: q [B][Lp][H*hd] (pre-scaled),
+    kc/vc [B][H][T][hd] holding the prompt's keys and values at positions 0..Lp-1;
+    returns ctx [B][Lp][H*hd].  ``mma_sync`` selects the mma.sync kernel."""
+    import torch
+    lib = load_library()
+    B, H, T, hd = kc.shape
+    ctx = torch.empty((B, Lp, H * hd), dtype=q.dtype, device=q.device)
+    _check(lib.he_op_attn_prefill(_dtype_code(torch, q.dtype), q.data_ptr(), kc.data_ptr(),
+                                  vc.data_ptr(), ctx.data_ptr(), B, Lp, H, hd, T,
+                                  HE_ATTN_PREFILL_MMA_SYNC if mma_sync else 0,
+                                  dev_flags.data_ptr() if dev_flags is not None else None,
+                                  _stream_handle(torch, stream)))
     return ctx
 
 

@@ -357,8 +357,12 @@ cudaError_t launch_attn_prefill_mma(int act, const void *q, const void *kc, cons
 
 cudaError_t launch_attn_prefill(int act, const void *q, const void *kc, const void *vc,
                                 void *ctx, int B, int Lp, int H, int hd, int max_seq,
-                                cudaStream_t st) {
-  if (act != ACT_F32)  // 16-bit types: tensor cores (attn_prefill_mma.cu)
+                                int *dev_err, cudaStream_t st, bool legacy_mma) {
+  // 16-bit types: tcgen05 (attn_prefill_tc.cu) for head sizes 64 and 128, else
+  // mma.sync (attn_prefill_mma.cu)
+  if (!legacy_mma && attn_prefill_tc_supported(act, hd))
+    return launch_attn_prefill_tc(act, q, kc, vc, ctx, B, Lp, H, hd, max_seq, dev_err, st);
+  if (act != ACT_F32)
     return launch_attn_prefill_mma(act, q, kc, vc, ctx, B, Lp, H, hd, max_seq, st);
   if (hd == 128) return prefill_t<float, 128>(q, kc, vc, ctx, B, Lp, H, max_seq, st);
   if (hd == 64) return prefill_t<float, 64>(q, kc, vc, ctx, B, Lp, H, max_seq, st);

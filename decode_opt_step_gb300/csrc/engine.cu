@@ -399,7 +399,8 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   if (prefill) {
     Timed t(h, HE_KCLASS_PREFILL_ATTN, c.st);
     c.check(launch_attn_prefill(act, h->q.p, at(h->kc.p, lay), at(h->vc.p, lay), h->ctx.p, B,
-                                tok_per_seq, cf.n_heads, hd, cf.max_seq, c.st),
+                                tok_per_seq, cf.n_heads, hd, cf.max_seq,
+                                static_cast<int *>(h->err.p), c.st),
             1);
   } else {
     const int n_keys = pos0 + 1;
@@ -1372,6 +1373,25 @@ he_status he_op_attn_decode(int dtype, const void *q, const void *kc, const void
   cudaError_t r = launch_attn_decode(dtype, q, kc, vc, ctx, 0, B, H, hd, max_seq, n_keys, split,
                                      part, static_cast<cudaStream_t>(stream));
   if (r != cudaSuccess) return cuda_fail(r, "he_op_attn_decode");
+  return HE_OK;
+}
+
+he_status he_op_attn_prefill(int dtype, const void *q, const void *kc, const void *vc, void *ctx,
+                             int B, int Lp, int H, int hd, int max_seq, int flags, int *dev_flags,
+                             void *stream) {
+  g_err.clear();
+  if (!q || !kc || !vc || !ctx) return fail(HE_ERR_ARG, "NULL buffer");
+  if (dtype != HE_DTYPE_F32 && dtype != HE_DTYPE_BF16 && dtype != HE_DTYPE_F16)
+    return fail(HE_ERR_ARG, "bad dtype");
+  if (B < 1 || H < 1 || Lp < 1 || Lp > max_seq) return fail(HE_ERR_ARG, "bad sizes");
+  if (hd != 32 && hd != 64 && hd != 128) return fail(HE_ERR_UNSUPPORTED, "head_dim %d", hd);
+  if (flags & ~HE_ATTN_PREFILL_MMA_SYNC) return fail(HE_ERR_ARG, "unknown flags 0x%x", flags);
+  if ((uintptr_t)q % 16 || (uintptr_t)kc % 16 || (uintptr_t)vc % 16 || (uintptr_t)ctx % 16)
+    return fail(HE_ERR_ARG, "buffers not 16-byte aligned");
+  cudaError_t r = launch_attn_prefill(dtype, q, kc, vc, ctx, B, Lp, H, hd, max_seq, dev_flags,
+                                      static_cast<cudaStream_t>(stream),
+                                      (flags & HE_ATTN_PREFILL_MMA_SYNC) != 0);
+  if (r != cudaSuccess) return cuda_fail(r, "he_op_attn_prefill");
   return HE_OK;
 }
 

@@ -509,6 +509,24 @@ bool make_tmap_16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, i
                    fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+// 3-D 16-bit map {d0 (innermost), d1, d2} with byte strides stride1 (d1) and stride2
+// (d2), box {box0, box1, 1}, 128-byte swizzle, zero fill out of bounds.
+bool make_tmap_3d_16(CUtensorMap *m, const void *ptr, long long d0, long long d1, long long d2,
+                     long long stride1_bytes, long long stride2_bytes, int box0, int box1,
+                     bool fp16) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)stride1_bytes, (cuuint64_t)stride2_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   // Shape rules of this kernel (checked again by the engine at create time):
   // K rows 16-byte aligned (K % 8), row groups whole tiles, pointers 16-byte aligned.

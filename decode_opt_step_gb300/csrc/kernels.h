@@ -300,9 +300,15 @@ cudaError_t launch_attn_decode(int act, const void *q, const void *kc, const voi
 int attn_decode_pick_split(int B, int H, int n_keys, int num_sms);
 
 // Prefill attention: causal within each prompt of Lp tokens (positions 0..Lp-1).
+// dev_err: error flags (a bounded wait of the tcgen05 kernel ran out), may be null;
+// legacy_mma: use the mma.sync kernel even where the tcgen05 one applies.
 cudaError_t launch_attn_prefill(int act, const void *q, const void *kc, const void *vc,
                                 void *ctx, int B, int Lp, int H, int hd, int max_seq,
-                                cudaStream_t st);
+                                int *dev_err, cudaStream_t st, bool legacy_mma = false);
+bool attn_prefill_tc_supported(int act, int hd);
+cudaError_t launch_attn_prefill_tc(int act, const void *q, const void *kc, const void *vc,
+                                   void *ctx, int B, int Lp, int H, int hd, int max_seq,
+                                   int *dev_err, cudaStream_t st);
 
 // W <- round(W + scale * B A) after saving W's bits to `save`.
 cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, void *save,

@@ -100,6 +100,25 @@ he_status he_op_fuse_tiled(const void *w, const void *lora_a, const void *lora_b
 he_status he_op_linear_fp8(const void *x, int ldx, const void *w8, const float *scale, float *y,
                            int M, int N, int K, int split, float *scratch, void *stream);
 
+/* Causal attention of the prompt pass: every prompt token attends to the prompt's
+ * tokens up to itself ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training
+ * of ChatGPT-like Models at All Scales", §3.4 "Step 3: RLHF Training via PPO",
+ * item 1: the actor first reads the whole 256-token prompt, then generates; the
+ * prompt pass fills the key/value cache of §3.4 "Inference Mode", Optimization 2).
+ * q: [B][Lp][H*hd] (already scaled by hd^-1/2); kc, vc: [B][H][max_seq][hd], the
+ * prompt's keys and values at positions 0..Lp-1 (later positions are not read);
+ * ctx: [B][Lp][H*hd] out.  dtype F32, BF16 or F16; hd in {32, 64, 128}; fp32
+ * softmax and accumulation.  BF16 / F16 with hd 64 or 128 run on the tcgen05
+ * tensor cores (the probabilities rounded to dtype for the P V product), unless
+ * flags has HE_ATTN_PREFILL_MMA_SYNC, which selects the mma.sync kernel (also used
+ * for hd 32).  All four pointers 16-byte aligned, Lp <= max_seq, else HE_ERR_ARG.
+ * dev_flags: device int that receives DEVERR bits (a bounded pipeline wait that
+ * ran out: the output is then not valid), or NULL.  Asynchronous on `stream`. */
+enum { HE_ATTN_PREFILL_MMA_SYNC = 1 };
+he_status he_op_attn_prefill(int dtype, const void *q, const void *kc, const void *vc, void *ctx,
+                             int B, int Lp, int H, int hd, int max_seq, int flags, int *dev_flags,
+                             void *stream);
+
 /* Single-query attention of one decode step over the KV cache
  * ("DeepSpeed-Chat: Easy, Fast and Affordable RLHF Training of ChatGPT-like
  * Models at All Scales", §3.4 "Inference Mode: Generation Phase Optimizations",

@@ -79,6 +79,15 @@ def test_argument_errors_without_gpu(lib):
                                  None) == he.HE_ERR_ARG
     assert lib.he_op_linear_fp8(None, 128, None, None, None, 1, 128, 128, 0, None,
                                 None) == he.HE_ERR_ARG
+    assert lib.he_op_attn_prefill(1, None, None, None, None, 1, 1, 1, 64, 8, 0, None,
+                                  None) == he.HE_ERR_ARG
+    dummy = 4096  # never dereferenced: the size checks fail first
+    assert lib.he_op_attn_prefill(1, dummy, dummy, dummy, dummy, 1, 9, 1, 64, 8, 0, None,
+                                  None) == he.HE_ERR_ARG  # Lp > max_seq
+    assert lib.he_op_attn_prefill(1, dummy, dummy, dummy, dummy, 1, 4, 1, 64, 8, 2, None,
+                                  None) == he.HE_ERR_ARG  # unknown flag
+    assert lib.he_op_attn_prefill(1, dummy, dummy, dummy, dummy, 1, 4, 1, 96, 8, 0, None,
+                                  None) == he.HE_ERR_UNSUPPORTED
     assert lib.he_set_weight_format(None, 1) == he.HE_ERR_ARG
     assert lib.he_read_fused_fp8(None, 0, 0, None, 0, None, None) == he.HE_ERR_ARG
     assert b"sm_103a" in lib.he_version()

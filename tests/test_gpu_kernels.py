@@ -164,6 +164,53 @@ def test_attn_decode_matches_softmax(cuda_device, dtype, B, H, hd, T, n, split):
     np.testing.assert_allclose(got, ref, atol=tol, rtol=tol)
 
 
+@pytest.mark.parametrize("mma_sync", [False, True])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("B,H,hd,Lp,T", [(2, 3, 64, 256, 300), (3, 2, 128, 67, 128),
+                                         (1, 2, 128, 511, 512), (2, 2, 64, 1, 8),
+                                         (1, 3, 128, 129, 160), (2, 1, 64, 384, 384),
+                                         (1, 2, 32, 100, 128)])
+def test_attn_prefill_matches_causal_softmax(cuda_device, dtype, mma_sync, B, H, hd, Lp, T):
+    """he_op_attn_prefill (tcgen05 for hd 64 / 128, mma.sync otherwise or on request)
+    against a float64 causal softmax; cache rows past the prompt hold NaN, which no
+    kernel may read."""
+    g = torch.Generator().manual_seed(B * 1000 + Lp * 7 + hd)
+    q = (torch.randn(B, Lp, H * hd, generator=g) * hd ** -0.5).to(dtype).cuda()
+    kc = torch.full((B, H, T, hd), float("nan"), dtype=dtype)
+    vc = torch.full((B, H, T, hd), float("nan"), dtype=dtype)
+    kc[:, :, :Lp] = torch.randn(B, H, Lp, hd, generator=g).to(dtype)
+    vc[:, :, :Lp] = torch.randn(B, H, Lp, hd, generator=g).to(dtype)
+    kc, vc = kc.cuda(), vc.cuda()
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx = he.attn_prefill(q, kc, vc, Lp, mma_sync=mma_sync, dev_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    qd = q.double().cpu().view(B, Lp, H, hd).transpose(1, 2)
+    kd, vd = kc.double().cpu()[:, :, :Lp], vc.double().cpu()[:, :, :Lp]
+    s = qd @ kd.transpose(-1, -2)
+    s = s.masked_fill(torch.ones(Lp, Lp, dtype=torch.bool).triu(1), float("-inf"))
+    ref = (torch.softmax(s, -1) @ vd).transpose(1, 2).reshape(B, Lp, H * hd).numpy()
+    got = ctx.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    # probabilities rounded to dtype for the P V product, plus the output rounding
+    tol = {torch.bfloat16: 2e-2, torch.float16: 4e-3}[dtype]
+    np.testing.assert_allclose(got, ref, atol=tol, rtol=tol)
+
+
+def test_attn_prefill_tc_equals_reference_rounding_path(cuda_device):
+    """The tcgen05 and mma.sync prompt attentions agree to within the rounding of the
+    probabilities (they differ only in summation order and exp evaluation)."""
+    B, H, hd, Lp, T = 2, 4, 128, 256, 256
+    g = torch.Generator().manual_seed(5)
+    q = (torch.randn(B, Lp, H * hd, generator=g) * hd ** -0.5).half().cuda()
+    kc = torch.randn(B, H, T, hd, generator=g).half().cuda()
+    vc = torch.randn(B, H, T, hd, generator=g).half().cuda()
+    a = he.attn_prefill(q, kc, vc, Lp).float()
+    b = he.attn_prefill(q, kc, vc, Lp, mma_sync=True).float()
+    torch.cuda.synchronize()
+    assert (a - b).abs().max().item() < 4e-3
+
+
 def test_fuse_tiled_is_one_rounding_of_the_merge(cuda_device):
     """he_op_fuse_tiled (one projection of the bf16 fuse): fp16 of W + scale B A, tiled."""
     N, K, r, scale = 256, 192, 8, 2.0
