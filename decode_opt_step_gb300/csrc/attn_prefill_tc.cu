@@ -78,6 +78,14 @@ __host__ __device__ constexpr uint32_t idesc_attn(int n, bool b_mn) {
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(QB >> 4) << 24);
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x by the SFU's approximate base-2 exponential (ex2.approx; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (std::is_same<T, bf16>::value) {
@@ -228,28 +236,37 @@ __global__ void __launch_bounds__(128, 1)
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
     }
     const int last = kb == qb ? rr : KBLK - 1;  // keys past the query are masked
-    float mx = m;
+    // maximum and sum over eight independent partials (short dependency chains)
+    float ma[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ma[i] = m;
 #pragma unroll
     for (int c = 0; c < KBLK; ++c) {
       if (c > last) s[c] = -INFINITY;
-      mx = fmaxf(mx, s[c]);
+      ma[c & 7] = fmaxf(ma[c & 7], s[c]);
     }
+    const float mx = fmaxf(fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])),
+                           fmaxf(fmaxf(ma[4], ma[5]), fmaxf(ma[6], ma[7])));
     // key kb*128 precedes every query of the block, so mx is finite
-    const float corr = __expf(m - mx);
+    const float corr = ex2_approx((m - mx) * kLog2e);
     m = mx;
-    float rs = 0.f;
+    const float mxl = mx * kLog2e;
+    float ra[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ra[i] = 0.f;
 #pragma unroll
     for (int c = 0; c < KBLK / 32; ++c) {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = __expf(s[c * 32 + 2 * i] - mx), p1 = __expf(s[c * 32 + 2 * i + 1] - mx);
-        rs += p0 + p1;
+        const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], kLog2e, -mxl));
+        const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], kLog2e, -mxl));
+        ra[i & 7] += p0 + p1;
         pk[i] = pack2<T>(p0, p1);
       }
       tmem_st16(tS + lrow + (uint32_t)(c * 16), pk);  // over S columns already read
     }
-    l = l * corr + rs;
+    l = l * corr + (((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7])));
     if (kb > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
       // the previous P V is complete (S(kb) was issued after it), so O is stable
 #pragma unroll

@@ -510,6 +510,26 @@ __global__ void k_lora_fuse(T *w, const T *A, const T *Bm, T *save, int rows, in
   for (int e = 0; e < 8; ++e) wp[e] = from_f<T>(to_f<T>(wv[e]) + scale * delta[e]);
 }
 
+// Packed fp32 pairs (low word = first element) and the paired fused multiply-add
+// (fma.rn.f32x2: two independent round-to-nearest fmaf in one instruction).
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack_f2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// two bf16 (a 32-bit word) -> the packed fp32 pair (exact)
+__device__ __forceinline__ uint64_t widen2(uint32_t u) {
+  return pack_f2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
 // The tiled output in 16-byte chunks: chunk q of tile t holds row r = (q % 1024) / 8,
 // logical 16-byte column chunk (q % 8) ^ (r % 8).
 template <typename OT>
@@ -545,7 +565,9 @@ __global__ void __launch_bounds__(256, 4)
   };
 #pragma unroll
   for (int pr = 0; pr < 2; ++pr) {  // rows 2 pr and 2 pr + 1 of this thread
-    float delta[2][8] = {};
+    // delta[i][e] and delta[i][e + 1] as one packed pair: each fma.rn.f32x2 is two
+    // independent fmaf, so the sums are those of the scalar loop, bit for bit
+    uint64_t delta[2][4] = {};
     for (int j0 = 0; j0 < (lora ? r : 0); j0 += 8) {
       uint4 bu[2];
 #pragma unroll
@@ -565,17 +587,14 @@ __global__ void __launch_bounds__(256, 4)
       for (int q = 0; q < 8; ++q) {
         if (j0 + q >= r) break;
         const uint4 av = *reinterpret_cast<const uint4 *>(A + (long long)(j0 + q) * cols + k0);
-        float a[8];
-        widen(av.x, a[0], a[1]);
-        widen(av.y, a[2], a[3]);
-        widen(av.z, a[4], a[5]);
-        widen(av.w, a[6], a[7]);
+        const uint64_t a2[4] = {widen2(av.x), widen2(av.y), widen2(av.z), widen2(av.w)};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const uint32_t word = q < 2 ? bu[i].x : q < 4 ? bu[i].y : q < 6 ? bu[i].z : bu[i].w;
           const float b = __uint_as_float(q & 1 ? (word & 0xFFFF0000u) : (word << 16));
+          const uint64_t b2 = pack_f2(b, b);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) delta[i][e] = fmaf(b, a[e], delta[i][e]);
+          for (int e = 0; e < 4; ++e) delta[i][e] = fma_f32x2(b2, a2[e], delta[i][e]);
         }
       }
     }
@@ -590,7 +609,12 @@ __global__ void __launch_bounds__(256, 4)
       uint4 res;
       OT *rp = reinterpret_cast<OT *>(&res);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) rp[e] = from_f<OT>(w[e] + scale * delta[i][e]);
+      for (int e = 0; e < 4; ++e) {
+        float d0, d1;
+        unpack_f2(delta[i][e], d0, d1);
+        rp[2 * e] = from_f<OT>(w[2 * e] + scale * d0);
+        rp[2 * e + 1] = from_f<OT>(w[2 * e + 1] + scale * d1);
+      }
       o[256 * (2 * pr + i)] = res;
     }
   }

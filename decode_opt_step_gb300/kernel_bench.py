@@ -1,7 +1,7 @@
 """Microbenchmark of single kernels at the OPT-13B decode shapes (B = 128).
 
-    python -m decode_opt_step_gb300.kernel_bench [attn_decode|gemm_sk|gemm_prefill|fuse|all]
-        [--iters N]
+    python -m decode_opt_step_gb300.kernel_bench
+        [attn_decode|gemm_sk|gemm_prefill|fuse|attn_prefill|all] [--iters N] [--batch B]
 
 Small, self-contained cases (a few GB on the device) that run one kernel of the
 generation path the way a decode step does, for profiling one kernel at a time:
@@ -12,6 +12,9 @@ generation path the way a decode step does, for profiling one kernel at a time:
   stream-K over one CTA per SM (210 MB of weights, two copies alternated);
 * fuse: the LoRA merge of the fc1 projection, 20480 x 5120, r = 8, bf16 in and fp16
   out in the tiled layout (420 MB moved, two weights alternated);
+* attn_prefill: the causal prompt attention of one layer, B=128 (--batch) prompts
+  of 256 tokens, 40 heads of 128, fp16, tcgen05 and mma.sync kernels (1.34 GB of
+  q, K, V and ctx at B=128);
 * gemm_prefill: the fc1 projection of a prefill, 32768 tokens (128 prompts of
   256) x 5120 -> 20480, tiled weights, the persistent tensor-core kernel
   (fp32 output, 3.3 GB in all).
@@ -83,11 +86,26 @@ def gemm_prefill(iters):
           f"{2 * M * N * K / (ms / 1e3) / 1e12:.0f} TFLOP/s")
 
 
+def attn_prefill(iters, B=128):
+    H, hd, Lp, T = 40, 128, 256, 512
+    q = (torch.randn(B, Lp, H * hd, device="cuda") * hd ** -0.5).half()
+    kc = torch.randn(B, H, T, hd, device="cuda").half()
+    vc = torch.randn(B, H, T, hd, device="cuda").half()
+    byts = 4 * B * Lp * H * hd * 2  # q, k, v read once, ctx written
+    flops = 4 * B * H * hd * Lp * (Lp + 1) // 2
+    for name, mma in (("tcgen05", False), ("mma.sync", True)):
+        ms = _time(lambda i: he.attn_prefill(q, kc, vc, Lp, mma_sync=mma), iters)
+        print(f"attn_prefill[{name}] B={B} H={H} hd={hd} Lp={Lp}: {ms * 1e3:.1f} us/launch, "
+              f"{byts / (ms / 1e3) / 1e9:.0f} GB/s, {flops / (ms / 1e3) / 1e12:.0f} TFLOP/s")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", nargs="?", default="all",
-                    choices=["attn_decode", "gemm_sk", "gemm_prefill", "fuse", "all"])
+                    choices=["attn_decode", "gemm_sk", "gemm_prefill", "fuse", "attn_prefill",
+                             "all"])
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=128, help="attn_prefill: prompts")
     args = ap.parse_args()
     torch.cuda.set_device(0)
     if args.case in ("attn_decode", "all"):
@@ -98,6 +116,8 @@ def main():
         gemm_prefill(args.iters)
     if args.case in ("fuse", "all"):
         fuse(args.iters)
+    if args.case in ("attn_prefill", "all"):
+        attn_prefill(args.iters, args.batch)
 
 
 if __name__ == "__main__":
