@@ -64,3 +64,39 @@ def test_opt125m_graph_replay_and_score(cuda_device):
     answers = ids.cpu().numpy()[:2]
     _, lps_o, _ = oracle.generate(prompts_np[:2], L, force_ids=answers)
     assert np.abs(sc.cpu().numpy()[:2] - lps_o).max() < BF16_LP_TOL
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["opt-1.3b", "opt-13b"])
+def test_large_models_score_sampled_sequences(cuda_device, name):
+    """he_score at the full batch and length (256 prompt + 256 answer tokens per
+    sequence, one prefill-kernel pass), against the oracle's log-probs of its own
+    greedy answer tokens 1..8 for sequences 0 and 1; the other answer tokens are random
+    ids (each score row depends only on the tokens before it)."""
+    import numpy as np
+
+    from oracle import OracleModel
+    from synth.workloads import make_model, make_prompts
+    from tests.gpu_helpers import engine_for
+
+    cfg = WORKLOADS[name]
+    inputs = make_model(cfg)
+    prompts = make_prompts(cfg)
+    B, Lp = prompts.shape
+    K = 8
+    oracle = OracleModel(inputs, "merged")
+    ref_ids, ref_lps, _ = oracle.generate(prompts[:2], K)
+    del oracle
+    answers = np.random.default_rng(7).integers(3, cfg.vocab, size=(B, cfg.gen_len))
+    answers = answers.astype(np.int32)
+    answers[:2, :K] = ref_ids
+    full = np.ascontiguousarray(np.concatenate([prompts, answers], axis=1))
+    eng, _w = engine_for(cfg, inputs, torch)
+    eng.fuse_lora()
+    sc = eng.score(torch.from_numpy(full).cuda(), Lp)
+    eng.unfuse_lora()
+    eng.check()
+    torch.cuda.synchronize()
+    err = np.abs(sc.cpu().numpy()[:2, :K] - ref_lps).max()
+    assert err < BF16_LP_TOL, (name, err)
+    eng.close()
