@@ -630,7 +630,8 @@ cudaError_t convert_proj(he_engine *h, int l, int p, bool lora, cudaStream_t st)
                            const_cast<float *>(h->fused_scale[i]), lw.w[p], a, b, proj_rows(c, p),
                            proj_cols(c, p), c.lora_r, scale, st);
   return launch_fuse_tiled(const_cast<void *>(h->fused_w[i]), ACT_F16, lw.w[p], a, b,
-                           proj_rows(c, p), proj_cols(c, p), c.lora_r, scale, st);
+                           proj_rows(c, p), proj_cols(c, p), c.lora_r, scale, st,
+                           static_cast<int *>(h->err.p));
 }
 
 // BF16 engines always generate in fp16 from tiled projections.  While LoRA is fused

@@ -509,6 +509,26 @@ bool make_tmap_16(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, i
                    fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+// 2-D 16-bit map over [rows][cols] (row stride ld elements), box {box_cols, box_rows},
+// swizzle of `swizzle_bytes` (0, 32 or 128; the box's inner extent in bytes must not
+// exceed it), zero fill out of bounds.
+bool make_tmap_2d_16sw(CUtensorMap *m, const void *ptr, int rows, int cols, int ld, int box_cols,
+                       int box_rows, int swizzle_bytes, bool fp16) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D 16-bit map {d0 (innermost), d1, d2} with byte strides stride1 (d1) and stride2
 // (d2), box {box0, box1, 1}, 128-byte swizzle, zero fill out of bounds.
 bool make_tmap_3d_16(CUtensorMap *m, const void *ptr, long long d0, long long d1, long long d2,

@@ -315,10 +315,17 @@ cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, 
                              int rows, int cols, int r, float scale, cudaStream_t st);
 // out (tiled layout, type out_act: ACT_BF16 or ACT_F16) <- round(src + scale * B A),
 // src, A, B bf16, src row-major [rows][cols]; A / B may be null (then a plain
-// re-tiling, bit-exact for ACT_BF16).  out and src must not overlap.
+// re-tiling, bit-exact for ACT_BF16).  out and src must not overlap.  For ACT_F16 with
+// r = 8 or 16 (16-byte aligned factors) the delta runs on the tensor cores
+// (k_fuse_tc), otherwise on the SIMT pipes (k_fuse_tiled).  dev_err (may be null)
+// receives DEVERR_WAIT_TIMEOUT if a bounded wait of the tensor-core kernel ran out.
 cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const void *a,
                               const void *bm, int rows, int cols, int r, float scale,
-                              cudaStream_t st);
+                              cudaStream_t st, int *dev_err = nullptr);
+bool fuse_tc_supported(int r, const void *a, const void *bm);
+cudaError_t launch_fuse_tc(void *out, const void *src, const void *a, const void *bm, int rows,
+                           int cols, int r, float scale, int num_sms, int *dev_err,
+                           cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 // FP8 weights of a projection W [rows][cols] (bf16, rows and cols multiples of 128):
 // the merged weight W + scale B A (A / B may be null) gets the row scales

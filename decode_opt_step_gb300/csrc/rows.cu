@@ -890,11 +890,18 @@ cudaError_t launch_lora_fuse(int dtype, void *w, const void *a, const void *bm, 
 
 cudaError_t launch_fuse_tiled(void *out, int out_act, const void *src, const void *a,
                               const void *bm, int rows, int cols, int r, float scale,
-                              cudaStream_t st) {
+                              cudaStream_t st, int *dev_err) {
   if (rows % 128 || cols % 64) return cudaErrorInvalidValue;
   const long long tiles = (long long)(rows / 128) * (cols / 64);
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int blocks = (int)tiles;
+  if (out_act == ACT_F16 && fuse_tc_supported(r, a, bm)) {  // the delta on the tensor cores
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    return launch_fuse_tc(out, src, a, bm, rows, cols, r, scale, sms, dev_err, st);
+  }
   if (out_act == ACT_F16)
     k_fuse_tiled<f16><<<blocks, 256, 0, st>>>((uint4 *)out, (const bf16 *)src, (const bf16 *)a,
                                               (const bf16 *)bm, rows, cols, r, scale);

@@ -211,10 +211,13 @@ def test_attn_prefill_tc_equals_reference_rounding_path(cuda_device):
     assert (a - b).abs().max().item() < 4e-3
 
 
-def test_fuse_tiled_is_one_rounding_of_the_merge(cuda_device):
-    """he_op_fuse_tiled (one projection of the bf16 fuse): fp16 of W + scale B A, tiled."""
-    N, K, r, scale = 256, 192, 8, 2.0
-    g = torch.Generator().manual_seed(11)
+@pytest.mark.parametrize("N,K,r", [(256, 192, 8), (384, 640, 16), (128, 64, 8), (256, 320, 4),
+                                   (256, 192, 24), (1280, 512, 8)])
+def test_fuse_tiled_is_one_rounding_of_the_merge(cuda_device, N, K, r):
+    """he_op_fuse_tiled (one projection of the bf16 fuse): fp16 of W + scale B A, tiled;
+    r = 8 and 16 take the tensor-core kernel, other ranks the SIMT one."""
+    scale = 2.0
+    g = torch.Generator().manual_seed(11 + N + K + r)
     w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
     a = (torch.randn(r, K, generator=g) * 0.02).to(torch.bfloat16)
     b = (torch.randn(N, r, generator=g) * 0.02).to(torch.bfloat16)
