@@ -83,6 +83,10 @@ WORKLOADS = {
     "opt-1.3b": OptConfig("opt-1.3b", 2, 24, 2048, 32, 8192, 50272, 2048, "bf16", 32, 256, 256),
     "opt-6.7b": OptConfig("opt-6.7b", 3, 32, 4096, 32, 16384, 50272, 2048, "bf16", 64, 256, 256),
     "opt-13b": OptConfig("opt-13b", 4, 40, 5120, 40, 20480, 50272, 2048, "bf16", 128, 256, 256),
+    # the OPT-13B layer and batch shapes in two layers and eight answer tokens: a few GB
+    # on the device, for profiling single launches of the full-size kernels
+    "opt-13b-2layer": OptConfig("opt-13b-2layer", 6, 2, 5120, 40, 20480, 50272, 2048, "bf16",
+                                128, 256, 8),
     # tiny fp32 variant whose biases and LayerNorm affine parameters are not trivial
     "opt-tiny-fp32-bias": OptConfig("opt-tiny-fp32-bias", 5, 2, 128, 4, 512, 1024, 64, "f32",
                                     2, 16, 16, bias_std=0.02, ln_gamma_std=0.1,
