@@ -440,9 +440,10 @@ def main():
     # DRAM bytes (read + write) per launch, scaled from one ncu capture of the kernel
     # (summaries under profiles/) by the ratio of measured to algorithmic bytes of the
     # captured launch: k_attn_decode at B=128, 40 heads, 384 keys (the average decode
-    # launch here) and k_gemm_sk on the fc1 shape.  Set to None when the kernel changes.
+    # launch here) and k_gemm_sk on the fc1 shape as the engine launches it (a decode
+    # step of the two-layer OPT-13B-shape workload).  Set to None when the kernel changes.
     traffic_ratio = {"attn_decode": (1.007987e9 + 4.402432e6) / 1.00663296e9,
-                     "gemm": (211.110656e6 + 6.247168e6) / 209.7152e6}
+                     "gemm": (211.179264e6 + 6.607872e6) / 209.7152e6}
     if args.weights != "f16":
         traffic_ratio.pop("gemm")  # captured on the 16-bit kernel only
     traffic = (pk["bytes_per_launch"] * traffic_ratio[dom]
