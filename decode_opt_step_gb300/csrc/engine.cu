@@ -424,7 +424,7 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
     Timed t(h, HE_KCLASS_NORM, c.st);
     c.check(launch_resid_ln(cf.dtype, act, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                             lw.b[HE_PROJ_O], static_cast<float *>(h->x.p), lw.ln2_g, lw.ln2_b,
-                            cf.ln_eps, h->h.p, R, M, d, c.st),
+                            cf.ln_eps, h->h.p, R, M, d, c.st, static_cast<int *>(h->err.p)),
             1);
   }
   // fc1 + b1 + ReLU
@@ -451,7 +451,7 @@ void layer_forward(Ctx &c, int l, int B, int M, int tok_per_seq, int pos0, bool 
   Timed t(h, HE_KCLASS_NORM, c.st);
   c.check(launch_resid_ln(cf.dtype, out_act, static_cast<float *>(h->partial.p), si, (long long)M * d, d,
                           lw.b[HE_PROJ_FC2], static_cast<float *>(h->x.p), g, bb, cf.ln_eps,
-                          h->h.p, R, M, d, c.st),
+                          h->h.p, R, M, d, c.st, static_cast<int *>(h->err.p)),
           1);
 }
 

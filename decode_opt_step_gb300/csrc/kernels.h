@@ -247,10 +247,12 @@ cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const
 
 // x[row] += sum_s partial[s][row] + bias; h[row] = LN(x[row]; g, b) (storage type,
 // row-tiled with h_rows rows when h_rows > 0).
+// dev_err (may be null): DEVERR_WAIT_TIMEOUT from the bounded waits of the streaming
+// many-rows variant (one slice of 16-bit-model output, d a multiple of 1024).
 cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
                             const void *g, const void *b, float eps, void *h, int h_rows,
-                            int rows, int d, cudaStream_t st);
+                            int rows, int d, cudaStream_t st, int *dev_err = nullptr);
 // out (row-tiled, R rows) <- x rows 0..M-1 (row stride ldx), rows M..R-1 zero.
 // 16-bit elements (bf16 or fp16 bits).
 cudaError_t launch_tile_act(const void *x, int M, int K, int ldx, int R, void *out,

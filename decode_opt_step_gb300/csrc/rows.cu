@@ -530,6 +530,112 @@ __device__ __forceinline__ uint64_t widen2(uint32_t u) {
   return pack_f2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 
+// k_resid_ln_rows for one slice of projection output (the prefill GEMMs), as a
+// persistent pipeline: each CTA walks rows blockIdx.x, + gridDim.x, ..., and one thread
+// keeps the next rows' projection output and residual (d fp32 each) coming into a ring
+// of RS_STAGES stages by bulk copies while the CTA works on the current row, so the HBM
+// stream does not stop between rows.  Thread t owns the same 8-element groups
+// (8t + 1024 j) and does the same arithmetic in the same order as k_resid_ln_rows, so the
+// results are bit-identical.  Every wait is bounded (DEVERR_WAIT_TIMEOUT on a timeout).
+constexpr int RS_STAGES = 2;
+
+template <typename PT, typename OT, int NG>
+__global__ void __launch_bounds__(128)
+    k_resid_ln_stream(const float *partial, int ldp, const PT *bias, float *x, const PT *g,
+                      const PT *b, float eps, OT *h, int h_rows, int rows, int d, int *dev_err) {
+  __shared__ float red[33];
+  __shared__ uint64_t full[RS_STAGES];
+  extern __shared__ __align__(16) float ring[];  // RS_STAGES x (projection row, residual row)
+  const long long first = blockIdx.x, step = gridDim.x;
+  const long long n_mine = first < rows ? (rows - first + step - 1) / step : 0;
+  const uint32_t row_bytes = (uint32_t)d * 4u;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < RS_STAGES; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the projection output and the residual come from the kernels before
+  pdl_trigger();
+  auto issue = [&](long long i) {
+    const int st = (int)(i % RS_STAGES);
+    const long long r = first + i * step;
+    float *dst = ring + (size_t)st * 2 * d;
+    mbar_arrive_expect_tx(&full[st], 2 * row_bytes);
+    bulk_load(dst, partial + r * ldp, row_bytes, &full[st]);
+    bulk_load(dst + d, x + r * d, row_bytes, &full[st]);
+  };
+  if (threadIdx.x == 0)
+    for (long long i = 0; i < n_mine && i < RS_STAGES; ++i) issue(i);
+  long long done = 0;
+  for (long long i = 0; i < n_mine; ++i) {
+    const int st = (int)(i % RS_STAGES);
+    const long long r = first + i * step;
+    if (!mbar_wait_bounded(&full[st], (uint32_t)((i / RS_STAGES) & 1))) {
+      set_dev_error(dev_err, DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    done = i + 1;
+    const float *ps = ring + (size_t)st * 2 * d, *xs = ps + d;
+    float v[NG][8];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      const int c = 8 * threadIdx.x + 1024 * j;
+      float bs[8];
+      load8<PT>(bias + c, bs);
+      const float4 p0 = *reinterpret_cast<const float4 *>(ps + c);
+      const float4 p1 = *reinterpret_cast<const float4 *>(ps + c + 4);
+      float4 x0 = *reinterpret_cast<const float4 *>(xs + c);
+      float4 x1 = *reinterpret_cast<const float4 *>(xs + c + 4);
+      // the one slice added to zero, as the slice sum does
+      x0.x += (0.f + p0.x) + bs[0];
+      x0.y += (0.f + p0.y) + bs[1];
+      x0.z += (0.f + p0.z) + bs[2];
+      x0.w += (0.f + p0.w) + bs[3];
+      x1.x += (0.f + p1.x) + bs[4];
+      x1.y += (0.f + p1.y) + bs[5];
+      x1.z += (0.f + p1.z) + bs[6];
+      x1.w += (0.f + p1.w) + bs[7];
+      float4 *xr = reinterpret_cast<float4 *>(x + r * d + c);
+      xr[0] = x0;
+      xr[1] = x1;
+      v[j][0] = x0.x; v[j][1] = x0.y; v[j][2] = x0.z; v[j][3] = x0.w;
+      v[j][4] = x1.x; v[j][5] = x1.y; v[j][6] = x1.z; v[j][7] = x1.w;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += v[j][e];
+    }
+    // every thread has read this stage: refill it with the row after next
+    const float mean = block_sum(sum, red) / (float)d;
+    if (threadIdx.x == 0 && i + RS_STAGES < n_mine) issue(i + RS_STAGES);
+    float q = 0.f;
+#pragma unroll
+    for (int j = 0; j < NG; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[j][e] -= mean;
+        q += v[j][e] * v[j][e];
+      }
+    const float var = block_sum(q, red) / (float)d;
+    const float rstd = 1.0f / sqrtf(var + eps);
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      const int c = 8 * threadIdx.x + 1024 * j;
+      float gs[8], bt[8];
+      load8<PT>(g + c, gs);
+      load8<PT>(b + c, bt);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[j][e] = v[j][e] * rstd * gs[e] + bt[e];
+      store8<OT>(h + act_index((int)r, c, d, h_rows), v[j]);
+    }
+  }
+  // nothing may still be landing when the CTA exits (only after a timeout)
+  if (threadIdx.x == 0) {
+    const long long issued = n_mine < done + RS_STAGES ? n_mine : done + RS_STAGES;
+    for (long long i = done; i < issued; ++i)
+      if (!mbar_wait_bounded(&full[i % RS_STAGES], (uint32_t)((i / RS_STAGES) & 1))) break;
+  }
+}
+
 // The tiled output in 16-byte chunks: chunk q of tile t holds row r = (q % 1024) / 8,
 // logical 16-byte column chunk (q % 8) ^ (r % 8).
 template <typename OT>
@@ -808,10 +914,44 @@ cudaError_t launch_sk_reduce_epi(int dtype, int act, const float *partial, const
   return cudaSuccess;
 }
 
+template <typename PT, typename OT, int NG>
+cudaError_t launch_resid_stream_n(const float *partial, int ldp, const PT *bias, float *x,
+                                  const PT *g, const PT *b, float eps, OT *h, int h_rows, int rows,
+                                  int d, int *dev_err, cudaStream_t st) {
+  const int smem = RS_STAGES * 2 * d * 4;
+  cudaError_t e = ensure_smem_limit<k_resid_ln_stream<PT, OT, NG>>(RS_STAGES * 2 * 8192 * 4);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // as many CTAs as fit the SMs by shared memory (two at d = 5120)
+  const int per_sm = std::max(1, std::min(8, (227 * 1024) / (smem + 1024)));
+  const int grid = (int)std::min<long long>(rows, (long long)per_sm * sms);
+  return launch_k(k_resid_ln_stream<PT, OT, NG>, dim3(grid), dim3(128), (size_t)smem, st, g_pdl,
+                  partial, ldp, bias, x, g, b, eps, h, h_rows, rows, d, dev_err);
+}
+
+template <typename PT, typename OT>
+cudaError_t launch_resid_stream(int ng, const float *partial, int ldp, const PT *bias, float *x,
+                                const PT *g, const PT *b, float eps, OT *h, int h_rows, int rows,
+                                int d, int *dev_err, cudaStream_t st) {
+  switch (ng) {
+#define HE_RS_CASE(N)                                                                            \
+  case N:                                                                                        \
+    return launch_resid_stream_n<PT, OT, N>(partial, ldp, bias, x, g, b, eps, h, h_rows, rows, d, \
+                                            dev_err, st);
+    HE_RS_CASE(1) HE_RS_CASE(2) HE_RS_CASE(3) HE_RS_CASE(4) HE_RS_CASE(5) HE_RS_CASE(6)
+    HE_RS_CASE(7) HE_RS_CASE(8)
+#undef HE_RS_CASE
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const SliceInfo &si,
                             long long split_stride, int ldp, const void *bias, float *x,
                             const void *g, const void *b, float eps, void *h, int h_rows,
-                            int rows, int d, cudaStream_t st) {
+                            int rows, int d, cudaStream_t st, int *dev_err) {
   if (rows <= 0) return cudaSuccess;
   if (d % 4 || ldp % 4 || split_stride % 4 || (uintptr_t)partial % 16 || (uintptr_t)x % 16)
     return cudaErrorInvalidValue;
@@ -823,7 +963,13 @@ cudaError_t launch_resid_ln(int dtype, int out_act, const float *partial, const 
   // many rows (prefill): four warps per row, up to 8 groups of 1024 elements
   const int ng = d / 1024;
   const bool rows4 = reg8 && rows >= 2048 && d % 1024 == 0 && ng >= 1 && ng <= 8;
+  // one slice (the prefill GEMMs): rows streamed into shared memory by bulk copies
+  const bool stream1 = rows4 && si.split == 1 && si.sk_U == 0 && ldp % 4 == 0;
   HE_DISPATCH_PT_CT(dtype, out_act, {
+    if (stream1)
+      return launch_resid_stream<PT, CT>(ng, partial, ldp, (const PT *)bias, x, (const PT *)g,
+                                         (const PT *)b, eps, (CT *)h, h_rows, rows, d, dev_err,
+                                         st);
     if (rows4)
       return launch_resid_rows<PT, CT>(ng, partial, si, split_stride, ldp, (const PT *)bias, x,
                                        (const PT *)g, (const PT *)b, eps, (CT *)h, h_rows, rows,
