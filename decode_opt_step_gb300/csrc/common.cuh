@@ -163,6 +163,24 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
       : "memory");
 }
 
+// 2-D tiled TMA load multicast to the CTAs of the cluster in `mask`: the box lands at
+// the same shared-memory offset in each, and each one's mbarrier at `bar`'s offset
+// counts the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const void *tmap, uint64_t *bar,
+                                               int c0, int c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
+// All threads of all CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completion counted on `bar`.
 // L2 policy for data read exactly once (streamed weights): evicted first, so that
@@ -259,6 +277,16 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// As tc_commit, arriving on the mbarrier at `bar`'s offset in each CTA of the cluster
+// in `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
       : "memory");
 }
 

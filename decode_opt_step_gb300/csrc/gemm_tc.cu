@@ -223,7 +223,11 @@ __host__ __device__ inline void tcp_tile(long long L, int MT, int NT, int *mt, i
   *nt = (int)g * kTokGroup + (int)(rem % gnt);
 }
 
-template <typename CT, bool ABULK>
+// PAIR: CTAs run in clusters of two on weight tiles 2m and 2m + 1 of the same token
+// tile; each loads its own weight tile and half of the token tile, multicast into both
+// CTAs' shared memory, so the pair reads the activations from L2 once, and each MMA
+// releases a stage in both CTAs (multicast commit).
+template <typename CT, bool ABULK, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tcp(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x,
@@ -244,13 +248,20 @@ __global__ void __launch_bounds__(192, 1)
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = gridDim.x, c = blockIdx.x;
-  const long long T = (long long)MT * NT;
+  const int rank = PAIR ? (int)(blockIdx.x & 1) : 0;  // rank in the cluster of two
+  const int P = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int c = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int MTL = PAIR ? MT / 2 : MT;  // weight tiles (pairs of tiles) in the tile order
+  const long long T = (long long)MTL * NT;
+  auto tile_of = [&](long long L, int *mt, int *nt) {
+    tcp_tile(L, MTL, NT, mt, nt);
+    if (PAIR) *mt = 2 * *mt + rank;
+  };
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);  // the MMAs of both CTAs read a stage's token half
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -265,6 +276,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before anything targets them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
@@ -282,7 +294,7 @@ __global__ void __launch_bounds__(192, 1)
     bool stop = false;
     for (long long L = c; L < T && !stop; L += P) {
       int mt, nt;
-      tcp_tile(L, MT, NT, &mt, &nt);
+      tile_of(L, &mt, &nt);
       const int group = mt / tiles_per_group;
       const CUtensorMap *tw = group == 0 ? &tm_w0 : (group == 1 ? &tm_w1 : &tm_w2);
       const int m_row = (mt - group * tiles_per_group) * BM;
@@ -305,7 +317,11 @@ __global__ void __launch_bounds__(192, 1)
           bulk_load(smA + s * A_BYTES, wtile + (long long)kb * (BM * BK), A_BYTES, &full[s]);
         else
           tma_load_2d(smA + s * A_BYTES, tw, &full[s], kb * BK, m_row);
-        tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kb * BK, nt * PBN);
+        if (PAIR)  // this CTA's half of the token tile, into both CTAs
+          tma_load_2d_mc(smB + s * C::B_BYTES + rank * (C::B_BYTES / 2), &tm_x, &full[s],
+                         kb * BK, nt * PBN + rank * (PBN / 2), 0x3);
+        else
+          tma_load_2d(smB + s * C::B_BYTES, &tm_x, &full[s], kb * BK, nt * PBN);
         issued = it + 1;
       }
     }
@@ -345,7 +361,10 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < BK / UMMA_K; ++kk)
           tc_mma_f16(acc, sdesc_sw128(a0 + kk * UMMA_K * 2), sdesc_sw128(b0 + kk * UMMA_K * 2),
                      idesc, (kb | kk) != 0);
-        tc_commit(&empty[s]);
+        if (PAIR)
+          tc_commit_mc(&empty[s], 0x3);
+        else
+          tc_commit(&empty[s]);
       }
       tc_commit(&acc_full[buf]);  // also issued on abort so the epilogue is released
     }
@@ -358,7 +377,7 @@ __global__ void __launch_bounds__(192, 1)
     for (long long L = c; L < T; L += P, ++tcount) {
       if (*(volatile int *)abort_flag) break;
       int mt, nt;
-      tcp_tile(L, MT, NT, &mt, &nt);
+      tile_of(L, &mt, &nt);
       const int buf = tcount & 1;
       const bool ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)((tcount >> 1) & 1));
       if (!ok) {
@@ -390,6 +409,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal or fill it
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
@@ -464,7 +484,7 @@ cudaError_t launch_bn(const GemmArgs &a, int *dev_err, cudaStream_t st) {
                   dev_err);
 }
 
-template <typename CT, bool ABULK>
+template <typename CT, bool ABULK, bool PAIR>
 cudaError_t launch_tcp(const GemmArgs &a, int num_sms, int *dev_err, cudaStream_t st) {
   using C = Cfg<PBN, PSTAGES>;
   CUtensorMap tw[3], tx;
@@ -481,16 +501,48 @@ cudaError_t launch_tcp(const GemmArgs &a, int num_sms, int *dev_err, cudaStream_
   wt.group_rows = a.group_rows;
   if (a.w_scale[0])
     for (int g = 0; g < 3; ++g) wt.scale[g] = a.w_scale[g < a.n_groups ? g : 0];
-  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, PBN, tmap_type<CT>())) return cudaErrorInvalidValue;
-  cudaError_t ae = ensure_smem_limit<k_gemm_tcp<CT, ABULK>>(C::SMEM);
+  if (!make_tmap(&tx, a.x, a.M, a.K, a.ldx, PAIR ? PBN / 2 : PBN, tmap_type<CT>()))
+    return cudaErrorInvalidValue;
+  cudaError_t ae = ensure_smem_limit<k_gemm_tcp<CT, ABULK, PAIR>>(C::SMEM);
   if (ae != cudaSuccess) return ae;
   const int kb_total = (a.K + BK - 1) / BK;
   const int tiles_per_group = a.n_groups > 1 ? a.group_rows / BM : (1 << 30);
   const int MT = a.N / BM + (a.N % BM != 0), NT = (a.M + PBN - 1) / PBN;
+  if (PAIR) {
+    // as many clusters as can be resident at once (a cluster's two CTAs share a GPC)
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int &mc = max_clusters[dev & 63];
+    if (!mc) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(num_sms);
+      qc.blockDim = dim3(192);
+      qc.dynamicSmemBytes = C::SMEM;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tcp<CT, ABULK, PAIR>, &qc) != cudaSuccess ||
+          n <= 0)
+        return cudaErrorInvalidValue;
+      mc = n;
+    }
+    const long long T = (long long)(MT / 2) * NT;
+    const int P = (int)(T < mc ? T : mc);
+    return launch_k_cluster2(k_gemm_tcp<CT, ABULK, PAIR>, dim3(2 * P), dim3(192), C::SMEM, st,
+                             g_pdl, tw[0], tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total,
+                             MT, NT, a.epi, wt, dev_err);
+  }
   const long long T = (long long)MT * NT;
   const int P = (int)(T < num_sms ? T : num_sms);
-  return launch_k(k_gemm_tcp<CT, ABULK>, dim3(P), dim3(192), C::SMEM, st, g_pdl, tw[0], tw[1],
-                  tw[2], tx, tiles_per_group, a.M, a.N, kb_total, MT, NT, a.epi, wt, dev_err);
+  return launch_k(k_gemm_tcp<CT, ABULK, PAIR>, dim3(P), dim3(192), C::SMEM, st, g_pdl, tw[0],
+                  tw[1], tw[2], tx, tiles_per_group, a.M, a.N, kb_total, MT, NT, a.epi, wt,
+                  dev_err);
 }
 
 int device_sms() {
@@ -568,9 +620,16 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, int *dev_err, cudaStream_t st) {
   const bool persist = a.split == 1 && a.M > PBN && sms > 0;
   auto pick = [&](auto ct) -> cudaError_t {
     using CT = decltype(ct);
-    if (persist)
-      return a.w_tiled ? launch_tcp<CT, true>(a, sms, dev_err, st)
-                       : launch_tcp<CT, false>(a, sms, dev_err, st);
+    if (persist) {
+      // clusters of two sharing each token tile when the weight tiles pair up
+      const int MT = a.N / BM + (a.N % BM != 0);
+      const bool pair = MT % 2 == 0;
+      if (pair)
+        return a.w_tiled ? launch_tcp<CT, true, true>(a, sms, dev_err, st)
+                         : launch_tcp<CT, false, true>(a, sms, dev_err, st);
+      return a.w_tiled ? launch_tcp<CT, true, false>(a, sms, dev_err, st)
+                       : launch_tcp<CT, false, false>(a, sms, dev_err, st);
+    }
     if (a.w_tiled) {
       if (a.M <= 16) return launch_bn<CT, 16, 10, true>(a, dev_err, st);
       if (a.M <= 32) return launch_bn<CT, 32, 9, true>(a, dev_err, st);
