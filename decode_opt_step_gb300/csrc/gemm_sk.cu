@@ -686,6 +686,12 @@ int sk_ctas(const GemmArgs &g, int num_sms, bool fixup) {
   if (!fixup && T <= num_sms && 10 * T >= 7LL * num_sms) return (int)T;
   long long P = num_sms;
   if (P > U) P = U;
+  if (U < 2 * P) {
+    // under two units a run: the longest runs set the time, so give every run that many
+    // and use fewer runs (fewer slices to add, fewer fix-ups)
+    const long long per = (U + P - 1) / P;
+    P = (U + per - 1) / per;
+  }
   if (P > 15 * T) P = 15 * T;
   return (int)P;
 }
