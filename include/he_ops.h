@@ -80,7 +80,9 @@ he_status he_op_tile_weight(const void *w, void *out, int N, int K, void *stream
  * out = W + scale * B A (fp32 arithmetic, one rounding to fp16) in the tiled
  * streaming layout above (fp16 elements).  w: bf16 [N][K] (N % 128 == 0, K % 64 ==
  * 0); lora_a: bf16 [r][K], lora_b: bf16 [N][r] (r = 0: no delta, w converted to
- * fp16).  For tests and profiling.  Asynchronous on `stream`. */
+ * fp16; 0 <= r <= 64).  For r = 8 or 16 with 16-byte-aligned factors the product B A
+ * runs on the tensor cores (exact products, fp32 sums), otherwise as fp32 fused
+ * multiply-adds in j order.  For tests and profiling.  Asynchronous on `stream`. */
 he_status he_op_fuse_tiled(const void *w, const void *lora_a, const void *lora_b, int r, float scale,
                            void *out, int N, int K, void *stream);
 
