@@ -58,7 +58,7 @@ template <> struct Vec16<float> {
 };
 
 template <typename T, int HD, int UNROLL>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 7)  // 72 registers, seven CTAs (28 warps) per SM
     k_attn_decode(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
                   T *__restrict__ ctx, int ctx_rows, int H, int max_seq, int n_keys, int per_split,
                   float *__restrict__ part, int *__restrict__ cnt) {
