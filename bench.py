@@ -442,7 +442,7 @@ def main():
     # captured launch: k_attn_decode at B=128, 40 heads, 384 keys (the average decode
     # launch here) and k_gemm_sk on the fc1 shape as the engine launches it (a decode
     # step of the two-layer OPT-13B-shape workload).  Set to None when the kernel changes.
-    traffic_ratio = {"attn_decode": (1.007987e9 + 4.402432e6) / 1.00663296e9,
+    traffic_ratio = {"attn_decode": (1.007984e9 + 4.334592e6) / 1.00663296e9,
                      "gemm": (211.179264e6 + 6.607872e6) / 209.7152e6}
     if args.weights != "f16":
         traffic_ratio.pop("gemm")  # captured on the 16-bit kernel only
